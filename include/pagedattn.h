@@ -1,0 +1,168 @@
+/*
+ * pagedattn.h -- C ABI of libpagedattn, a unified paged-attention forward pass
+ * for NVIDIA GB300 (sm_103a).
+ *
+ * The operation.  For every sequence b of a batch and every new query token i
+ * of it, and every query head h:
+ *
+ *     out[t, h, :] = softmax_j( scale * <q[t, h, :], K_b[j, h / G, :]> ) . V_b[j, h / G, :]
+ *
+ * over the keys j = 0 .. p that the token may see, where t = query_start_loc[b] + i,
+ * p = seq_lens[b] - n_b + i (the n_b new tokens are the last n_b positions of
+ * the sequence, so the causal mask is bottom-right aligned) and G = Hq / Hkv.
+ * This is scaled dot-product attention as defined on the GPU programming guide
+ * page ("From megabytes to megawatts: a full guide to high-performance LLM and
+ * diffusion kernels with CUDA and Triton", section "Decomposing multi-head
+ * attention (MHA)"), masked causally as in its section "Flash Attention in
+ * Triton" (future tokens get -inf).  K_b and V_b are read through the block table
+ * from a paged KV cache, and query heads that share a KV head are computed
+ * together (Q-Block), as the Triton unified-attention page describes ("One line
+ * of Triton code beats both NVIDIA and AMD ...", papers.ananclaw.com, section
+ * "What three things the IBM paper got right", second item, the five-step list).
+ * Decode (n_b = 1) and chunked-prefill (n_b > 1) sequences may be mixed in one
+ * call.  Long key ranges are split across SMs and the partial results merged by
+ * log-sum-exp ("Parallel Tiled Softmax", same list), using the online-softmax
+ * recurrence of the guide's section "The Flash Attention revolution".
+ *
+ * Layouts (all row-major and contiguous; element counts, not bytes):
+ *   q               [T, Hq, D]        bf16    T = query_start_loc[B]
+ *   k_cache,v_cache [NB, P, Hkv, D]   bf16    token-major pages: the D values of
+ *                                             one token of one KV head are
+ *                                             contiguous
+ *   block_table     [B, max_pages]    int32   logical page -> physical page
+ *   seq_lens        [B]               int32   L_b: cached prefix + new tokens
+ *   query_start_loc [B + 1]           int32   0 = qsl[0] <= qsl[1] <= ... = T
+ *   out             [T, Hq, D]        bf16    written for every query row
+ * Logical position j of sequence b is slot j % P of physical page
+ * block_table[b][j / P].  Entries of block_table past a sequence's last page are
+ * never read.
+ *
+ * Pointers.  Every data pointer is a DEVICE pointer on the current CUDA device
+ * (the one the stream belongs to).  q, k_cache, v_cache and out must be 16-byte
+ * aligned; the int32 arrays 4-byte aligned.  The caller owns all of them; the
+ * library keeps none after a call returns.
+ *
+ * Streams and graphs.  Every call is asynchronous on the given stream
+ * (a cudaStream_t passed as void*; NULL is the legacy default stream).  No call
+ * of pa_forward reads device memory on the host or synchronises, and its launch
+ * grids depend only on the pa_dims, so it can be captured in a CUDA graph and
+ * replayed with new contents of the same buffers (the "static launch grid" and
+ * "CUDA / HIP Graphs" items of the same five-step list).
+ *
+ * Scratch memory.  Splitting a long key range needs a workspace of
+ * pa_plan(...).workspace_bytes bytes, which the library allocates and caches per
+ * (device, stream).  It grows on demand outside graph capture; inside capture it
+ * cannot, so call pa_prepare with the largest dims first.  Buffers are kept until
+ * pa_release_workspaces, so graphs that captured them stay valid.
+ *
+ * Errors.  Functions return a pa_status and never abort or throw.  Argument
+ * checks are done on the host before any launch; on failure nothing is
+ * launched and pa_last_error() (per thread) says why.  Values that live on the
+ * device (block ids, lengths) are the caller's contract; the kernels check them
+ * anyway, never access memory outside the buffers because of them, and record
+ * the first violation in a sticky per-stream error word (pa_device_error).
+ */
+#ifndef PAGEDATTN_H_
+#define PAGEDATTN_H_
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    PA_OK = 0,
+    PA_ERR_INVALID_ARG = 1,   /* bad pointer, shape, alignment or option      */
+    PA_ERR_UNSUPPORTED = 2,   /* valid but not built: head_dim, page size ...  */
+    PA_ERR_NOT_PREPARED = 3,  /* workspace too small while the stream captures */
+    PA_ERR_CUDA = 4,          /* a CUDA runtime call failed (see pa_last_error) */
+} pa_status;
+
+/* Shapes of one call.  head_dim must be 64 or 128 and page_size 16; any
+ * num_q_heads that is a multiple of num_kv_heads is accepted. */
+typedef struct {
+    int64_t num_tokens;    /* T: rows of q and out (= query_start_loc[B])        */
+    int64_t num_blocks;    /* NB: pages in each of k_cache and v_cache           */
+    int32_t num_seqs;      /* B                                                  */
+    int32_t num_q_heads;   /* Hq                                                 */
+    int32_t num_kv_heads;  /* Hkv                                                */
+    int32_t head_dim;      /* D                                                  */
+    int32_t page_size;     /* P                                                  */
+    int32_t max_pages;     /* row length of block_table; max_pages * P bounds L_b */
+} pa_dims;
+
+/* Optional knobs, for tests and the offline sweep.  Zero-initialise. */
+typedef struct {
+    int32_t kv_chunk;  /* 0: from the tuned table; else keys per split (multiple
+                          of page_size); a chunk >= max_pages * P means no split */
+    int32_t reserved;
+    /* cudaEvent_t handles recorded on the stream immediately before and after
+       the decode kernel and the prefill kernel (NULL: not recorded). */
+    void* decode_start_event;
+    void* decode_stop_event;
+    void* prefill_start_event;
+    void* prefill_stop_event;
+} pa_options;
+
+/* What a call with these dims launches (host-only; no device work). */
+typedef struct {
+    int32_t kv_chunk;         /* keys per split                                */
+    int32_t splits;           /* splits of the longest possible sequence       */
+    int64_t decode_ctas;      /* decode kernel grid                            */
+    int64_t combine_ctas;     /* log-sum-exp combine kernel grid (0 if unused)  */
+    int64_t prefill_ctas;     /* prefill kernel grid                           */
+    int64_t workspace_bytes;  /* scratch this call needs                       */
+    int32_t launches;         /* kernels launched per pa_forward               */
+    int32_t reserved;
+} pa_plan_info;
+
+/*
+ * The forward pass.  Computes out for every query row of the batch (see the top
+ * of this file).  scale multiplies the dot products (typically 1/sqrt(D)).
+ * Returns PA_OK after enqueuing the kernels on stream; PA_ERR_* otherwise,
+ * without launching anything.  Zero sequences or zero tokens is a no-op.
+ */
+pa_status pa_forward(const void* q, const void* k_cache, const void* v_cache,
+                     const int32_t* block_table, const int32_t* seq_lens,
+                     const int32_t* query_start_loc, void* out, float scale,
+                     const pa_dims* dims, void* stream);
+
+/* pa_forward with options (opts may be NULL). */
+pa_status pa_forward_ex(const void* q, const void* k_cache, const void* v_cache,
+                        const int32_t* block_table, const int32_t* seq_lens,
+                        const int32_t* query_start_loc, void* out, float scale,
+                        const pa_dims* dims, const pa_options* opts, void* stream);
+
+/* Fills *info with the launch plan for dims (host only).  The split size comes
+ * from the table an offline sweep produced, keyed on the context bound
+ * (max_pages * page_size) and the batch size: the "offline micro-benchmarks ->
+ * decision tree" of the same page's third section, with no tuning at run time. */
+pa_status pa_plan(const pa_dims* dims, const pa_options* opts, pa_plan_info* info);
+
+/* Allocates (outside any capture) the workspace a pa_forward with these dims and
+ * options needs on stream, so that the call can then be captured. */
+pa_status pa_prepare(const pa_dims* dims, const pa_options* opts, void* stream);
+
+/* Synchronises stream, then returns the stream's sticky device error code in
+ * *code (0 = none; 1 bad block id; 2 seq_len above max_pages * page_size;
+ * 3 more new tokens than seq_len; 4 a bounded wait gave up; 5 query_start_loc
+ * outside [0, num_tokens]) and clears it.  Rows the check skipped are not written. */
+pa_status pa_device_error(void* stream, int32_t* code);
+
+/* Frees every cached workspace on every device.  No graph that captured a
+ * pa_forward may be replayed afterwards. */
+pa_status pa_release_workspaces(void);
+
+/* Static text for a status, and this thread's last error detail. */
+const char* pa_status_string(pa_status status);
+const char* pa_last_error(void);
+
+/* Library version, major * 10000 + minor * 100 + patch. */
+int32_t pa_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* PAGEDATTN_H_ */

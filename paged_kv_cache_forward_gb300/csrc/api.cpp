@@ -1,0 +1,339 @@
+// api.cpp -- the C ABI of libpagedattn (declared in include/pagedattn.h):
+// host-side argument checks, the launch plan (split size from the tuned table),
+// the per-(device, stream) workspace cache, and the kernel launches.
+
+#include <cuda_runtime.h>
+
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <mutex>
+#include <vector>
+
+#include "pa_internal.h"
+#include "pagedattn.h"
+
+namespace {
+
+thread_local char g_last_error[512] = "";
+
+pa_status fail(pa_status st, const char* fmt, ...) __attribute__((format(printf, 2, 3)));
+pa_status fail(pa_status st, const char* fmt, ...) {
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(g_last_error, sizeof g_last_error, fmt, ap);
+    va_end(ap);
+    return st;
+}
+
+pa_status cuda_fail(cudaError_t e, const char* what) {
+    return fail(PA_ERR_CUDA, "%s: %s (%s)", what, cudaGetErrorName(e), cudaGetErrorString(e));
+}
+
+// ---------------------------------------------------------------- split table
+// Keys per split, picked from the context bound (max_pages * page_size) and the
+// number of sequences, as measured by the offline sweep (lut_gb300.inc).
+struct LutEntry {
+    int32_t max_bound;  // applies when context bound <= max_bound
+    int32_t max_seqs;   // ... and num_seqs <= max_seqs
+    int32_t kv_chunk;
+};
+#include "lut_gb300.inc"
+
+int32_t table_chunk(int64_t bound, int32_t num_seqs) {
+    for (const LutEntry& e : kSplitTable)
+        if (bound <= e.max_bound && num_seqs <= e.max_seqs) return e.kv_chunk;
+    return kSplitTable[sizeof(kSplitTable) / sizeof(kSplitTable[0]) - 1].kv_chunk;
+}
+
+// ----------------------------------------------------------------- validation
+constexpr int64_t kMaxCtas = 0x7fffffffLL;
+
+bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
+
+pa_status check_dims(const pa_dims* d) {
+    if (!d) return fail(PA_ERR_INVALID_ARG, "dims is NULL");
+    if (d->num_tokens < 0 || d->num_seqs < 0) return fail(PA_ERR_INVALID_ARG, "negative num_tokens or num_seqs");
+    if (d->num_q_heads <= 0 || d->num_kv_heads <= 0)
+        return fail(PA_ERR_INVALID_ARG, "num_q_heads and num_kv_heads must be positive");
+    if (d->num_q_heads % d->num_kv_heads != 0)
+        return fail(PA_ERR_INVALID_ARG, "num_q_heads (%d) is not a multiple of num_kv_heads (%d)", d->num_q_heads,
+                    d->num_kv_heads);
+    if (d->head_dim != 64 && d->head_dim != 128)
+        return fail(PA_ERR_UNSUPPORTED, "head_dim %d not built (64, 128)", d->head_dim);
+    if (d->page_size != 16) return fail(PA_ERR_UNSUPPORTED, "page_size %d not built (16)", d->page_size);
+    if (d->num_q_heads / d->num_kv_heads > 64)
+        return fail(PA_ERR_UNSUPPORTED, "more than 64 query heads per KV head");
+    if (d->num_blocks <= 0) return fail(PA_ERR_INVALID_ARG, "num_blocks must be positive");
+    if (d->max_pages <= 0) return fail(PA_ERR_INVALID_ARG, "max_pages must be positive");
+    if (static_cast<int64_t>(d->max_pages) * d->page_size > 0x7fffffffLL)
+        return fail(PA_ERR_INVALID_ARG, "max_pages * page_size overflows int32");
+    if (d->num_tokens > 0x7fffffffLL) return fail(PA_ERR_UNSUPPORTED, "more than 2^31-1 tokens");
+    if (d->num_seqs > 0 && d->num_tokens == 0) return PA_OK;
+    return PA_OK;
+}
+
+struct Plan {
+    int32_t kv_chunk = 0, splits = 0, row_groups = 0;
+    int64_t decode_ctas = 0, combine_ctas = 0, prefill_ctas = 0, ws_bytes = 0;
+    int32_t launches = 0;
+    pa::Args args{};
+};
+
+constexpr int64_t kErrWordBytes = 256;  // the sticky error word lives at the workspace start
+
+pa_status make_plan(const pa_dims* d, const pa_options* o, Plan* p) {
+    pa_status st = check_dims(d);
+    if (st != PA_OK) return st;
+    const int64_t bound = static_cast<int64_t>(d->max_pages) * d->page_size;
+    int64_t chunk = (o && o->kv_chunk) ? o->kv_chunk : table_chunk(bound, d->num_seqs);
+    if (chunk < d->page_size || chunk % d->page_size)
+        return fail(PA_ERR_INVALID_ARG, "kv_chunk %lld must be a positive multiple of page_size",
+                    static_cast<long long>(chunk));
+    if (chunk > bound) chunk = bound;
+    const int32_t group = d->num_q_heads / d->num_kv_heads;
+    pa::Args& a = p->args;
+    a.num_tokens = d->num_tokens;
+    a.num_blocks = d->num_blocks;
+    a.num_seqs = d->num_seqs;
+    a.num_q_heads = d->num_q_heads;
+    a.num_kv_heads = d->num_kv_heads;
+    a.group = group;
+    a.head_dim = d->head_dim;
+    a.page_size = d->page_size;
+    a.max_pages = d->max_pages;
+    a.kv_chunk = static_cast<int32_t>(chunk);
+    a.splits = static_cast<int32_t>((bound + chunk - 1) / chunk);
+    a.row_groups = (group + 15) / 16;
+    p->kv_chunk = a.kv_chunk;
+    p->splits = a.splits;
+    p->row_groups = a.row_groups;
+    if (d->num_seqs == 0 || d->num_tokens == 0) {
+        p->ws_bytes = 0;
+        return PA_OK;
+    }
+    p->decode_ctas = pa::decode_ctas(a);
+    p->combine_ctas = pa::combine_ctas(a);
+    p->prefill_ctas = pa::prefill_ctas(a);
+    if (p->decode_ctas > kMaxCtas || p->combine_ctas > kMaxCtas || p->prefill_ctas > kMaxCtas)
+        return fail(PA_ERR_UNSUPPORTED, "launch grid above 2^31-1 CTAs; use a larger kv_chunk");
+    p->launches = (p->decode_ctas > 0) + (p->combine_ctas > 0) + (p->prefill_ctas > 0);
+    const int64_t partial_rows = a.splits > 1 ? static_cast<int64_t>(d->num_seqs) * a.splits * d->num_q_heads : 0;
+    p->ws_bytes = kErrWordBytes + partial_rows * d->head_dim * 4 + partial_rows * 2 * 4;
+    return PA_OK;
+}
+
+// --------------------------------------------------------- workspace cache
+struct Workspace {
+    int device;
+    cudaStream_t stream;
+    void* ptr;
+    int64_t bytes;
+};
+
+std::mutex g_ws_mutex;
+std::vector<Workspace> g_ws;       // live, one per (device, stream)
+std::vector<Workspace> g_retired;  // outgrown buffers, kept for captured graphs
+
+// Returns the workspace of (device, stream) with at least `bytes`, growing it if
+// allowed.  The error word at its start is zeroed whenever a buffer is created.
+pa_status get_workspace(cudaStream_t stream, int64_t bytes, bool may_grow, void** out) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+    std::lock_guard<std::mutex> lock(g_ws_mutex);
+    Workspace* w = nullptr;
+    for (Workspace& x : g_ws)
+        if (x.device == dev && x.stream == stream) w = &x;
+    if (w && w->bytes >= bytes) {
+        *out = w->ptr;
+        return PA_OK;
+    }
+    if (!may_grow)
+        return fail(PA_ERR_NOT_PREPARED,
+                    "workspace of %lld bytes needed while the stream is capturing; call pa_prepare first",
+                    static_cast<long long>(bytes));
+    void* p = nullptr;
+    e = cudaMalloc(&p, static_cast<size_t>(bytes));
+    if (e != cudaSuccess) return cuda_fail(e, "cudaMalloc(workspace)");
+    e = cudaMemsetAsync(p, 0, kErrWordBytes, stream);
+    if (e == cudaSuccess && w) {
+        // carry the old sticky error over, then retire the old buffer
+        e = cudaMemcpyAsync(p, w->ptr, sizeof(int32_t), cudaMemcpyDeviceToDevice, stream);
+    }
+    if (e != cudaSuccess) {
+        cudaFree(p);
+        return cuda_fail(e, "workspace init");
+    }
+    if (w) {
+        g_retired.push_back(*w);
+        w->ptr = p;
+        w->bytes = bytes;
+    } else {
+        g_ws.push_back(Workspace{dev, stream, p, bytes});
+    }
+    *out = p;
+    return PA_OK;
+}
+
+pa_status check_pointers(const void* q, const void* k, const void* v, const int32_t* bt, const int32_t* sl,
+                         const int32_t* qsl, const void* out) {
+    if (!q || !k || !v || !bt || !sl || !qsl || !out) return fail(PA_ERR_INVALID_ARG, "NULL data pointer");
+    if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(out, 16))
+        return fail(PA_ERR_INVALID_ARG, "q, k_cache, v_cache and out must be 16-byte aligned");
+    if (!aligned(bt, 4) || !aligned(sl, 4) || !aligned(qsl, 4))
+        return fail(PA_ERR_INVALID_ARG, "block_table, seq_lens and query_start_loc must be 4-byte aligned");
+    return PA_OK;
+}
+
+// Records a caller's timing event.  Inside stream capture the record must be an
+// external one, so that replaying the graph records the event again.
+pa_status record(void* ev, cudaStream_t s, bool capturing) {
+    if (!ev) return PA_OK;
+    cudaError_t e = cudaEventRecordWithFlags(static_cast<cudaEvent_t>(ev), s,
+                                             capturing ? cudaEventRecordExternal : cudaEventRecordDefault);
+    return e == cudaSuccess ? PA_OK : cuda_fail(e, "cudaEventRecord");
+}
+
+}  // namespace
+
+extern "C" {
+
+pa_status pa_plan(const pa_dims* dims, const pa_options* opts, pa_plan_info* info) {
+    if (!info) return fail(PA_ERR_INVALID_ARG, "info is NULL");
+    Plan p;
+    pa_status st = make_plan(dims, opts, &p);
+    if (st != PA_OK) return st;
+    info->kv_chunk = p.kv_chunk;
+    info->splits = p.splits;
+    info->decode_ctas = p.decode_ctas;
+    info->combine_ctas = p.combine_ctas;
+    info->prefill_ctas = p.prefill_ctas;
+    info->workspace_bytes = p.ws_bytes;
+    info->launches = p.launches;
+    info->reserved = 0;
+    return PA_OK;
+}
+
+pa_status pa_prepare(const pa_dims* dims, const pa_options* opts, void* stream) {
+    Plan p;
+    pa_status st = make_plan(dims, opts, &p);
+    if (st != PA_OK) return st;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+    cudaError_t e = cudaStreamIsCapturing(s, &cs);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaStreamIsCapturing");
+    if (cs != cudaStreamCaptureStatusNone) return fail(PA_ERR_INVALID_ARG, "pa_prepare called during capture");
+    void* ws = nullptr;
+    return get_workspace(s, p.ws_bytes > kErrWordBytes ? p.ws_bytes : kErrWordBytes, true, &ws);
+}
+
+pa_status pa_forward_ex(const void* q, const void* k_cache, const void* v_cache, const int32_t* block_table,
+                        const int32_t* seq_lens, const int32_t* query_start_loc, void* out, float scale,
+                        const pa_dims* dims, const pa_options* opts, void* stream) {
+    Plan p;
+    pa_status st = make_plan(dims, opts, &p);
+    if (st != PA_OK) return st;
+    if (dims->num_seqs == 0 || dims->num_tokens == 0) return PA_OK;
+    st = check_pointers(q, k_cache, v_cache, block_table, seq_lens, query_start_loc, out);
+    if (st != PA_OK) return st;
+    if (!(scale == scale)) return fail(PA_ERR_INVALID_ARG, "scale is NaN");
+
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+    cudaError_t e = cudaStreamIsCapturing(s, &cs);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaStreamIsCapturing");
+    void* ws = nullptr;
+    st = get_workspace(s, p.ws_bytes, cs == cudaStreamCaptureStatusNone, &ws);
+    if (st != PA_OK) return st;
+
+    pa::Args a = p.args;
+    a.q = q;
+    a.k_cache = k_cache;
+    a.v_cache = v_cache;
+    a.block_table = block_table;
+    a.seq_lens = seq_lens;
+    a.query_start_loc = query_start_loc;
+    a.out = out;
+    a.err = static_cast<int32_t*>(ws);
+    float* partials = reinterpret_cast<float*>(static_cast<char*>(ws) + kErrWordBytes);
+    const int64_t partial_rows = a.splits > 1 ? static_cast<int64_t>(a.num_seqs) * a.splits * a.num_q_heads : 0;
+    a.ws_o = partials;
+    a.ws_ml = partials + partial_rows * a.head_dim;
+    a.scale = scale;
+    a.scale_log2 = scale * 1.4426950408889634f;
+
+    const bool capturing = cs != cudaStreamCaptureStatusNone;
+    if ((st = record(opts ? opts->decode_start_event : nullptr, s, capturing)) != PA_OK) return st;
+    if ((e = pa::launch_decode(a, s)) != cudaSuccess) return cuda_fail(e, "decode launch");
+    if ((st = record(opts ? opts->decode_stop_event : nullptr, s, capturing)) != PA_OK) return st;
+    if ((e = pa::launch_combine(a, s)) != cudaSuccess) return cuda_fail(e, "combine launch");
+    if ((st = record(opts ? opts->prefill_start_event : nullptr, s, capturing)) != PA_OK) return st;
+    if ((e = pa::launch_prefill(a, s)) != cudaSuccess) return cuda_fail(e, "prefill launch");
+    if ((st = record(opts ? opts->prefill_stop_event : nullptr, s, capturing)) != PA_OK) return st;
+    return PA_OK;
+}
+
+pa_status pa_forward(const void* q, const void* k_cache, const void* v_cache, const int32_t* block_table,
+                     const int32_t* seq_lens, const int32_t* query_start_loc, void* out, float scale,
+                     const pa_dims* dims, void* stream) {
+    return pa_forward_ex(q, k_cache, v_cache, block_table, seq_lens, query_start_loc, out, scale, dims, nullptr,
+                         stream);
+}
+
+pa_status pa_device_error(void* stream, int32_t* code) {
+    if (!code) return fail(PA_ERR_INVALID_ARG, "code is NULL");
+    *code = 0;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    void* ws = nullptr;
+    pa_status st = get_workspace(s, kErrWordBytes, true, &ws);
+    if (st != PA_OK) return st;
+    cudaError_t e = cudaStreamSynchronize(s);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaStreamSynchronize");
+    int32_t v = 0;
+    e = cudaMemcpy(&v, ws, sizeof v, cudaMemcpyDeviceToHost);
+    if (e != cudaSuccess) return cuda_fail(e, "read error word");
+    if (v) {
+        const int32_t zero = 0;
+        e = cudaMemcpy(ws, &zero, sizeof zero, cudaMemcpyHostToDevice);
+        if (e != cudaSuccess) return cuda_fail(e, "clear error word");
+    }
+    *code = v;
+    return PA_OK;
+}
+
+pa_status pa_release_workspaces(void) {
+    std::lock_guard<std::mutex> lock(g_ws_mutex);
+    int cur = 0;
+    cudaGetDevice(&cur);
+    pa_status st = PA_OK;
+    auto drop = [&](std::vector<Workspace>& v) {
+        for (Workspace& w : v) {
+            cudaSetDevice(w.device);
+            cudaError_t e = cudaFree(w.ptr);
+            if (e != cudaSuccess && st == PA_OK) st = cuda_fail(e, "cudaFree(workspace)");
+        }
+        v.clear();
+    };
+    drop(g_ws);
+    drop(g_retired);
+    cudaSetDevice(cur);
+    return st;
+}
+
+const char* pa_status_string(pa_status status) {
+    switch (status) {
+        case PA_OK: return "ok";
+        case PA_ERR_INVALID_ARG: return "invalid argument";
+        case PA_ERR_UNSUPPORTED: return "unsupported configuration";
+        case PA_ERR_NOT_PREPARED: return "workspace not prepared before capture";
+        case PA_ERR_CUDA: return "CUDA error";
+    }
+    return "unknown status";
+}
+
+const char* pa_last_error(void) { return g_last_error; }
+
+int32_t pa_version(void) { return 100; }
+
+}  // extern "C"

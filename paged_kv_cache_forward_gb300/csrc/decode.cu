@@ -1,0 +1,315 @@
+// decode.cu -- GQA Q-block split-KV decode kernel.
+//
+// One CTA owns (sequence b, KV head h, row group rg, split s): the query heads
+// h*G + rg*16 .. +16 of b's single new token (the "Q-Block" item of the five-step
+// list on the Triton unified-attention page, section "What three things the IBM
+// paper got right": query heads sharing a KV head are computed together, so each
+// KV page is read once per KV head, not once per query head) against keys
+// [s*kv_chunk, min((s+1)*kv_chunk, L_b)) -- one tile of the "Parallel Tiled
+// Softmax" item of the same list.
+//
+// Inside the CTA, 4 warps take pages round-robin.  Each warp runs its own
+// 3-stage cp.async pipeline of one 16-token page of K and V (16-byte copies into
+// an XOR-swizzled layout, so the ldmatrix fragment loads are bank-conflict free),
+// computes S = Q K^T and O += P V with bf16 m16n8k16 MMAs (the G <= 16 query
+// rows padded to 16), and keeps an online softmax (running max m, sum l; the
+// recurrence of "The Flash Attention revolution" on the GPU programming guide
+// page) in the log2 domain.  At the end the 4 warps' (m, l, O) are merged in
+// shared memory; a sequence with one split writes bf16 out directly, otherwise
+// the unnormalised partial goes to the workspace for the combine kernel.
+//
+// HBM-bound: per CTA it streams (end - start) * D * 2 bytes of K and as many of
+// V, which is the whole algorithmic traffic of decode.  The contraction has only
+// G rows (4 for Llama), too few for a tcgen05 tile; the warp MMAs keep the
+// arithmetic well below the memory time.
+
+#include <cuda_bf16.h>
+
+#include "pa_device.cuh"
+#include "pa_internal.h"
+
+namespace pa {
+namespace {
+
+constexpr int kWarps = 4;
+constexpr int kStages = 3;
+constexpr int kPage = 16;
+constexpr int kRows = 16;  // MMA M: query-head rows per CTA
+
+template <int D>
+struct DecodeTile {
+    static constexpr int kRowBytes = D * 2;
+    static constexpr int kChunksPerRow = D / 8;                 // 16-byte chunks
+    static constexpr int kPageBytes = kPage * kRowBytes;        // K (or V) of one page, one head
+    static constexpr int kStageBytes = 2 * kPageBytes;          // K then V
+    static constexpr int kWarpBytes = kStages * kStageBytes;
+    static constexpr int kPipeBytes = kWarps * kWarpBytes;
+    // merge area: per warp O[16][D] fp32 + m[16] + l[16]
+    static constexpr int kMergeWarpFloats = kRows * D + 2 * kRows;
+    static constexpr int kMergeBytes = kWarps * kMergeWarpFloats * 4;
+    static constexpr int kSmemBytes = kPipeBytes > kMergeBytes ? kPipeBytes : kMergeBytes;
+};
+
+// Byte offset of 16-byte chunk c of row r: chunks are XOR-permuted by r % 8.
+template <int D>
+__device__ __forceinline__ uint32_t swz(int r, int c) {
+    return r * DecodeTile<D>::kRowBytes + ((c ^ (r & 7)) << 4);
+}
+
+template <int D>
+__global__ void __launch_bounds__(kWarps * 32) decode_splitkv_kernel(const Args a) {
+    using Tile = DecodeTile<D>;
+    extern __shared__ __align__(128) uint8_t smem[];
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    const int g = lane >> 2;   // MMA group id: row g and g + 8
+    const int tq = lane & 3;   // thread in quad: columns 2tq, 2tq + 1
+
+    int64_t idx = blockIdx.x;
+    const int s = static_cast<int>(idx % a.splits);
+    idx /= a.splits;
+    const int rg = static_cast<int>(idx % a.row_groups);
+    idx /= a.row_groups;
+    const int h = static_cast<int>(idx % a.num_kv_heads);
+    const int b = static_cast<int>(idx / a.num_kv_heads);
+
+    const int q0 = a.query_start_loc[b];
+    const int n = a.query_start_loc[b + 1] - q0;
+    if (n != 1) return;  // not a decode sequence (prefill kernel, or empty)
+    if (q0 < 0 || q0 >= a.num_tokens) {
+        flag_error(a.err, kDevBadQueryStart);
+        return;
+    }
+
+    const int cap = a.max_pages * kPage;
+    int L = a.seq_lens[b];
+    if (L > cap) {
+        flag_error(a.err, kDevSeqTooLong);
+        L = cap;
+    }
+    const int rows = min(kRows, a.group - rg * kRows);
+    const int hq0 = h * a.group + rg * kRows;
+    __nv_bfloat16* out = reinterpret_cast<__nv_bfloat16*>(a.out);
+    if (L < 1) {
+        // A query must see at least itself; the caller broke the contract.
+        if (s == 0) {
+            flag_error(a.err, kDevQueryTooLong);
+            for (int i = threadIdx.x; i < rows * D; i += blockDim.x)
+                out[(static_cast<int64_t>(q0) * a.num_q_heads + hq0 + i / D) * D + i % D] = __float2bfloat16(0.f);
+        }
+        return;
+    }
+    const int start = s * a.kv_chunk;
+    if (start >= L) return;
+    const int end = min(L, start + a.kv_chunk);
+    const int npages = (end - start + kPage - 1) / kPage;
+    const int nsplits = (L + a.kv_chunk - 1) / a.kv_chunk;
+    const int my_pages = warp < npages ? (npages - warp + kWarps - 1) / kWarps : 0;
+
+    // Q fragments for all D/16 k-steps; rows >= `rows` are zero.
+    const __nv_bfloat16* q = reinterpret_cast<const __nv_bfloat16*>(a.q);
+    const __nv_bfloat16* qg = q + (static_cast<int64_t>(q0) * a.num_q_heads + hq0 + g) * D;
+    const __nv_bfloat16* qg8 = qg + 8 * D;
+    const bool row_lo = g < rows, row_hi = g + 8 < rows;
+    uint32_t qa[D / 16][4];
+#pragma unroll
+    for (int ks = 0; ks < D / 16; ++ks) {
+        const int c = ks * 16 + 2 * tq;
+        qa[ks][0] = row_lo ? *reinterpret_cast<const uint32_t*>(qg + c) : 0u;
+        qa[ks][1] = row_hi ? *reinterpret_cast<const uint32_t*>(qg8 + c) : 0u;
+        qa[ks][2] = row_lo ? *reinterpret_cast<const uint32_t*>(qg + c + 8) : 0u;
+        qa[ks][3] = row_hi ? *reinterpret_cast<const uint32_t*>(qg8 + c + 8) : 0u;
+    }
+
+    const __nv_bfloat16* kc = reinterpret_cast<const __nv_bfloat16*>(a.k_cache);
+    const __nv_bfloat16* vc = reinterpret_cast<const __nv_bfloat16*>(a.v_cache);
+    const int32_t* bt = a.block_table + static_cast<int64_t>(b) * a.max_pages;
+    const uint32_t wbase = smem_u32(smem) + warp * Tile::kWarpBytes;
+    const uint64_t policy = policy_evict_first();
+
+    // Issue the copies of this warp's it-th page into stage it % kStages; always
+    // commit a group so that the wait count below stays uniform.
+    auto issue = [&](int it) {
+        if (it < my_pages) {
+            const int lp = start / kPage + warp + kWarps * it;
+            const int page = bt[lp];
+            const bool ok = static_cast<uint32_t>(page) < static_cast<uint64_t>(a.num_blocks);
+            if (!ok) flag_error(a.err, kDevBadBlock);
+            const int valid = ok ? min(kPage, end - lp * kPage) : 0;
+            const uint32_t st = wbase + (it % kStages) * Tile::kStageBytes;
+            const int64_t page_base = static_cast<int64_t>(ok ? page : 0) * kPage;
+#pragma unroll
+            for (int i = 0; i < Tile::kChunksPerRow / 2; ++i) {
+                const int c = lane + 32 * i;
+                const int r = c / Tile::kChunksPerRow;
+                const int cc = c % Tile::kChunksPerRow;
+                const int bytes = r < valid ? 16 : 0;
+                const int64_t off = ((page_base + (r < valid ? r : 0)) * a.num_kv_heads + h) * D + cc * 8;
+                cp_async_16_stream(st + swz<D>(r, cc), kc + off, bytes, policy);
+                cp_async_16_stream(st + Tile::kPageBytes + swz<D>(r, cc), vc + off, bytes, policy);
+            }
+        }
+        cp_async_commit();
+    };
+
+    float o[D / 8][4];
+#pragma unroll
+    for (int i = 0; i < D / 8; ++i) o[i][0] = o[i][1] = o[i][2] = o[i][3] = 0.f;
+    float m_lo = -INFINITY, m_hi = -INFINITY;  // running max (log2 units) of rows g, g+8
+    float l_lo = 0.f, l_hi = 0.f;              // this thread's share of the running sums
+
+#pragma unroll
+    for (int i = 0; i < kStages - 1; ++i) issue(i);
+
+    for (int it = 0; it < my_pages; ++it) {
+        issue(it + kStages - 1);
+        cp_async_wait<kStages - 1>();
+        __syncwarp();
+        const uint32_t sk = wbase + (it % kStages) * Tile::kStageBytes;
+        const uint32_t sv = sk + Tile::kPageBytes;
+
+        // S = Q K^T for the page's 16 tokens: two n-tiles of 8 tokens.
+        float sc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+        {
+            const int mi = lane >> 3;
+            const int tok = (mi >> 1) * 8 + (lane & 7);
+#pragma unroll
+            for (int ks = 0; ks < D / 16; ++ks) {
+                uint32_t k0, k1, k2, k3;
+                ldmatrix_x4(sk + swz<D>(tok, 2 * ks + (mi & 1)), k0, k1, k2, k3);
+                mma_bf16_16816(sc[0], qa[ks], k0, k1);
+                mma_bf16_16816(sc[1], qa[ks], k2, k3);
+            }
+        }
+        // Mask keys past the end of the split (only the sequence's last page is
+        // partial) and move to log2 units.
+        const int tok0 = (start / kPage + warp + kWarps * it) * kPage;
+#pragma unroll
+        for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                const int j = tok0 + nt * 8 + 2 * tq + (e & 1);
+                sc[nt][e] = j < end ? sc[nt][e] * a.scale_log2 : -INFINITY;
+            }
+        const float mx_lo = quad_max(fmaxf(fmaxf(sc[0][0], sc[0][1]), fmaxf(sc[1][0], sc[1][1])));
+        const float mx_hi = quad_max(fmaxf(fmaxf(sc[0][2], sc[0][3]), fmaxf(sc[1][2], sc[1][3])));
+        const float mn_lo = fmaxf(m_lo, mx_lo), mn_hi = fmaxf(m_hi, mx_hi);
+        const float mu_lo = mn_lo == -INFINITY ? 0.f : mn_lo;
+        const float mu_hi = mn_hi == -INFINITY ? 0.f : mn_hi;
+        const float al_lo = fast_exp2(m_lo - mu_lo), al_hi = fast_exp2(m_hi - mu_hi);
+        m_lo = mn_lo;
+        m_hi = mn_hi;
+
+        // P in bf16 as the A operand of P V; the sums use the same rounded P.
+        uint32_t pa[4];
+        pa[0] = pack_bf16(fast_exp2(sc[0][0] - mu_lo), fast_exp2(sc[0][1] - mu_lo));
+        pa[1] = pack_bf16(fast_exp2(sc[0][2] - mu_hi), fast_exp2(sc[0][3] - mu_hi));
+        pa[2] = pack_bf16(fast_exp2(sc[1][0] - mu_lo), fast_exp2(sc[1][1] - mu_lo));
+        pa[3] = pack_bf16(fast_exp2(sc[1][2] - mu_hi), fast_exp2(sc[1][3] - mu_hi));
+        l_lo = l_lo * al_lo + ((bf16_lo(pa[0]) + bf16_hi(pa[0])) + (bf16_lo(pa[2]) + bf16_hi(pa[2])));
+        l_hi = l_hi * al_hi + ((bf16_lo(pa[1]) + bf16_hi(pa[1])) + (bf16_lo(pa[3]) + bf16_hi(pa[3])));
+#pragma unroll
+        for (int i = 0; i < D / 8; ++i) {
+            o[i][0] *= al_lo;
+            o[i][1] *= al_lo;
+            o[i][2] *= al_hi;
+            o[i][3] *= al_hi;
+        }
+        // O += P V: V rows are tokens, so the B fragments come from transposed loads.
+        {
+            const int mi = lane >> 3;
+            const int tok = (mi & 1) * 8 + (lane & 7);
+#pragma unroll
+            for (int nd = 0; nd < D / 16; ++nd) {
+                uint32_t v0, v1, v2, v3;
+                ldmatrix_x4_trans(sv + swz<D>(tok, 2 * nd + (mi >> 1)), v0, v1, v2, v3);
+                mma_bf16_16816(o[2 * nd], pa, v0, v1);
+                mma_bf16_16816(o[2 * nd + 1], pa, v2, v3);
+            }
+        }
+        __syncwarp();
+    }
+    cp_async_wait<0>();
+    __syncthreads();
+
+    // Merge the 4 warps' partial softmax states in shared memory.
+    float* mw = reinterpret_cast<float*>(smem) + warp * Tile::kMergeWarpFloats;
+#pragma unroll
+    for (int i = 0; i < D / 8; ++i) {
+        const int c = i * 8 + 2 * tq;
+        mw[g * D + c] = o[i][0];
+        mw[g * D + c + 1] = o[i][1];
+        mw[(g + 8) * D + c] = o[i][2];
+        mw[(g + 8) * D + c + 1] = o[i][3];
+    }
+    l_lo = quad_sum(l_lo);
+    l_hi = quad_sum(l_hi);
+    if (tq == 0) {
+        mw[kRows * D + g] = m_lo;
+        mw[kRows * D + g + 8] = m_hi;
+        mw[kRows * D + kRows + g] = l_lo;
+        mw[kRows * D + kRows + g + 8] = l_hi;
+    }
+    __syncthreads();
+
+    const float* ms = reinterpret_cast<const float*>(smem);
+    for (int i = threadIdx.x; i < rows * D; i += blockDim.x) {
+        const int r = i / D, d = i % D;
+        float M = -INFINITY;
+#pragma unroll
+        for (int w = 0; w < kWarps; ++w) M = fmaxf(M, ms[w * Tile::kMergeWarpFloats + kRows * D + r]);
+        float acc = 0.f, l = 0.f;
+#pragma unroll
+        for (int w = 0; w < kWarps; ++w) {
+            const float* mwr = ms + w * Tile::kMergeWarpFloats;
+            const float mwv = mwr[kRows * D + r];
+            const float sc = mwv == -INFINITY ? 0.f : fast_exp2(mwv - M);
+            acc += sc * mwr[r * D + d];
+            l += sc * mwr[kRows * D + kRows + r];
+        }
+        if (nsplits == 1) {
+            out[(static_cast<int64_t>(q0) * a.num_q_heads + hq0 + r) * D + d] = __float2bfloat16(acc / l);
+        } else {
+            const int64_t slot = (static_cast<int64_t>(b) * a.splits + s) * a.num_q_heads + hq0 + r;
+            a.ws_o[slot * D + d] = acc;
+            if (d == 0) {
+                a.ws_ml[slot * 2] = M;
+                a.ws_ml[slot * 2 + 1] = l;
+            }
+        }
+    }
+}
+
+template <int D>
+cudaError_t launch_decode_d(const Args& a, cudaStream_t stream) {
+    using Tile = DecodeTile<D>;
+    static bool configured[64] = {};  // the attribute is set once per device
+    int dev = 0;
+    cudaGetDevice(&dev);
+    if (!configured[dev & 63]) {
+        cudaError_t e = cudaFuncSetAttribute(decode_splitkv_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             Tile::kSmemBytes);
+        if (e != cudaSuccess) return e;
+        configured[dev & 63] = true;
+    }
+    const int64_t ctas = decode_ctas(a);
+    if (ctas == 0) return cudaSuccess;
+    decode_splitkv_kernel<D><<<static_cast<unsigned>(ctas), kWarps * 32, Tile::kSmemBytes, stream>>>(a);
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+int64_t decode_ctas(const Args& a) {
+    return static_cast<int64_t>(a.num_seqs) * a.num_kv_heads * a.row_groups * a.splits;
+}
+
+cudaError_t launch_decode(const Args& a, cudaStream_t stream) {
+    switch (a.head_dim) {
+        case 64: return launch_decode_d<64>(a, stream);
+        case 128: return launch_decode_d<128>(a, stream);
+        default: return cudaErrorInvalidValue;
+    }
+}
+
+}  // namespace pa

@@ -1,0 +1,50 @@
+// pa_internal.h -- what the C-ABI layer hands to the kernel launchers.
+// Not installed; the public interface is include/pagedattn.h.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace pa {
+
+// Device error codes written to the sticky error word (first one wins).
+enum DeviceError : int32_t {
+    kDevOk = 0,
+    kDevBadBlock = 1,      // a block-table entry outside [0, num_blocks)
+    kDevSeqTooLong = 2,    // seq_lens[b] > max_pages * page_size (clamped)
+    kDevQueryTooLong = 3,  // query_start_loc gives n_b > seq_lens[b] (rows written as 0)
+    kDevWaitTimeout = 4,   // a bounded wait in a kernel gave up
+    kDevBadQueryStart = 5, // query_start_loc not within [0, T] or decreasing (rows skipped)
+};
+
+struct Args {
+    const void* q;        // [T, Hq, D] bf16
+    const void* k_cache;  // [NB, P, Hkv, D] bf16
+    const void* v_cache;  // [NB, P, Hkv, D] bf16
+    const int32_t* block_table;      // [B, max_pages]
+    const int32_t* seq_lens;         // [B]
+    const int32_t* query_start_loc;  // [B + 1]
+    void* out;                       // [T, Hq, D] bf16
+    float* ws_o;    // split partials: [B, splits, Hq, D] fp32 (unnormalised O)
+    float* ws_ml;   // [B, splits, Hq, 2] fp32: running max (log2 domain) and sum
+    int32_t* err;   // sticky device error word
+    int64_t num_tokens;
+    int64_t num_blocks;
+    int32_t num_seqs, num_q_heads, num_kv_heads, group, head_dim, page_size, max_pages;
+    int32_t kv_chunk;    // tokens per split (multiple of the page size)
+    int32_t splits;      // splits in the static decode grid
+    int32_t row_groups;  // ceil(group / 16): 16 query-head rows per decode CTA
+    float scale;         // softmax scale
+    float scale_log2;    // scale * log2(e)
+};
+
+cudaError_t launch_decode(const Args& a, cudaStream_t stream);
+cudaError_t launch_combine(const Args& a, cudaStream_t stream);
+cudaError_t launch_prefill(const Args& a, cudaStream_t stream);
+
+// Static grid sizes (functions of shapes only), shared with the planner.
+int64_t decode_ctas(const Args& a);
+int64_t combine_ctas(const Args& a);
+int64_t prefill_ctas(const Args& a);
+
+}  // namespace pa

@@ -323,3 +323,81 @@ def decode_position_code(v: torch.Tensor) -> int:
 def logical_to_physical(block_table_row: torch.Tensor, j: int, page_size: int = PAGE_SIZE):
     """(physical page, slot) that holds logical position j of one sequence."""
     return int(block_table_row[j // page_size]), j % page_size
+
+
+def position_codes(pos: torch.Tensor, head_dim: int) -> torch.Tensor:
+    """Vectorised position_code: [N] int64 positions -> [N, D] float32 codes."""
+    r = head_dim // 4
+    pos = pos.to(torch.int64)
+    if pos.numel() and (int(pos.min()) < 0 or int(pos.max()) >= r ** 4):
+        raise ValueError("position out of range for the code")
+    out = torch.zeros((pos.numel(), head_dim), dtype=torch.float32)
+    x = pos.clone()
+    rows = torch.arange(pos.numel())
+    for k in range(4):
+        out[rows, k * r + (x % r)] = 1.0
+        x = x // r
+    return out
+
+
+def spike_batch(q_lens, seq_lens, num_q_heads, num_kv_heads, head_dim, *, seed: int,
+                spikes: int = 4, max_pages=None, pool_factor: float = 1.5):
+    """Inputs whose exact output is known by construction (scale 1).
+
+    V at logical position j is position_code(j).  K is zero except "spikes": for
+    every (sequence, KV head, head-in-group g) there are up to ``spikes`` positions
+    f_1 < f_2 < ... with K[f_k][g] = 100 * k, f_1 <= the sequence's first query
+    position.  Query head h = hk * G + g is the one-hot e_g.  Its scores are 100*k
+    at the spikes it can see and 0 elsewhere; the largest visible one beats every
+    other by >= 100 (2^-144 after exp2, which flushes to 0 in fp32), so the exact
+    output is position_code(largest f_k <= p).  A key read from the wrong page or
+    slot, a wrong head, or a future key leaking through the causal mask changes
+    the output bits.
+
+    Returns (batch, expected) with expected [T, Hq] int64 positions.
+    """
+    b = make_batch(q_lens, seq_lens, num_q_heads, num_kv_heads, head_dim, seed=seed,
+                   max_pages=max_pages, pool_factor=pool_factor, scale=1.0, poison=True)
+    G = num_q_heads // num_kv_heads
+    if G > head_dim:
+        raise ValueError("one channel per head in a group is needed")
+    g = torch.Generator().manual_seed(seed + 7919)
+    P = b.page_size
+    used = torch.zeros(b.num_blocks, dtype=torch.bool)
+    nan = float("nan")
+    # clean data everywhere a sequence has a page; tails and unused pages stay NaN
+    for s, L in enumerate(seq_lens):
+        npg = (L + P - 1) // P
+        pages = b.block_table[s, :npg].to(torch.int64)
+        used[pages] = True
+        j = torch.arange(L)
+        codes = position_codes(j, head_dim).to(torch.bfloat16)
+        pg = pages[j // P]
+        sl = j % P
+        b.k_cache[pg, sl] = torch.zeros((L, num_kv_heads, head_dim), dtype=torch.bfloat16)
+        b.v_cache[pg, sl] = codes[:, None, :].expand(L, num_kv_heads, head_dim)
+    b.q.zero_()
+    for h in range(num_q_heads):
+        b.q[:, h, h % G] = 1.0
+    T = sum(q_lens)
+    expected = torch.full((T, num_q_heads), -1, dtype=torch.int64)
+    qsl = b.query_start_loc.tolist()
+    for s, (n, L) in enumerate(zip(q_lens, seq_lens)):
+        if n == 0:
+            continue
+        first = L - n
+        for hk in range(num_kv_heads):
+            for gi in range(G):
+                f1 = int(torch.randint(0, first + 1, (1,), generator=g))
+                rest = torch.randperm(L - f1 - 1, generator=g)[: spikes - 1] + f1 + 1 if L - f1 - 1 > 0 else \
+                    torch.zeros(0, dtype=torch.int64)
+                fs = [f1] + sorted(rest.tolist())
+                for k, f in enumerate(fs):
+                    page = int(b.block_table[s, f // P])
+                    b.k_cache[page, f % P, hk, gi] = 100.0 * (k + 1)
+                ft = torch.tensor(fs)
+                for i in range(n):
+                    p = first + i
+                    expected[qsl[s] + i, hk * G + gi] = int(ft[ft <= p].max())
+    del nan, used
+    return b, expected

@@ -1,0 +1,78 @@
+"""Helpers for the GPU parity tests: run the CUDA path, compare with the oracle."""
+
+from __future__ import annotations
+
+import numpy as np
+import torch
+
+import paged_kv_cache_forward_gb300 as pa
+from paged_kv_cache_forward_gb300 import build as build_mod
+from paged_kv_cache_forward_gb300 import workloads as W
+
+# Tolerance of the GPU bf16 output against the fp64 oracle, over all compared
+# elements: max-abs error 1.5e-2 and mean-abs error 2e-3.
+TOL_MAX = 1.5e-2
+TOL_MEAN = 2e-3
+
+_built = False
+
+
+def ensure_built():
+    global _built
+    if not _built:
+        build_mod.build()
+        pa.load()
+        _built = True
+
+
+def run(b: W.Batch, kv_chunk: int = 0, device="cuda", check_errors: bool = True) -> torch.Tensor:
+    """pa_forward on the batch; returns the output on the CPU (bf16).  The output
+    buffer starts as NaN so that an unwritten row cannot pass."""
+    ensure_built()
+    d = b.to(device)
+    out = torch.full_like(d.q, float("nan"))
+    pa.forward(d.q, d.k_cache, d.v_cache, d.block_table, d.seq_lens, d.query_start_loc, out,
+               scale=b.scale, kv_chunk=kv_chunk)
+    torch.cuda.synchronize()
+    if check_errors:
+        assert pa.device_error() == 0
+    return out.cpu()
+
+
+def errors(got_bf16: torch.Tensor, ref: np.ndarray):
+    g = got_bf16.double().numpy()
+    assert g.shape == ref.shape, (g.shape, ref.shape)
+    assert np.isfinite(g).all(), "non-finite GPU output"
+    e = np.abs(g - ref)
+    return float(e.max()), float(e.mean())
+
+
+def assert_close(got_bf16, ref, what=""):
+    mx, mean = errors(got_bf16, ref)
+    assert mx <= TOL_MAX and mean <= TOL_MEAN, f"{what}: max_abs {mx:.3e} mean_abs {mean:.3e}"
+    return mx, mean
+
+
+def sample_rows(b: W.Batch, n_random: int, seed: int = 0):
+    """(token, head) rows to check on a batch too large for a full oracle pass:
+    the first and last new token of every sequence (all heads of one, one head of
+    the rest), plus random rows."""
+    g = torch.Generator().manual_seed(seed)
+    Hq = b.num_q_heads
+    qsl = b.query_start_loc.tolist()
+    rows = set()
+    for s in range(b.num_seqs):
+        if qsl[s + 1] == qsl[s]:
+            continue
+        first, last = qsl[s], qsl[s + 1] - 1
+        if s == 0:
+            for h in range(Hq):
+                rows.add((first, h))
+                rows.add((last, h))
+        else:
+            rows.add((first, s % Hq))
+            rows.add((last, (s * 7 + 3) % Hq))
+    T = b.num_tokens
+    for _ in range(n_random):
+        rows.add((int(torch.randint(0, T, (1,), generator=g)), int(torch.randint(0, Hq, (1,), generator=g))))
+    return sorted(rows)

@@ -1,0 +1,125 @@
+"""The C-ABI library without a GPU: it loads, exports every declared symbol,
+plans on the host, and rejects bad arguments before touching CUDA."""
+
+import ctypes
+import os
+import re
+
+import pytest
+
+from paged_kv_cache_forward_gb300 import binding as B
+from paged_kv_cache_forward_gb300 import build as build_mod
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "pagedattn.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    build_mod.build()
+    return B.load()
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(pa_[a-z_0-9]+)\s*\(", text)))
+
+
+def test_header_declares_what_binding_knows():
+    assert declared_functions() == sorted(B.EXPORTED)
+
+
+def test_every_declared_symbol_is_exported(lib):
+    for name in declared_functions():
+        assert hasattr(lib, name), name
+
+
+def test_status_strings(lib):
+    for st in range(5):
+        assert lib.pa_status_string(st)
+    assert lib.pa_version() == 100
+
+
+def llama_dims(**kw):
+    d = dict(num_tokens=1, num_blocks=3072, num_seqs=1, num_q_heads=32, num_kv_heads=8, head_dim=128,
+             page_size=16, max_pages=2048)
+    d.update(kw)
+    return B.Dims(**d)
+
+
+def test_plan_shapes_only(lib):
+    p = B.plan(llama_dims())
+    assert p["kv_chunk"] % 16 == 0
+    assert p["splits"] == -(-2048 * 16 // p["kv_chunk"])
+    assert p["decode_ctas"] == 1 * 8 * 1 * p["splits"]
+    assert p["workspace_bytes"] >= 256
+    # static grid: a plan never depends on anything but the dims
+    assert B.plan(llama_dims()) == p
+
+
+def test_plan_forced_chunk(lib):
+    p = B.plan(llama_dims(), kv_chunk=1024)
+    assert p["kv_chunk"] == 1024 and p["splits"] == 32
+    p = B.plan(llama_dims(), kv_chunk=1 << 20)
+    assert p["splits"] == 1 and p["combine_ctas"] == 0
+
+
+def test_plan_row_groups(lib):
+    # G = 32 query heads per KV head: two decode row groups of 16
+    p = B.plan(llama_dims(num_kv_heads=1))
+    assert p["decode_ctas"] == 1 * 1 * 2 * p["splits"]
+
+
+@pytest.mark.parametrize("kw,status", [
+    (dict(head_dim=96), B.PA_ERR_UNSUPPORTED),
+    (dict(page_size=32), B.PA_ERR_UNSUPPORTED),
+    (dict(num_q_heads=30), B.PA_ERR_INVALID_ARG),
+    (dict(num_kv_heads=0), B.PA_ERR_INVALID_ARG),
+    (dict(num_blocks=0), B.PA_ERR_INVALID_ARG),
+    (dict(max_pages=0), B.PA_ERR_INVALID_ARG),
+    (dict(num_tokens=-1), B.PA_ERR_INVALID_ARG),
+    (dict(num_q_heads=128, num_kv_heads=1), B.PA_ERR_UNSUPPORTED),
+])
+def test_plan_rejects(lib, kw, status):
+    with pytest.raises(B.PagedAttnError) as e:
+        B.plan(llama_dims(**kw))
+    assert e.value.status == status
+    assert lib.pa_last_error().decode()
+
+
+def test_bad_chunk_rejected(lib):
+    with pytest.raises(B.PagedAttnError) as e:
+        B.plan(llama_dims(), kv_chunk=24)
+    assert e.value.status == B.PA_ERR_INVALID_ARG
+
+
+def test_forward_rejects_before_cuda(lib):
+    d = llama_dims()
+    # NULL dims, NULL pointers and misaligned pointers are refused on the host
+    st = lib.pa_forward(None, None, None, None, None, None, None, ctypes.c_float(1.0), None, None)
+    assert st == B.PA_ERR_INVALID_ARG
+    st = lib.pa_forward(None, None, None, None, None, None, None, ctypes.c_float(1.0), ctypes.byref(d), None)
+    assert st == B.PA_ERR_INVALID_ARG
+    buf = (ctypes.c_uint8 * 64)()
+    base = ctypes.addressof(buf)
+    a16 = (base + 15) & ~15
+    st = lib.pa_forward(a16 + 2, a16, a16, a16, a16, a16, a16, ctypes.c_float(1.0), ctypes.byref(d), None)
+    assert st == B.PA_ERR_INVALID_ARG
+    assert "aligned" in lib.pa_last_error().decode()
+
+
+def test_empty_batch_is_noop(lib):
+    d = llama_dims(num_tokens=0, num_seqs=0)
+    st = lib.pa_forward(None, None, None, None, None, None, None, ctypes.c_float(1.0), ctypes.byref(d), None)
+    assert st == B.PA_OK
+
+
+def test_library_has_no_oracle_dependency():
+    # the product library must not link or name the test oracle
+    data = open(B.LIB_PATH, "rb").read()
+    assert b"oracle_attention" not in data
+    for f in os.listdir(os.path.join(ROOT, "paged_kv_cache_forward_gb300")):
+        if f.endswith(".py") and f != "workloads.py":
+            src = open(os.path.join(ROOT, "paged_kv_cache_forward_gb300", f)).read()
+            assert "import oracle" not in src and "from oracle" not in src, f

@@ -1,0 +1,273 @@
+"""GPU parity: the CUDA path against the fp64 oracle on the same seeded inputs.
+
+Bar (the problem's stated tolerance): max-abs error <= 1.5e-2 and mean-abs
+error <= 2e-3 over all compared elements; block-table indexing and causal
+masking bit-exact (position-code spikes); block permutation, causal hiding and
+graph replay bit-exact against the same kernel.
+"""
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import paged_kv_cache_forward_gb300 as pa
+from paged_kv_cache_forward_gb300 import workloads as W
+
+from gpu_util import assert_close, errors, run, sample_rows
+
+pytestmark = pytest.mark.gpu
+
+
+# ------------------------------------------------------------ the five configs
+
+def test_tiny_decode_all_seeds():
+    for seed in range(5):
+        b = W.tiny_decode(seed)
+        assert_close(run(b), oracle.batch_attention(b), f"tiny seed {seed}")
+
+
+@pytest.mark.parametrize("ctx", [1024, 8192, 32768])
+def test_llama_decode(ctx):
+    b = W.llama_decode(ctx, seed=0)
+    assert_close(run(b), oracle.batch_attention(b), f"llama decode {ctx}")
+
+
+def test_batched_decode():
+    b = W.batched_decode(seed=0)
+    assert_close(run(b), oracle.batch_attention(b), "batched decode")
+
+
+def test_varlen_prefill_full_size_sampled():
+    b = W.varlen_prefill(seed=0)
+    got = run(b)
+    rows = sample_rows(b, 600, seed=1)
+    ref = oracle.batch_attention(b, rows=rows)
+    sel = torch.stack([got[t, h] for t, h in rows])
+    assert_close(sel, ref, "varlen prefill (sampled rows)")
+
+
+def test_mixed_full_size_sampled_in_graph():
+    b = W.mixed_batch(seed=0)
+    d = b.to("cuda")
+    out = torch.full_like(d.q, float("nan"))
+    s = torch.cuda.Stream()
+    pa.prepare(d.q, d.k_cache, d.block_table, d.seq_lens, stream=s)
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s):
+        pa.forward(d.q, d.k_cache, d.v_cache, d.block_table, d.seq_lens, d.query_start_loc, out, scale=b.scale)
+    g.replay()
+    torch.cuda.synchronize()
+    assert pa.device_error(s) == 0
+    got = out.cpu()
+    assert torch.isfinite(got.float()).all()
+    rows = sample_rows(b, 400, seed=2)
+    T = b.num_tokens
+    rows += [(T - 1, h) for h in range(b.num_q_heads)]  # the 131072-context decode row
+    rows = sorted(set(rows))
+    ref = oracle.batch_attention(b, rows=rows)
+    sel = torch.stack([got[t, h] for t, h in rows])
+    assert_close(sel, ref, "mixed (sampled rows)")
+
+
+# --------------------------------------------------- smaller full comparisons
+
+def test_prefill_small_full():
+    for seed in range(3):
+        g = torch.Generator().manual_seed(100 + seed)
+        B = 4
+        n = torch.randint(2, 200, (B,), generator=g).tolist()
+        p = torch.randint(0, 300, (B,), generator=g).tolist()
+        b = W.make_batch(n, [a + c for a, c in zip(n, p)], 32, 8, 128, seed=seed)
+        assert_close(run(b), oracle.batch_attention(b), f"prefill small seed {seed}")
+
+
+def test_mixed_small_full():
+    q_lens = [40, 1, 1, 17, 1, 2, 1]
+    seq_lens = [40, 700, 1, 100, 3000, 2, 16]
+    b = W.make_batch(q_lens, seq_lens, 32, 8, 128, seed=5)
+    assert_close(run(b), oracle.batch_attention(b), "mixed small")
+
+
+@pytest.mark.parametrize("Hq,Hkv,D", [(4, 1, 64), (8, 8, 128), (16, 2, 64), (32, 1, 128), (12, 4, 128),
+                                      (64, 2, 64)])
+def test_head_shapes(Hq, Hkv, D):
+    q_lens = [1, 9, 1, 33]
+    seq_lens = [333, 9, 17, 50]
+    b = W.make_batch(q_lens, seq_lens, Hq, Hkv, D, seed=Hq + Hkv + D)
+    assert_close(run(b), oracle.batch_attention(b), f"heads {Hq}/{Hkv} D {D}")
+
+
+@pytest.mark.parametrize("chunk", [16, 48, 256, 4096])
+def test_split_invariance(chunk):
+    b = W.make_batch([1, 1, 1, 5], [2000, 1, 777, 300], 32, 8, 128, seed=9, max_pages=128)
+    ref = oracle.batch_attention(b)
+    got = run(b, kv_chunk=chunk)
+    assert_close(got, ref, f"kv_chunk {chunk}")
+    whole = run(b, kv_chunk=128 * 16)
+    mx, _ = errors(got, whole.double().numpy())
+    assert mx <= 2 * 2 ** -8 * 4, mx  # a few bf16 ulps of |out| <= ~4
+
+
+# ------------------------------------------------------------------- edge cases
+
+def test_edge_lengths():
+    # single key, exact page multiples, one-token prefill, n == L prefill, empty sequences
+    q_lens = [1, 1, 0, 2, 16, 1, 0, 3]
+    seq_lens = [1, 16, 0, 2, 16, 32, 5, 3]
+    b = W.make_batch(q_lens, seq_lens, 8, 2, 128, seed=11, max_pages=4)
+    got = run(b)
+    assert_close(got, oracle.batch_attention(b), "edge lengths")
+    # the single-key row is V[0] exactly
+    page = int(b.block_table[0, 0])
+    for h in range(8):
+        assert torch.equal(got[0, h], b.v_cache[page, 0, h // 4])
+
+
+def test_empty_and_zero_token_batches():
+    b = W.make_batch([0, 0], [5, 0], 8, 2, 128, seed=12)
+    d = b.to("cuda")
+    out = torch.zeros_like(d.q)
+    pa.forward(d.q, d.k_cache, d.v_cache, d.block_table, d.seq_lens, d.query_start_loc, out, scale=b.scale)
+    torch.cuda.synchronize()
+    assert out.numel() == 0
+
+
+def test_max_pages_exact_fit_and_poison_neighbours():
+    # every page of the table used, NaN everywhere else in the pool
+    b = W.make_batch([1, 4], [64 * 16, 64 * 16], 32, 8, 128, seed=13, max_pages=64, pool_factor=1.05)
+    assert_close(run(b), oracle.batch_attention(b), "exact fit")
+
+
+# ------------------------------------------------------------- bit-exact checks
+
+def _codes(expected, D):
+    T, Hq = expected.shape
+    return W.position_codes(expected.flatten(), D).reshape(T, Hq, D).to(torch.bfloat16)
+
+
+@pytest.mark.parametrize("case", ["decode", "prefill", "mixed", "tiny"])
+def test_position_code_spikes_bit_exact(case):
+    if case == "decode":
+        b, exp = W.spike_batch([1] * 6, [1, 15, 16, 17, 1000, 5000], 32, 8, 128, seed=21)
+    elif case == "prefill":
+        b, exp = W.spike_batch([37, 128, 5], [37, 300, 70], 32, 8, 128, seed=22)
+    elif case == "mixed":
+        b, exp = W.spike_batch([64, 1, 1, 9], [64, 20000, 33, 40], 32, 8, 128, seed=23)
+    else:
+        b, exp = W.spike_batch([1], [256], 4, 1, 64, seed=24, max_pages=16)
+    got = run(b)
+    want = _codes(exp, b.head_dim)
+    bad = (got.view(torch.int16) != want.view(torch.int16)).any(-1)
+    assert not bad.any(), f"{int(bad.sum())} rows differ, first {torch.nonzero(bad)[:5].tolist()}"
+
+
+def test_spikes_bit_exact_across_splits():
+    b, exp = W.spike_batch([1, 1, 3], [4000, 257, 900], 32, 8, 128, seed=25, max_pages=256)
+    want = _codes(exp, 128)
+    for chunk in (16, 64, 1024, 4096):
+        got = run(b, kv_chunk=chunk)
+        assert torch.equal(got.view(torch.int16), want.view(torch.int16)), chunk
+
+
+def _rescatter(b: W.Batch, seed: int, extra: int) -> W.Batch:
+    g = torch.Generator().manual_seed(seed)
+    nb = b.num_blocks + extra
+    perm = torch.randperm(nb, generator=g)
+    k = torch.full((nb,) + tuple(b.k_cache.shape[1:]), float("nan"), dtype=torch.bfloat16)
+    v = k.clone()
+    bt = torch.full_like(b.block_table, int(perm[-1]))
+    cur = 0
+    for s, L in enumerate(b.seq_lens.tolist()):
+        for pg in range((L + 15) // 16):
+            src, dst = int(b.block_table[s, pg]), int(perm[cur])
+            cur += 1
+            k[dst] = b.k_cache[src]
+            v[dst] = b.v_cache[src]
+            bt[s, pg] = dst
+    return W.Batch(name=b.name, q=b.q, k_cache=k, v_cache=v, block_table=bt, seq_lens=b.seq_lens,
+                   query_start_loc=b.query_start_loc, scale=b.scale, poison_page=int(perm[-1]), seed=seed)
+
+
+def test_block_permutation_bit_exact():
+    b = W.make_batch([1, 23, 1, 2], [900, 100, 33, 2], 32, 8, 128, seed=31)
+    got = run(b)
+    got2 = run(_rescatter(b, 77, 13))
+    assert torch.equal(got.view(torch.int16), got2.view(torch.int16))
+
+
+def test_causal_hiding_bit_exact():
+    n, L = 70, 200
+    b = W.make_batch([n], [L], 32, 8, 128, seed=32)
+    got = run(b)
+    k2, v2 = b.k_cache.clone(), b.v_cache.clone()
+    g = torch.Generator().manual_seed(4)
+    cut = L - n + 30  # query 30 sits at this position
+    for j in range(cut + 1, L):
+        page, slot = W.logical_to_physical(b.block_table[0], j)
+        k2[page, slot] = (torch.randn(8, 128, generator=g) * 30).to(torch.bfloat16)
+        v2[page, slot] = (torch.randn(8, 128, generator=g) * 30).to(torch.bfloat16)
+    b2 = W.Batch(**{**b.__dict__, "k_cache": k2, "v_cache": v2})
+    got2 = run(b2)
+    assert torch.equal(got[:31].view(torch.int16), got2[:31].view(torch.int16))
+    assert not torch.equal(got[31:], got2[31:])
+
+
+# ------------------------------------------------------------------ CUDA graphs
+
+def test_graph_replay_new_contents_bit_exact():
+    """Capture once; replay with other lengths, tables and query split of the
+    same shapes: the static grid must give the eager results bit for bit."""
+    Hq, Hkv, D, mp = 32, 8, 128, 64
+    b1 = W.make_batch([1, 6, 1, 1], [700, 40, 1000, 5], Hq, Hkv, D, seed=41, max_pages=mp, pool_pages=200)
+    b2 = W.make_batch([3, 1, 4, 1], [3, 1024, 4, 600], Hq, Hkv, D, seed=42, max_pages=mp, pool_pages=200)
+    e1, e2 = run(b1), run(b2)
+    d = b1.to("cuda")
+    out = torch.full_like(d.q, float("nan"))
+    s = torch.cuda.Stream()
+    pa.prepare(d.q, d.k_cache, d.block_table, d.seq_lens, stream=s)
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s):
+        pa.forward(d.q, d.k_cache, d.v_cache, d.block_table, d.seq_lens, d.query_start_loc, out, scale=b1.scale)
+    for b, e in ((b1, e1), (b2, e2), (b1, e1)):
+        for name in ("q", "k_cache", "v_cache", "block_table", "seq_lens", "query_start_loc"):
+            getattr(d, name).copy_(getattr(b, name))
+        out.fill_(float("nan"))
+        g.replay()
+        torch.cuda.synchronize()
+        assert torch.equal(out.cpu().view(torch.int16), e.view(torch.int16))
+
+
+def test_capture_without_prepare_is_refused():
+    b = W.make_batch([1], [50000], 32, 8, 128, seed=43, max_pages=4096, pool_pages=3200)
+    d = b.to("cuda")
+    out = torch.empty_like(d.q)
+    s = torch.cuda.Stream()  # a fresh stream has no workspace
+    g = torch.cuda.CUDAGraph()
+    with pytest.raises(pa.PagedAttnError) as e:
+        with torch.cuda.graph(g, stream=s):
+            pa.forward(d.q, d.k_cache, d.v_cache, d.block_table, d.seq_lens, d.query_start_loc, out,
+                       scale=b.scale, kv_chunk=512)
+    assert e.value.status == 3
+    torch.cuda.synchronize()
+
+
+# --------------------------------------------------------- device-side checks
+
+def test_bad_block_id_sets_error_word_without_fault():
+    b = W.make_batch([1, 2], [40, 30], 8, 2, 128, seed=51)
+    b.block_table[0, 1] = b.num_blocks + 5  # out of range: the kernels skip it
+    run(b, check_errors=False)
+    assert pa.device_error() == 1
+    assert pa.device_error() == 0  # cleared
+    # the context is still usable
+    b2 = W.tiny_decode(0)
+    assert_close(run(b2), oracle.batch_attention(b2), "after error")
+
+
+def test_query_longer_than_context_flagged():
+    b = W.make_batch([3], [3], 8, 2, 128, seed=52)
+    b.seq_lens[0] = 2  # 3 new tokens but 2 keys: contract violation
+    got = run(b, check_errors=False)
+    assert pa.device_error() == 3
+    assert torch.isfinite(got.float()).all()
