@@ -65,6 +65,8 @@ def parse_args(argv=None):
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=10.0, help="target CPU time of the oracle leg")
+    ap.add_argument("--min-warm-ms", type=float, default=500.0,
+                    help="graph warm-up time before the timed region (clocks settle); 0 for profiling runs")
     return ap.parse_args(argv)
 
 
@@ -291,10 +293,10 @@ def run_reference(args):
     metric, unit, _ = metric_of(args.config)
     steps = args.steps or 3
     warm = max(0, min(args.warmup, 1))
-    budget = 120.0 / max(1, steps + warm)
+    budget = min(120.0 / max(1, steps + warm), args.cpu_seconds)
     for _ in range(warm):
         cpu_baseline(batch, args.config, min(budget, 5.0))
-    vals = [cpu_baseline(batch, args.config, min(budget, 20.0)) for _ in range(steps)]
+    vals = [cpu_baseline(batch, args.config, budget) for _ in range(steps)]
     v = statistics.median(x["value"] for x in vals)
     step_s = (work_of(batch)["flops"] / v / 1e12) if args.config == "varlen_prefill" else \
         (work_of(batch)["kv_bytes"] / v / 1e9)
@@ -377,6 +379,12 @@ def run_ours(args):
 
     def make_graph(n):
         evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(n)]
+        # torch creates the CUDA event on its first record(); do that outside the
+        # capture so that the library receives real handles to re-record.
+        for e_a, e_b in evs:
+            e_a.record(stream)
+            e_b.record(stream)
+        stream.synchronize()
         g = torch.cuda.CUDAGraph()
         with torch.cuda.graph(g, stream=stream):
             for i in range(n):
@@ -390,7 +398,7 @@ def run_ours(args):
 
     sampler = ClockSampler(local).start()
     # graph warm-up: at least W steps, and at least ~0.5 s so that clocks settle
-    warm_reps = max(1, int(math.ceil(args.warmup / M)), int(500.0 / max(est_ms * M, 1e-3)))
+    warm_reps = max(1, int(math.ceil(args.warmup / M)), int(args.min_warm_ms / max(est_ms * M, 1e-3)))
     for _ in range(warm_reps):
         g_main.replay()
     stream.synchronize()

@@ -169,6 +169,8 @@ def options(kv_chunk: int = 0, events=None) -> Options:
     if events:
         for key in ("decode_start_event", "decode_stop_event", "prefill_start_event", "prefill_stop_event"):
             ev = events.get(key)
+            if ev is not None and not ev.cuda_event:
+                raise ValueError(f"{key}: the torch event has no CUDA event yet (record it once first)")
             setattr(o, key, ev.cuda_event if ev is not None else None)
     return o
 

@@ -1,0 +1,535 @@
+// prefill_tc.cu -- causal varlen chunked prefill on the 5th-generation tensor
+// cores (tcgen05 + TMEM + TMA), sm_103a.
+//
+// One CTA owns (query tile, KV head h).  The tile packs TQ = floor(128 / G)
+// consecutive new tokens of one sequence times the G query heads sharing h into
+// the M = 128 rows of one MMA tile, row r = (token r / G, head h*G + r % G): the
+// "Q-Block" item of the five-step list on the Triton unified-attention page
+// (section "What three things the IBM paper got right"), so each KV tile is
+// loaded once for all G heads.  Keys are walked in tiles of 128 (8 pages) up to
+// the tile's last causal position, with the FlashAttention recurrence of "The
+// Flash Attention revolution" (GPU programming guide page): S = Q K^T, causal
+// -inf mask bottom-right aligned ("Flash Attention in Triton"), online softmax,
+// O += P V, out = O / l.
+//
+// Warp roles (192 threads):
+//   warp 0      TMA producer: Q once, then K and V page boxes (64 x 16 rows of
+//               128 B, 128-byte swizzle) per KV tile into a 2-stage ring.  The
+//               one page of V that holds the sequence end is copied by plain
+//               loads with zero fill, so no slot past seq_len reaches the MMA.
+//   warp 1      allocates TMEM (S double buffer + O: 384 of 512 columns); its
+//               lane 0 issues the MMAs: S(kt) = Q K(kt)^T (M=128, N=128, K=D) into
+//               TMEM, then O += P(kt-1) V(kt-1) (N=D, K=128) so that the softmax of
+//               tile kt overlaps the MMAs of the neighbours.
+//   warps 2-5   softmax, one thread per row (TMEM lane): load S from TMEM,
+//               mask, running max in log2 units, P = 2^(x - m) to bf16 in shared
+//               memory (K-major, 128-byte swizzle) for the P V MMA.  The running
+//               max is only moved (and O in TMEM rescaled) when the row max grows
+//               by more than 2^8; the final O / l is exact either way.
+// Every wait on an mbarrier is bounded (2 s); on timeout the CTA records
+// kDevWaitTimeout, stops all roles, drains the MMAs it issued, frees TMEM and
+// exits.
+
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include "pa_device.cuh"
+#include "pa_internal.h"
+#include "tc_device.cuh"
+
+namespace pa {
+namespace {
+
+constexpr int kThreads = 192;
+constexpr int kM = 128;            // rows per tile
+constexpr int kKeys = 128;         // keys per KV tile
+constexpr int kPage = 16;
+constexpr int kPagesPerTile = kKeys / kPage;
+constexpr int kHalfBytes = 128 * 128;  // 128 rows x 128 B: one 64-column half of a tile
+constexpr uint64_t kTimeoutNs = 2000000000ull;
+constexpr uint32_t kTmemCols = 512;
+constexpr uint32_t kTmemS0 = 0, kTmemS1 = 128, kTmemO = 256;
+
+template <int D>
+struct Smem {
+    static constexpr int kHalves = D / 64;
+    static constexpr int kQ = 0;
+    static constexpr int kK0 = kQ + kHalves * kHalfBytes;
+    static constexpr int kStage = kHalves * kHalfBytes;  // one K or V tile
+    static constexpr int kV0 = kK0 + 2 * kStage;
+    static constexpr int kP = kV0 + 2 * kStage;
+    static constexpr int kBar = kP + 2 * kHalfBytes;  // P: 128 keys = 2 halves
+    // barriers: q_full, kv_full[2], kv_empty[2], s_full[2], s_free[2], p_full, pv_done, drain
+    static constexpr int kNumBars = 12;
+    static constexpr int kMisc = kBar + kNumBars * 8;  // tmem address, abort flag, tile info
+    static constexpr int kBytes = kMisc + 64;
+    static constexpr int kAlloc = kBytes + 1024;  // slack to align the base to 1024
+};
+
+enum Bar { kQFull = 0, kKvFull0 = 1, kKvEmpty0 = 3, kSFull0 = 5, kSFree0 = 7, kPFull = 9, kPvDone = 10, kDrain = 11 };
+
+__device__ __forceinline__ int tiles_of(int n, int tq) { return n >= 2 ? (n + tq - 1) / tq : 0; }
+
+// Bounded wait by every lane of a warp; the result is made warp-uniform so that a
+// timeout can never leave some lanes at a warp-collective instruction alone.
+__device__ __forceinline__ bool warp_wait(uint32_t addr, uint32_t parity, const volatile int* abort) {
+    const bool ok = tc::mbar_wait(addr, parity, abort, kTimeoutNs);
+    return __all_sync(0xffffffffu, ok);
+}
+
+// Byte offset of 16-byte chunk c (0..7) of row r inside a 128-byte-swizzled half.
+__device__ __forceinline__ uint32_t sw128(int r, int c) { return r * 128 + ((c ^ (r & 7)) << 4); }
+
+template <int D>
+__global__ void __launch_bounds__(kThreads, 1)
+    prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+                      const __grid_constant__ CUtensorMap tm_v, const Args a, int tq_tokens, int tiles_bound) {
+    using S = Smem<D>;
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t raw = smem_u32(smem_raw);
+    const uint32_t base = (raw + 1023u) & ~1023u;
+    uint8_t* const sp = smem_raw + (base - raw);
+    auto bar = [&](int i) { return base + S::kBar + 8 * i; };
+    uint32_t* const s_tmem = reinterpret_cast<uint32_t*>(sp + S::kMisc);
+    volatile int* const s_abort = reinterpret_cast<volatile int*>(sp + S::kMisc + 4);
+    int* const s_info = reinterpret_cast<int*>(sp + S::kMisc + 8);
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    const int tile = blockIdx.x % tiles_bound;
+    const int h = blockIdx.x / tiles_bound;
+
+    // ---- which sequence owns this tile (prefix sum of per-sequence tile counts)
+    if (warp == 0) {
+        int found_b = -1, found_t = 0, base_t = 0;
+        for (int b0 = 0; b0 < a.num_seqs && found_b < 0; b0 += 32) {
+            const int b = b0 + lane;
+            const int cnt = b < a.num_seqs ? tiles_of(a.query_start_loc[b + 1] - a.query_start_loc[b], tq_tokens) : 0;
+            int inc = cnt;
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const int v = __shfl_up_sync(0xffffffffu, inc, o);
+                if (lane >= o) inc += v;
+            }
+            const int excl = base_t + inc - cnt;
+            const unsigned m = __ballot_sync(0xffffffffu, cnt > 0 && tile >= excl && tile < excl + cnt);
+            if (m) {
+                const int src = __ffs(m) - 1;
+                found_b = b0 + src;
+                found_t = tile - __shfl_sync(0xffffffffu, excl, src);
+            }
+            base_t += __shfl_sync(0xffffffffu, inc, 31);
+        }
+        if (lane == 0) {
+            s_info[0] = found_b;
+            s_info[1] = found_t;
+            *s_abort = 0;
+        }
+    }
+    __syncthreads();
+    const int b = s_info[0];
+    if (b < 0) return;  // surplus CTA of the static grid (uniform for the block)
+    const int t_in_seq = s_info[1];
+
+    const int q0 = a.query_start_loc[b];
+    const int n = a.query_start_loc[b + 1] - q0;
+    if (q0 < 0 || static_cast<int64_t>(q0) + n > a.num_tokens) {
+        if (threadIdx.x == 0) flag_error(a.err, kDevBadQueryStart);
+        return;
+    }
+    const int cap = a.max_pages * kPage;
+    int L = a.seq_lens[b];
+    if (L > cap) {
+        if (threadIdx.x == 0) flag_error(a.err, kDevSeqTooLong);
+        L = cap;
+    }
+    const int G = a.group;
+    const int i0 = t_in_seq * tq_tokens;
+    const int ntok = min(tq_tokens, n - i0);
+    const int prefix = L - n;
+    __nv_bfloat16* const out = reinterpret_cast<__nv_bfloat16*>(a.out);
+    if (prefix < 0) {
+        if (threadIdx.x == 0) flag_error(a.err, kDevQueryTooLong);
+        for (int i = threadIdx.x; i < ntok * G * D; i += blockDim.x) {
+            const int r = i / D;
+            out[(static_cast<int64_t>(q0 + i0 + r / G) * a.num_q_heads + h * G + r % G) * D + i % D] =
+                __float2bfloat16(0.f);
+        }
+        return;
+    }
+    const int kv_end = prefix + i0 + ntok;  // keys [0, kv_end) are visible to some row
+    const int ntiles = (kv_end + kKeys - 1) / kKeys;
+    const int last_page = (kv_end + kPage - 1) / kPage;  // pages [0, last_page) are read
+    const int full_pages = L / kPage;                    // pages with no slot past L
+
+    // ---- barriers and TMEM
+    if (threadIdx.x == 0) {
+        tc::mbar_init(bar(kQFull), 1);
+        for (int i = 0; i < 2; ++i) {
+            tc::mbar_init(bar(kKvFull0 + i), 1);
+            tc::mbar_init(bar(kKvEmpty0 + i), 1);
+            tc::mbar_init(bar(kSFull0 + i), 1);
+            tc::mbar_init(bar(kSFree0 + i), 4);
+        }
+        tc::mbar_init(bar(kPFull), 4);
+        tc::mbar_init(bar(kPvDone), 1);
+        tc::mbar_init(bar(kDrain), 1);
+        tc::fence_mbar_init();
+    }
+    if (warp == 1) {
+        tc::tmem_alloc(base + S::kMisc, kTmemCols);
+        tc::tmem_relinquish();
+    }
+    tc::tc_fence_before();
+    __syncthreads();
+    tc::tc_fence_after();
+    const uint32_t tmem = *s_tmem;
+    bool ok = true;
+
+    if (warp == 0) {
+        // ================================================= TMA producer
+        if (lane == 0) {
+            tc::prefetch_tmap(&tm_q);
+            tc::prefetch_tmap(&tm_k);
+            tc::prefetch_tmap(&tm_v);
+            tc::mbar_arrive_expect_tx(bar(kQFull), S::kHalves * 64 * 2 * G * tq_tokens);
+#pragma unroll
+            for (int hf = 0; hf < S::kHalves; ++hf)
+                tc::tma_load_3d(base + S::kQ + hf * kHalfBytes, &tm_q, bar(kQFull), hf * 64, h * G, q0 + i0);
+        }
+        const int32_t* bt = a.block_table + static_cast<int64_t>(b) * a.max_pages;
+        for (int kt = 0; kt < ntiles && ok; ++kt) {
+            const int st = kt & 1;
+            if (kt >= 2 && !warp_wait(bar(kKvEmpty0 + st), ((kt >> 1) - 1) & 1, s_abort)) {
+                ok = false;
+                break;
+            }
+            const int p0 = kt * kPagesPerTile;
+            const int np = min(kPagesPerTile, last_page - p0);
+            const int nv = max(0, min(np, full_pages - p0));  // V pages by TMA
+            int page = 0;
+            if (lane < np) {
+                page = bt[p0 + lane];
+                if (static_cast<uint32_t>(page) >= static_cast<uint64_t>(a.num_blocks)) {
+                    flag_error(a.err, kDevBadBlock);
+                    page = 0;
+                }
+            }
+            const uint32_t sk = base + S::kK0 + st * S::kStage;
+            const uint32_t sv = base + S::kV0 + st * S::kStage;
+            if (nv < np) {
+                // The page holding the sequence end: plain loads, slots >= L as zeros.
+                const int pi = np - 1;
+                const int pg = __shfl_sync(0xffffffffu, page, pi);
+                const __nv_bfloat16* vc = reinterpret_cast<const __nv_bfloat16*>(a.v_cache);
+                for (int c = lane; c < kPage * (D / 8); c += 32) {
+                    const int t = c / (D / 8), ch = c % (D / 8);
+                    const int row = pi * kPage + t;
+                    uint4 val = make_uint4(0u, 0u, 0u, 0u);
+                    if ((p0 + pi) * kPage + t < L)
+                        val = *reinterpret_cast<const uint4*>(
+                            vc + ((static_cast<int64_t>(pg) * kPage + t) * a.num_kv_heads + h) * D + ch * 8);
+                    const uint32_t dst = sv + (ch >> 3) * kHalfBytes + sw128(row, ch & 7);
+                    asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};\n" ::"r"(dst), "r"(val.x), "r"(val.y),
+                                 "r"(val.z), "r"(val.w)
+                                 : "memory");
+                }
+                tc::fence_proxy_async_smem();
+            }
+            __syncwarp();
+            if (lane == 0)
+                tc::mbar_arrive_expect_tx(bar(kKvFull0 + st), (np + nv) * S::kHalves * 2048);
+            __syncwarp();
+            if (lane < np) {
+#pragma unroll
+                for (int hf = 0; hf < S::kHalves; ++hf) {
+                    tc::tma_load_4d(sk + hf * kHalfBytes + lane * 2048, &tm_k, bar(kKvFull0 + st), hf * 64, h, 0,
+                                    page);
+                    if (lane < nv)
+                        tc::tma_load_4d(sv + hf * kHalfBytes + lane * 2048, &tm_v, bar(kKvFull0 + st), hf * 64, h,
+                                        0, page);
+                }
+            }
+        }
+        if (!ok && lane == 0) {
+            *s_abort = 1;
+            flag_error(a.err, kDevWaitTimeout);
+        }
+    } else if (warp == 1) {
+        // ===================================================== MMA issuer
+        if (lane == 0) {
+            constexpr uint32_t kIdQK = tc::idesc_bf16_f32(kM, kKeys, false, false);
+            constexpr uint32_t kIdPV = tc::idesc_bf16_f32(kM, D, false, true);
+            auto issue_pv = [&](int j) -> bool {
+                if (!tc::mbar_wait(bar(kPFull), j & 1, s_abort, kTimeoutNs)) return false;
+                tc::tc_fence_after();
+                const int npj = min(kPagesPerTile, last_page - j * kPagesPerTile);
+                const uint32_t sv = base + S::kV0 + (j & 1) * S::kStage;
+                for (int ks = 0; ks < npj; ++ks) {  // one 16-key step per page
+                    const uint64_t ad = tc::desc_sw128(base + S::kP + (ks >> 2) * kHalfBytes + (ks & 3) * 32, 16, 1024);
+                    const uint64_t bd = tc::desc_sw128(sv + ks * 2048, kHalfBytes, 1024);
+                    tc::mma_bf16(tmem + kTmemO, ad, bd, kIdPV, (j > 0 || ks > 0) ? 1u : 0u);
+                }
+                tc::mma_commit(bar(kPvDone));
+                tc::mma_commit(bar(kKvEmpty0 + (j & 1)));
+                return true;
+            };
+            ok = tc::mbar_wait(bar(kQFull), 0, s_abort, kTimeoutNs);
+            tc::tc_fence_after();
+            for (int kt = 0; kt < ntiles && ok; ++kt) {
+                const int st = kt & 1;
+                ok = tc::mbar_wait(bar(kKvFull0 + st), (kt >> 1) & 1, s_abort, kTimeoutNs);
+                if (ok && kt >= 2) ok = tc::mbar_wait(bar(kSFree0 + st), ((kt >> 1) - 1) & 1, s_abort, kTimeoutNs);
+                if (!ok) break;
+                tc::tc_fence_after();
+                const uint32_t sk = base + S::kK0 + st * S::kStage;
+#pragma unroll
+                for (int ks = 0; ks < D / 16; ++ks) {
+                    const uint32_t off = (ks >> 2) * kHalfBytes + (ks & 3) * 32;
+                    const uint64_t ad = tc::desc_sw128(base + S::kQ + off, 16, 1024);
+                    const uint64_t bd = tc::desc_sw128(sk + off, 16, 1024);
+                    tc::mma_bf16(tmem + (st ? kTmemS1 : kTmemS0), ad, bd, kIdQK, ks > 0 ? 1u : 0u);
+                }
+                tc::mma_commit(bar(kSFull0 + st));
+                if (kt >= 1) ok = issue_pv(kt - 1);
+            }
+            if (ok) ok = issue_pv(ntiles - 1);
+            if (!ok) {
+                *s_abort = 1;
+                flag_error(a.err, kDevWaitTimeout);
+            }
+            // drain: every MMA issued above has finished before TMEM is freed
+            tc::mma_commit(bar(kDrain));
+            tc::mbar_wait(bar(kDrain), 0, nullptr, kTimeoutNs);
+        }
+        __syncwarp();
+    } else {
+        // ======================================================== softmax
+        const int quarter = warp & 3;
+        const int r = quarter * 32 + lane;  // row == TMEM lane
+        const uint32_t lane_addr = tmem + (static_cast<uint32_t>(quarter * 32) << 16);
+        const bool valid = r < ntok * G;
+        const int pos = valid ? prefix + i0 + r / G : -1;  // causal limit of this row
+        const float c = a.scale_log2;
+        float m_used = -INFINITY;  // running max, log2 units
+        float l = 0.f;
+        for (int kt = 0; kt < ntiles; ++kt) {
+            const int st = kt & 1;
+            if (!warp_wait(bar(kSFull0 + st), (kt >> 1) & 1, s_abort)) {
+                ok = false;
+                break;
+            }
+            tc::tc_fence_after();
+            uint32_t sr[kKeys];
+#pragma unroll
+            for (int q = 0; q < kKeys / 32; ++q)
+                tc::tmem_ld32(lane_addr + (st ? kTmemS1 : kTmemS0) + q * 32,
+                              *reinterpret_cast<uint32_t(*)[32]>(&sr[q * 32]));
+            tc::tc_fence_before();
+            __syncwarp();
+            if (lane == 0) tc::mbar_arrive(bar(kSFree0 + st));
+
+            const int j0 = kt * kKeys;
+            float mx = -INFINITY;
+            const bool diag = __any_sync(0xffffffffu, j0 + kKeys - 1 > pos);
+            if (diag) {
+#pragma unroll
+                for (int j = 0; j < kKeys; ++j) {
+                    const float s = __uint_as_float(sr[j]);
+                    const float v = (j0 + j <= pos) ? s : -INFINITY;
+                    sr[j] = __float_as_uint(v);
+                    mx = fmaxf(mx, v);
+                }
+            } else {
+#pragma unroll
+                for (int j = 0; j < kKeys; ++j) mx = fmaxf(mx, __uint_as_float(sr[j]));
+            }
+            const float mnew = mx * c;  // scale > 0, so the max commutes with it
+            bool waited_pv = false;
+            if (kt == 0) {
+                m_used = mnew;
+            } else {
+                const bool need = mnew > m_used + 8.f;
+                if (__any_sync(0xffffffffu, need)) {
+                    if (!warp_wait(bar(kPvDone), (kt - 1) & 1, s_abort)) {
+                        ok = false;
+                        break;
+                    }
+                    waited_pv = true;
+                    tc::tc_fence_after();
+                    const float alpha = need ? fast_exp2(m_used - mnew) : 1.f;
+#pragma unroll
+                    for (int q = 0; q < D / 32; ++q) {
+                        uint32_t o[32];
+                        tc::tmem_ld32(lane_addr + kTmemO + q * 32, o);
+#pragma unroll
+                        for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
+                        tc::tmem_st32(lane_addr + kTmemO + q * 32, o);
+                    }
+                    l *= alpha;
+                    if (need) m_used = mnew;
+                }
+            }
+            const float mu = m_used == -INFINITY ? 0.f : m_used;
+            if (kt >= 1 && !waited_pv) {  // the P buffer is free once P V of the previous tile is done
+                if (!warp_wait(bar(kPvDone), (kt - 1) & 1, s_abort)) {
+                    ok = false;
+                    break;
+                }
+            }
+            // P = 2^(s*c - m) in bf16; l sums the rounded values the MMA will use.
+            const uint32_t prow = base + S::kP;
+#pragma unroll
+            for (int ch = 0; ch < kKeys / 8; ++ch) {
+                uint32_t pk[4];
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    const float x0 = fast_exp2(fmaf(__uint_as_float(sr[ch * 8 + 2 * e]), c, -mu));
+                    const float x1 = fast_exp2(fmaf(__uint_as_float(sr[ch * 8 + 2 * e + 1]), c, -mu));
+                    pk[e] = pack_bf16(x0, x1);
+                    l += bf16_lo(pk[e]) + bf16_hi(pk[e]);
+                }
+                const uint32_t dst = prow + (ch >> 3) * kHalfBytes + sw128(r, ch & 7);
+                asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};\n" ::"r"(dst), "r"(pk[0]), "r"(pk[1]),
+                             "r"(pk[2]), "r"(pk[3])
+                             : "memory");
+            }
+            tc::fence_proxy_async_smem();
+            tc::tc_fence_before();
+            __syncwarp();
+            if (lane == 0) tc::mbar_arrive(bar(kPFull));
+        }
+        if (ok) ok = warp_wait(bar(kPvDone), (ntiles - 1) & 1, s_abort);
+        if (ok) {
+            tc::tc_fence_after();
+            const float inv = valid ? 1.f / l : 0.f;
+            __nv_bfloat16* orow =
+                out + (static_cast<int64_t>(q0 + i0 + (valid ? r / G : 0)) * a.num_q_heads + h * G + r % G) * D;
+#pragma unroll
+            for (int q = 0; q < D / 32; ++q) {
+                uint32_t o[32];
+                tc::tmem_ld32(lane_addr + kTmemO + q * 32, o);
+                if (valid) {
+#pragma unroll
+                    for (int e = 0; e < 32; e += 8) {
+                        uint4 v;
+                        v.x = pack_bf16(__uint_as_float(o[e]) * inv, __uint_as_float(o[e + 1]) * inv);
+                        v.y = pack_bf16(__uint_as_float(o[e + 2]) * inv, __uint_as_float(o[e + 3]) * inv);
+                        v.z = pack_bf16(__uint_as_float(o[e + 4]) * inv, __uint_as_float(o[e + 5]) * inv);
+                        v.w = pack_bf16(__uint_as_float(o[e + 6]) * inv, __uint_as_float(o[e + 7]) * inv);
+                        *reinterpret_cast<uint4*>(orow + q * 32 + e) = v;
+                    }
+                }
+            }
+        } else if (lane == 0) {
+            *s_abort = 1;
+            flag_error(a.err, kDevWaitTimeout);
+        }
+    }
+
+    // ---- teardown: every role is out of its loop; the MMA thread has drained.
+    tc::tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        tc::tc_fence_after();
+        tc::tmem_dealloc(tmem, kTmemCols);
+    }
+}
+
+// --------------------------------------------------------------- host side
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                   const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                   CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+    static EncodeTiledFn fn = nullptr;
+    if (!fn) {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<EncodeTiledFn>(p);
+    }
+    return fn;
+}
+
+int tokens_per_tile(int group) { return group <= kM ? kM / group : 0; }
+
+int tiles_bound(const Args& a) {
+    const int tq = tokens_per_tile(a.group);
+    if (tq == 0) return 0;
+    return static_cast<int>((a.num_tokens + tq - 1) / tq + a.num_seqs);
+}
+
+template <int D>
+cudaError_t launch_d(const Args& a, cudaStream_t stream) {
+    using S = Smem<D>;
+    static bool configured[64] = {};
+    int dev = 0;
+    cudaGetDevice(&dev);
+    if (!configured[dev & 63]) {
+        cudaError_t e = cudaFuncSetAttribute(prefill_tc_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             S::kAlloc);
+        if (e != cudaSuccess) return e;
+        configured[dev & 63] = true;
+    }
+    const int64_t ctas = prefill_ctas(a);
+    if (ctas == 0) return cudaSuccess;
+    EncodeTiledFn enc = encode_fn();
+    if (!enc) return cudaErrorNotSupported;
+    const int G = a.group, tq = tokens_per_tile(G);
+    CUtensorMap tq_map, tk_map, tv_map;
+    {
+        // q [T, Hq, D] as (D, Hq, T); one box = 64 columns x G heads x TQ tokens
+        const cuuint64_t dims[3] = {static_cast<cuuint64_t>(D), static_cast<cuuint64_t>(a.num_q_heads),
+                                    static_cast<cuuint64_t>(a.num_tokens)};
+        const cuuint64_t strides[2] = {static_cast<cuuint64_t>(D) * 2,
+                                       static_cast<cuuint64_t>(a.num_q_heads) * D * 2};
+        const cuuint32_t box[3] = {64, static_cast<cuuint32_t>(G), static_cast<cuuint32_t>(tq)};
+        const cuuint32_t es[3] = {1, 1, 1};
+        if (enc(&tq_map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(a.q), dims, strides, box, es,
+                CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+            return cudaErrorInvalidValue;
+    }
+    {
+        // cache [NB, P, Hkv, D] as (D, Hkv, P, NB); one box = 64 columns x 1 head x 16 slots of one page
+        const cuuint64_t dims[4] = {static_cast<cuuint64_t>(D), static_cast<cuuint64_t>(a.num_kv_heads),
+                                    static_cast<cuuint64_t>(kPage), static_cast<cuuint64_t>(a.num_blocks)};
+        const cuuint64_t strides[3] = {static_cast<cuuint64_t>(D) * 2,
+                                       static_cast<cuuint64_t>(a.num_kv_heads) * D * 2,
+                                       static_cast<cuuint64_t>(kPage) * a.num_kv_heads * D * 2};
+        const cuuint32_t box[4] = {64, 1, kPage, 1};
+        const cuuint32_t es[4] = {1, 1, 1, 1};
+        if (enc(&tk_map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(a.k_cache), dims, strides, box, es,
+                CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+            return cudaErrorInvalidValue;
+        if (enc(&tv_map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(a.v_cache), dims, strides, box, es,
+                CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+            return cudaErrorInvalidValue;
+    }
+    prefill_tc_kernel<D><<<static_cast<unsigned>(ctas), kThreads, S::kAlloc, stream>>>(tq_map, tk_map, tv_map, a, tq,
+                                                                                       tiles_bound(a));
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+int64_t prefill_ctas(const Args& a) {
+    if (a.num_tokens < 2) return 0;
+    return static_cast<int64_t>(tiles_bound(a)) * a.num_kv_heads;
+}
+
+cudaError_t launch_prefill(const Args& a, cudaStream_t stream) {
+    switch (a.head_dim) {
+        case 64: return launch_d<64>(a, stream);
+        case 128: return launch_d<128>(a, stream);
+        default: return cudaErrorInvalidValue;
+    }
+}
+
+}  // namespace pa
