@@ -158,6 +158,32 @@ pa_status pa_release_workspaces(void);
 const char* pa_status_string(pa_status status);
 const char* pa_last_error(void);
 
+/*
+ * pa_forward without any allocation.  The pages this library follows have no
+ * counterpart of this call; it exists for callers that cannot let a library
+ * allocate device memory: code running while a stream is captured into a CUDA
+ * graph (allocation is refused there), hosts whose device memory is owned or
+ * budgeted by their own allocator, and latency-critical loops where an
+ * allocation's cost or failure at an arbitrary call is not acceptable.
+ *
+ * Same arguments and result as pa_forward, plus device_error: a device int32
+ * that receives the first device-side error code (as pa_device_error reports
+ * them; the caller zeroes it), or NULL to discard the codes.  The split-KV
+ * scratch is a fixed 32 MiB array in the library's device image instead of an
+ * allocation; a GPU holds it from the time the library's code is loaded there
+ * (at the latest this call's first use) until the process exits.  Shapes whose
+ * pa_plan(...).workspace_bytes exceed 32 MiB are rejected with
+ * PA_ERR_UNSUPPORTED before any launch.  Every call on a device shares that one
+ * array, which keeps the last call's contents: calls that overlap on the GPU
+ * (unordered streams) race, so order them on one stream.  The first call on each
+ * device looks up the array's address with that device current; make it before
+ * any stream capture.  It calls no cudaMalloc, cudaFree or allocating routine.
+ */
+pa_status pa_forward_noalloc(const void* q, const void* k_cache, const void* v_cache,
+                             const int32_t* block_table, const int32_t* seq_lens,
+                             const int32_t* query_start_loc, void* out, float scale,
+                             const pa_dims* dims, int32_t* device_error, void* stream);
+
 /* Library version, major * 10000 + minor * 100 + patch. */
 int32_t pa_version(void);
 

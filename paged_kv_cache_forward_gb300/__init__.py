@@ -14,6 +14,7 @@ from .binding import (  # noqa: F401
     PagedAttnError,
     device_error,
     forward,
+    forward_noalloc,
     load,
     make_dims,
     plan,

@@ -24,7 +24,7 @@ PA_OK, PA_ERR_INVALID_ARG, PA_ERR_UNSUPPORTED, PA_ERR_NOT_PREPARED, PA_ERR_CUDA 
 # Every symbol include/pagedattn.h declares.
 EXPORTED = (
     "pa_forward", "pa_forward_ex", "pa_plan", "pa_prepare", "pa_device_error",
-    "pa_release_workspaces", "pa_status_string", "pa_last_error", "pa_version",
+    "pa_release_workspaces", "pa_status_string", "pa_last_error", "pa_version", "pa_forward_noalloc",
 )
 
 DEVICE_ERRORS = {
@@ -99,6 +99,7 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
     fwd = [P, P, P, P, P, P, P, ctypes.c_float, ctypes.POINTER(Dims)]
     lib.pa_forward.argtypes = fwd + [P]
     lib.pa_forward_ex.argtypes = fwd + [ctypes.POINTER(Options), P]
+    lib.pa_forward_noalloc.argtypes = fwd + [P, P]
     lib.pa_plan.argtypes = [ctypes.POINTER(Dims), ctypes.POINTER(Options), ctypes.POINTER(PlanInfo)]
     lib.pa_prepare.argtypes = [ctypes.POINTER(Dims), ctypes.POINTER(Options), P]
     lib.pa_device_error.argtypes = [P, ctypes.POINTER(ctypes.c_int32)]
@@ -109,7 +110,7 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.pa_last_error.restype = ctypes.c_char_p
     lib.pa_version.argtypes = []
     for name in ("pa_forward", "pa_forward_ex", "pa_plan", "pa_prepare", "pa_device_error",
-                 "pa_release_workspaces", "pa_version"):
+                 "pa_release_workspaces", "pa_version", "pa_forward_noalloc"):
         getattr(lib, name).restype = I32
     _lib = lib
     return lib
@@ -198,6 +199,26 @@ def forward(q, k_cache, v_cache, block_table, seq_lens, query_start_loc, out=Non
         _check(lib.pa_forward_ex(*args, ctypes.byref(opts), s))
     else:
         _check(lib.pa_forward(*args, s))
+    return out
+
+
+def forward_noalloc(q, k_cache, v_cache, block_table, seq_lens, query_start_loc, out=None,
+                    scale: Optional[float] = None, device_error=None, stream=None) -> torch.Tensor:
+    """pa_forward_noalloc: the forward pass using the library's fixed scratch
+    array instead of an allocated workspace (for callers that cannot allocate).
+    ``device_error`` (optional) is a CUDA int32 tensor of one element that
+    receives the first device-side error code; the caller zeroes it."""
+    if out is None:
+        out = torch.empty_like(q)
+    _check_tensors(q, k_cache, v_cache, block_table, seq_lens, query_start_loc, out)
+    if device_error is not None and (device_error.dtype != torch.int32 or not device_error.is_cuda):
+        raise TypeError("device_error must be a CUDA int32 tensor")
+    if scale is None:
+        scale = 1.0 / math.sqrt(q.shape[-1])
+    dims = make_dims(q.shape, k_cache.shape, block_table.shape, seq_lens.shape[0])
+    _check(load().pa_forward_noalloc(
+        _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(block_table), _ptr(seq_lens), _ptr(query_start_loc),
+        _ptr(out), ctypes.c_float(scale), ctypes.byref(dims), _ptr(device_error), _stream_handle(stream)))
     return out
 
 

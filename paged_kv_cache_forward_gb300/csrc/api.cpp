@@ -197,6 +197,11 @@ pa_status record(void* ev, cudaStream_t s, bool capturing) {
 
 }  // namespace
 
+namespace pa {
+// Lets other translation units of the library report through pa_last_error().
+void set_last_error(const char* msg) { snprintf(g_last_error, sizeof g_last_error, "%s", msg); }
+}  // namespace pa
+
 extern "C" {
 
 pa_status pa_plan(const pa_dims* dims, const pa_options* opts, pa_plan_info* info) {

@@ -42,6 +42,9 @@ cudaError_t launch_decode(const Args& a, cudaStream_t stream);
 cudaError_t launch_combine(const Args& a, cudaStream_t stream);
 cudaError_t launch_prefill(const Args& a, cudaStream_t stream);
 
+// Sets the calling thread's pa_last_error() text.
+void set_last_error(const char* msg);
+
 // Static grid sizes (functions of shapes only), shared with the planner.
 int64_t decode_ctas(const Args& a);
 int64_t combine_ctas(const Args& a);
