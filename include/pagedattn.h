@@ -110,7 +110,8 @@ typedef struct {
     int32_t kv_chunk;         /* keys per split                                */
     int32_t splits;           /* splits of the longest possible sequence       */
     int64_t decode_ctas;      /* decode kernel grid                            */
-    int64_t combine_ctas;     /* log-sum-exp combine kernel grid (0 if unused)  */
+    int64_t combine_ctas;     /* 0: the log-sum-exp merge of the splits runs in
+                                 the decode kernel (last split CTA to finish) */
     int64_t prefill_ctas;     /* prefill kernel grid                           */
     int64_t workspace_bytes;  /* scratch this call needs                       */
     int32_t launches;         /* kernels launched per pa_forward               */

@@ -55,6 +55,7 @@ def _compile(src: str, verbose_ptxas: bool) -> tuple:
            "-I", INCLUDE, "-I", CSRC, "-c", src, "-o", obj]
     if verbose_ptxas and src.endswith(".cu"):
         cmd += ["-Xptxas", "-v"]
+    cmd += os.environ.get("PA_NVCC_EXTRA", "").split()  # offline sweeps build variants this way
     r = subprocess.run(cmd, capture_output=True, text=True)
     return obj, r.returncode, r.stdout + r.stderr, " ".join(cmd)
 

@@ -113,13 +113,14 @@ pa_status make_plan(const pa_dims* d, const pa_options* o, Plan* p) {
         return PA_OK;
     }
     p->decode_ctas = pa::decode_ctas(a);
-    p->combine_ctas = pa::combine_ctas(a);
+    p->combine_ctas = 0;  // the log-sum-exp merge runs inside the decode kernel
     p->prefill_ctas = pa::prefill_ctas(a);
-    if (p->decode_ctas > kMaxCtas || p->combine_ctas > kMaxCtas || p->prefill_ctas > kMaxCtas)
+    if (p->decode_ctas > kMaxCtas || p->prefill_ctas > kMaxCtas)
         return fail(PA_ERR_UNSUPPORTED, "launch grid above 2^31-1 CTAs; use a larger kv_chunk");
-    p->launches = (p->decode_ctas > 0) + (p->combine_ctas > 0) + (p->prefill_ctas > 0);
-    const int64_t partial_rows = a.splits > 1 ? static_cast<int64_t>(d->num_seqs) * a.splits * d->num_q_heads : 0;
-    p->ws_bytes = kErrWordBytes + partial_rows * d->head_dim * 4 + partial_rows * 2 * 4;
+    p->launches = (p->decode_ctas > 0) + (p->prefill_ctas > 0);
+    p->ws_bytes = pa::workspace_layout(d->num_seqs, d->num_kv_heads, a.row_groups, a.splits, d->num_q_heads,
+                                       d->head_dim)
+                      .bytes;
     return PA_OK;
 }
 
@@ -136,7 +137,7 @@ std::vector<Workspace> g_ws;       // live, one per (device, stream)
 std::vector<Workspace> g_retired;  // outgrown buffers, kept for captured graphs
 
 // Returns the workspace of (device, stream) with at least `bytes`, growing it if
-// allowed.  The error word at its start is zeroed whenever a buffer is created.
+// allowed.  A new buffer is zeroed (error word and split counters start at 0).
 pa_status get_workspace(cudaStream_t stream, int64_t bytes, bool may_grow, void** out) {
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
@@ -156,7 +157,7 @@ pa_status get_workspace(cudaStream_t stream, int64_t bytes, bool may_grow, void*
     void* p = nullptr;
     e = cudaMalloc(&p, static_cast<size_t>(bytes));
     if (e != cudaSuccess) return cuda_fail(e, "cudaMalloc(workspace)");
-    e = cudaMemsetAsync(p, 0, kErrWordBytes, stream);
+    e = cudaMemsetAsync(p, 0, static_cast<size_t>(bytes), stream);
     if (e == cudaSuccess && w) {
         // carry the old sticky error over, then retire the old buffer
         e = cudaMemcpyAsync(p, w->ptr, sizeof(int32_t), cudaMemcpyDeviceToDevice, stream);
@@ -261,10 +262,11 @@ pa_status pa_forward_ex(const void* q, const void* k_cache, const void* v_cache,
     a.query_start_loc = query_start_loc;
     a.out = out;
     a.err = static_cast<int32_t*>(ws);
-    float* partials = reinterpret_cast<float*>(static_cast<char*>(ws) + kErrWordBytes);
-    const int64_t partial_rows = a.splits > 1 ? static_cast<int64_t>(a.num_seqs) * a.splits * a.num_q_heads : 0;
-    a.ws_o = partials;
-    a.ws_ml = partials + partial_rows * a.head_dim;
+    const pa::WorkspaceLayout wl =
+        pa::workspace_layout(a.num_seqs, a.num_kv_heads, a.row_groups, a.splits, a.num_q_heads, a.head_dim);
+    a.counters = reinterpret_cast<int32_t*>(static_cast<char*>(ws) + wl.counters_off);
+    a.ws_o = reinterpret_cast<float*>(static_cast<char*>(ws) + wl.o_off);
+    a.ws_ml = reinterpret_cast<float*>(static_cast<char*>(ws) + wl.ml_off);
     a.scale = scale;
     a.scale_log2 = scale * 1.4426950408889634f;
 
@@ -272,7 +274,6 @@ pa_status pa_forward_ex(const void* q, const void* k_cache, const void* v_cache,
     if ((st = record(opts ? opts->decode_start_event : nullptr, s, capturing)) != PA_OK) return st;
     if ((e = pa::launch_decode(a, s)) != cudaSuccess) return cuda_fail(e, "decode launch");
     if ((st = record(opts ? opts->decode_stop_event : nullptr, s, capturing)) != PA_OK) return st;
-    if ((e = pa::launch_combine(a, s)) != cudaSuccess) return cuda_fail(e, "combine launch");
     if ((st = record(opts ? opts->prefill_start_event : nullptr, s, capturing)) != PA_OK) return st;
     if ((e = pa::launch_prefill(a, s)) != cudaSuccess) return cuda_fail(e, "prefill launch");
     if ((st = record(opts ? opts->prefill_stop_event : nullptr, s, capturing)) != PA_OK) return st;

@@ -9,14 +9,17 @@
 // Softmax" item of the same list.
 //
 // Inside the CTA, 4 warps take pages round-robin.  Each warp runs its own
-// 3-stage cp.async pipeline of one 16-token page of K and V (16-byte copies into
+// 2-stage cp.async pipeline of one 16-token page of K and V (16-byte copies into
 // an XOR-swizzled layout, so the ldmatrix fragment loads are bank-conflict free),
 // computes S = Q K^T and O += P V with bf16 m16n8k16 MMAs (the G <= 16 query
 // rows padded to 16), and keeps an online softmax (running max m, sum l; the
 // recurrence of "The Flash Attention revolution" on the GPU programming guide
 // page) in the log2 domain.  At the end the 4 warps' (m, l, O) are merged in
-// shared memory; a sequence with one split writes bf16 out directly, otherwise
-// the unnormalised partial goes to the workspace for the combine kernel.
+// shared memory; a sequence with one split writes bf16 out directly.  With
+// several splits each CTA writes its unnormalised partial (O, m, l) to the
+// workspace and takes a ticket from a per-(sequence, KV head) counter; the CTA
+// that draws the last ticket merges all splits by log-sum-exp (no CTA waits
+// for another, so there is no spin and no second launch).
 //
 // HBM-bound: per CTA it streams (end - start) * D * 2 bytes of K and as many of
 // V, which is the whole algorithmic traffic of decode.  The contraction has only
@@ -31,8 +34,16 @@
 namespace pa {
 namespace {
 
-constexpr int kWarps = 4;
-constexpr int kStages = 3;
+// Warps per CTA and pipeline stages per warp (the offline sweep's choice; a
+// build may override them with -DPA_DECODE_WARPS=.. -DPA_DECODE_STAGES=..).
+#ifndef PA_DECODE_WARPS
+#define PA_DECODE_WARPS 4
+#endif
+#ifndef PA_DECODE_STAGES
+#define PA_DECODE_STAGES 2
+#endif
+constexpr int kWarps = PA_DECODE_WARPS;
+constexpr int kStages = PA_DECODE_STAGES;
 constexpr int kPage = 16;
 constexpr int kRows = 16;  // MMA M: query-head rows per CTA
 
@@ -54,6 +65,78 @@ struct DecodeTile {
 template <int D>
 __device__ __forceinline__ uint32_t swz(int r, int c) {
     return r * DecodeTile<D>::kRowBytes + ((c ^ (r & 7)) << 4);
+}
+
+// Log-sum-exp merge of the nsplits partials of rows hq0 .. hq0+rows-1 of
+// sequence b (the last step of "Parallel Tiled Softmax"): M = max_s m_s,
+// w_s = 2^(m_s - M), out = sum_s w_s O_s / sum_s w_s l_s.  The partials were
+// written by other CTAs, so they are read with L2-coherent loads.
+template <int D>
+__device__ __forceinline__ void merge_splits(const Args& a, int b, int hq0, int rows, int nsplits, int q0,
+                                             float* sm) {
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    float* s_m = sm;         // per-row max
+    float* s_inv = sm + kRows;  // per-row 1 / denominator
+    const int64_t split_ml = static_cast<int64_t>(a.num_q_heads) * 2;  // stride between splits in ws_ml
+    const int64_t split_o = static_cast<int64_t>(a.num_q_heads) * D;   // ... and in ws_o
+    const int64_t row0 = static_cast<int64_t>(b) * a.splits * a.num_q_heads + hq0;
+    for (int r = warp; r < rows; r += kWarps) {
+        const float* ml = a.ws_ml + (row0 + r) * 2;
+        float M = -INFINITY;
+        for (int s = lane; s < nsplits; s += 32) M = fmaxf(M, __ldcg(ml + s * split_ml));
+        M = warp_max(M);
+        float den = 0.f;
+        for (int s = lane; s < nsplits; s += 32)
+            den += fast_exp2(__ldcg(ml + s * split_ml) - M) * __ldcg(ml + s * split_ml + 1);
+        den = warp_sum(den);
+        if (lane == 0) {
+            s_m[r] = M;
+            s_inv[r] = 1.f / den;
+        }
+    }
+    __syncthreads();
+    __nv_bfloat16* out = reinterpret_cast<__nv_bfloat16*>(a.out);
+    constexpr int kGroups = D / 4;  // 4 consecutive columns per work item
+    for (int it = threadIdx.x; it < rows * kGroups; it += blockDim.x) {
+        const int r = it / kGroups;
+        const int d4 = (it % kGroups) * 4;
+        const float M = s_m[r];
+        const float* ml = a.ws_ml + (row0 + r) * 2;
+        const float* os = a.ws_o + (row0 + r) * D + d4;
+        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+        int s = 0;
+        for (; s + 8 <= nsplits; s += 8) {  // 8 independent loads in flight
+            float m8[8];
+            float4 v8[8];
+#pragma unroll
+            for (int k = 0; k < 8; ++k) {
+                m8[k] = __ldcg(ml + (s + k) * split_ml);
+                v8[k] = __ldcg(reinterpret_cast<const float4*>(os + (s + k) * split_o));
+            }
+#pragma unroll
+            for (int k = 0; k < 8; ++k) {
+                const float w = fast_exp2(m8[k] - M);
+                acc.x += w * v8[k].x;
+                acc.y += w * v8[k].y;
+                acc.z += w * v8[k].z;
+                acc.w += w * v8[k].w;
+            }
+        }
+        for (; s < nsplits; ++s) {
+            const float w = fast_exp2(__ldcg(ml + s * split_ml) - M);
+            const float4 v = __ldcg(reinterpret_cast<const float4*>(os + s * split_o));
+            acc.x += w * v.x;
+            acc.y += w * v.y;
+            acc.z += w * v.z;
+            acc.w += w * v.w;
+        }
+        const float inv = s_inv[r];
+        uint2 packed;
+        packed.x = pack_bf16(acc.x * inv, acc.y * inv);
+        packed.y = pack_bf16(acc.z * inv, acc.w * inv);
+        *reinterpret_cast<uint2*>(out + (static_cast<int64_t>(q0) * a.num_q_heads + hq0 + r) * D + d4) = packed;
+    }
 }
 
 template <int D>
@@ -278,6 +361,21 @@ __global__ void __launch_bounds__(kWarps * 32) decode_splitkv_kernel(const Args 
             }
         }
     }
+    if (nsplits == 1) return;
+
+    // Split merge.  Each split CTA publishes its partial, then takes a ticket;
+    // the one that draws the last ticket merges every split of (b, h, rg) and
+    // resets the counter for the next call.  Nobody waits on anybody.
+    __shared__ int s_last;
+    __threadfence();
+    __syncthreads();
+    int32_t* counter = a.counters + (static_cast<int64_t>(b) * a.num_kv_heads + h) * a.row_groups + rg;
+    if (threadIdx.x == 0) s_last = atomicAdd(counter, 1) == nsplits - 1;
+    __syncthreads();
+    if (!s_last) return;
+    __threadfence();
+    merge_splits<D>(a, b, hq0, rows, nsplits, q0, reinterpret_cast<float*>(smem));
+    if (threadIdx.x == 0) *counter = 0;
 }
 
 template <int D>

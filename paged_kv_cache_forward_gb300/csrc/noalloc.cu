@@ -36,7 +36,6 @@
 namespace {
 
 constexpr int64_t kNoAllocScratchBytes = 32ll << 20;
-constexpr int64_t kHeaderBytes = 256;  // error word slot, then the partials
 constexpr int kMaxDevices = 64;
 
 static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
@@ -125,10 +124,12 @@ extern "C" pa_status pa_forward_noalloc(const void* q, const void* k_cache, cons
     a.row_groups = (a.group + 15) / 16;
     a.scale = scale;
     a.scale_log2 = scale * 1.4426950408889634f;
-    float* partials = reinterpret_cast<float*>(static_cast<unsigned char*>(scratch) + kHeaderBytes);
-    const int64_t partial_rows = a.splits > 1 ? static_cast<int64_t>(a.num_seqs) * a.splits * a.num_q_heads : 0;
-    a.ws_o = partials;
-    a.ws_ml = partials + partial_rows * a.head_dim;
+    const pa::WorkspaceLayout wl =
+        pa::workspace_layout(a.num_seqs, a.num_kv_heads, a.row_groups, a.splits, a.num_q_heads, a.head_dim);
+    unsigned char* const sb = static_cast<unsigned char*>(scratch);
+    a.counters = reinterpret_cast<int32_t*>(sb + wl.counters_off);
+    a.ws_o = reinterpret_cast<float*>(sb + wl.o_off);
+    a.ws_ml = reinterpret_cast<float*>(sb + wl.ml_off);
     if (device_error) {
         a.err = device_error;
     } else {
@@ -136,10 +137,15 @@ extern "C" pa_status pa_forward_noalloc(const void* q, const void* k_cache, cons
         cudaError_t e = cudaMemsetAsync(scratch, 0, sizeof(int32_t), s);
         if (e != cudaSuccess) return report(PA_ERR_CUDA, "cudaMemsetAsync(error word) failed");
     }
-    // The split partials are written before they are read within one call, so
-    // they need no clearing.
+    // The split ticket counters must start at zero: clear them (a completed call
+    // leaves them zero, but the array is shared and the last call may not have
+    // completed normally).  The partials are written before they are read within
+    // one call, so they need no clearing.
+    if (wl.o_off > wl.counters_off) {
+        cudaError_t e = cudaMemsetAsync(sb + wl.counters_off, 0, static_cast<size_t>(wl.o_off - wl.counters_off), s);
+        if (e != cudaSuccess) return report(PA_ERR_CUDA, "cudaMemsetAsync(split counters) failed");
+    }
     cudaError_t e = pa::launch_decode(a, s);
-    if (e == cudaSuccess) e = pa::launch_combine(a, s);
     if (e == cudaSuccess) e = pa::launch_prefill(a, s);
     if (e != cudaSuccess) {
         char msg[256];

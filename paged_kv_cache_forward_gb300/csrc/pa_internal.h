@@ -27,6 +27,7 @@ struct Args {
     void* out;                       // [T, Hq, D] bf16
     float* ws_o;    // split partials: [B, splits, Hq, D] fp32 (unnormalised O)
     float* ws_ml;   // [B, splits, Hq, 2] fp32: running max (log2 domain) and sum
+    int32_t* counters;  // split tickets [B, Hkv, row_groups]; zero between calls
     int32_t* err;   // sticky device error word
     int64_t num_tokens;
     int64_t num_blocks;
@@ -39,15 +40,31 @@ struct Args {
 };
 
 cudaError_t launch_decode(const Args& a, cudaStream_t stream);
-cudaError_t launch_combine(const Args& a, cudaStream_t stream);
 cudaError_t launch_prefill(const Args& a, cudaStream_t stream);
+
+// Workspace layout shared by pa_forward and pa_forward_noalloc: a 256-byte
+// header (sticky error word), the split ticket counters (must be zero before a
+// call; each call leaves them zero), then the partials O and (m, l).
+struct WorkspaceLayout {
+    int64_t counters_off, o_off, ml_off, bytes;
+};
+inline WorkspaceLayout workspace_layout(int64_t num_seqs, int32_t num_kv_heads, int32_t row_groups, int32_t splits,
+                                        int32_t num_q_heads, int32_t head_dim) {
+    WorkspaceLayout w{};
+    const int64_t counters = splits > 1 ? num_seqs * num_kv_heads * row_groups : 0;
+    const int64_t rows = splits > 1 ? num_seqs * splits * num_q_heads : 0;
+    w.counters_off = 256;
+    w.o_off = w.counters_off + ((counters * 4 + 255) / 256) * 256;
+    w.ml_off = w.o_off + rows * head_dim * 4;
+    w.bytes = w.ml_off + rows * 2 * 4;
+    return w;
+}
 
 // Sets the calling thread's pa_last_error() text.
 void set_last_error(const char* msg);
 
 // Static grid sizes (functions of shapes only), shared with the planner.
 int64_t decode_ctas(const Args& a);
-int64_t combine_ctas(const Args& a);
 int64_t prefill_ctas(const Args& a);
 
 }  // namespace pa
