@@ -13,19 +13,23 @@
 // O += P V, out = O / l.
 //
 // Warp roles (192 threads):
-//   warp 0      TMA producer: Q once, then K and V page boxes (64 x 16 rows of
-//               128 B, 128-byte swizzle) per KV tile into a 2-stage ring.  The
-//               one page of V that holds the sequence end is copied by plain
-//               loads with zero fill, so no slot past seq_len reaches the MMA.
-//   warp 1      allocates TMEM (S double buffer + O: 384 of 512 columns); its
-//               lane 0 issues the MMAs: S(kt) = Q K(kt)^T (M=128, N=128, K=D) into
-//               TMEM, then O += P(kt-1) V(kt-1) (N=D, K=128) so that the softmax of
-//               tile kt overlaps the MMAs of the neighbours.
+//   warp 0      TMA producer: Q once, then per KV tile the K page boxes and the
+//               V page boxes (64 columns x 16 slots of one page and head, 128-byte
+//               swizzle) into separate 3-stage K and V rings, so a K stage is
+//               refilled as soon as its S MMA is done.  Block-table entries are
+//               fetched one group of 4 tiles ahead.  The one page of V that holds
+//               the sequence end is copied by plain loads with zero fill, so no
+//               slot past seq_len reaches the MMA.
+//   warp 1      allocates all 512 TMEM columns (S double buffer, O, P double
+//               buffer); its lane 0 issues the MMAs: S(kt) = Q K(kt)^T (M=128,
+//               N=128, K=D, both operands from shared memory) into TMEM, then
+//               O += P(kt-1) V(kt-1) (A = P read from TMEM, B = V MN-major in shared
+//               memory), so that the softmax of tile kt overlaps the MMAs.
 //   warps 2-5   softmax, one thread per row (TMEM lane): load S from TMEM,
-//               mask, running max in log2 units, P = 2^(x - m) to bf16 in shared
-//               memory (K-major, 128-byte swizzle) for the P V MMA.  The running
-//               max is only moved (and O in TMEM rescaled) when the row max grows
-//               by more than 2^8; the final O / l is exact either way.
+//               mask, running max in log2 units, P = 2^(x - m) as bf16 pairs
+//               stored straight into TMEM.  The running max is only moved (and O
+//               in TMEM rescaled) when the row max grows by more than 2^8; the
+//               final O / l is exact either way.
 // Every wait on an mbarrier is bounded (2 s); on timeout the CTA records
 // kDevWaitTimeout, stops all roles, drains the MMAs it issued, frees TMEM and
 // exits.
@@ -49,25 +53,37 @@ constexpr int kPagesPerTile = kKeys / kPage;
 constexpr int kHalfBytes = 128 * 128;  // 128 rows x 128 B: one 64-column half of a tile
 constexpr uint64_t kTimeoutNs = 2000000000ull;
 constexpr uint32_t kTmemCols = 512;
-constexpr uint32_t kTmemS0 = 0, kTmemS1 = 128, kTmemO = 256;
+constexpr uint32_t kTmemS0 = 0, kTmemS1 = 128, kTmemO = 256, kTmemP0 = 384, kTmemP1 = 448;
+constexpr int kKStages = 3, kVStages = 3;
+constexpr int kTilesPerGroup = 4;  // block-table prefetch: 4 tiles x 8 pages = one entry per lane
 
 template <int D>
 struct Smem {
     static constexpr int kHalves = D / 64;
+    static constexpr int kTile = kHalves * kHalfBytes;  // one K or V tile (128 keys x D)
     static constexpr int kQ = 0;
-    static constexpr int kK0 = kQ + kHalves * kHalfBytes;
-    static constexpr int kStage = kHalves * kHalfBytes;  // one K or V tile
-    static constexpr int kV0 = kK0 + 2 * kStage;
-    static constexpr int kP = kV0 + 2 * kStage;
-    static constexpr int kBar = kP + 2 * kHalfBytes;  // P: 128 keys = 2 halves
-    // barriers: q_full, kv_full[2], kv_empty[2], s_full[2], s_free[2], p_full, pv_done, drain
-    static constexpr int kNumBars = 12;
+    static constexpr int kK0 = kQ + kTile;
+    static constexpr int kV0 = kK0 + kKStages * kTile;
+    static constexpr int kBar = kV0 + kVStages * kTile;
+    static constexpr int kNumBars = 22;
     static constexpr int kMisc = kBar + kNumBars * 8;  // tmem address, abort flag, tile info
     static constexpr int kBytes = kMisc + 64;
     static constexpr int kAlloc = kBytes + 1024;  // slack to align the base to 1024
 };
 
-enum Bar { kQFull = 0, kKvFull0 = 1, kKvEmpty0 = 3, kSFull0 = 5, kSFree0 = 7, kPFull = 9, kPvDone = 10, kDrain = 11 };
+// barrier indices
+enum Bar {
+    kQFull = 0,
+    kKFull0 = 1,     // [3]
+    kKEmpty0 = 4,    // [3]
+    kVFull0 = 7,     // [3]
+    kVEmpty0 = 10,   // [3]
+    kSFull0 = 13,    // [2]
+    kSFree0 = 15,    // [2]
+    kPFull0 = 17,    // [2]
+    kPvDone0 = 19,   // [2]
+    kDrain = 21,
+};
 
 __device__ __forceinline__ int tiles_of(int n, int tq) { return n >= 2 ? (n + tq - 1) / tq : 0; }
 
@@ -166,14 +182,20 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ---- barriers and TMEM
     if (threadIdx.x == 0) {
         tc::mbar_init(bar(kQFull), 1);
+        for (int i = 0; i < kKStages; ++i) {
+            tc::mbar_init(bar(kKFull0 + i), 1);
+            tc::mbar_init(bar(kKEmpty0 + i), 1);
+        }
+        for (int i = 0; i < kVStages; ++i) {
+            tc::mbar_init(bar(kVFull0 + i), 1);
+            tc::mbar_init(bar(kVEmpty0 + i), 1);
+        }
         for (int i = 0; i < 2; ++i) {
-            tc::mbar_init(bar(kKvFull0 + i), 1);
-            tc::mbar_init(bar(kKvEmpty0 + i), 1);
             tc::mbar_init(bar(kSFull0 + i), 1);
             tc::mbar_init(bar(kSFree0 + i), 4);
+            tc::mbar_init(bar(kPFull0 + i), 4);
+            tc::mbar_init(bar(kPvDone0 + i), 1);
         }
-        tc::mbar_init(bar(kPFull), 4);
-        tc::mbar_init(bar(kPvDone), 1);
         tc::mbar_init(bar(kDrain), 1);
         tc::fence_mbar_init();
     }
@@ -199,30 +221,55 @@ __global__ void __launch_bounds__(kThreads, 1)
                 tc::tma_load_3d(base + S::kQ + hf * kHalfBytes, &tm_q, bar(kQFull), hf * 64, h * G, q0 + i0);
         }
         const int32_t* bt = a.block_table + static_cast<int64_t>(b) * a.max_pages;
-        for (int kt = 0; kt < ntiles && ok; ++kt) {
-            const int st = kt & 1;
-            if (kt >= 2 && !warp_wait(bar(kKvEmpty0 + st), ((kt >> 1) - 1) & 1, s_abort)) {
-                ok = false;
-                break;
+        // lane l holds the block-table entry of page (group * 32 + l); the next
+        // group's entries are loaded while the current group is being used.
+        auto load_group = [&](int grp) -> int {
+            const int pg = grp * kTilesPerGroup * kPagesPerTile + lane;
+            return pg < last_page ? bt[pg] : 0;
+        };
+        int cur_grp = load_group(0);
+        int next_grp = load_group(1);
+        const __nv_bfloat16* vc = reinterpret_cast<const __nv_bfloat16*>(a.v_cache);
+        for (int kt = 0; kt < ntiles; ++kt) {
+            const int slot = kt % kTilesPerGroup;
+            if (slot == 0 && kt > 0) {
+                cur_grp = next_grp;
+                next_grp = load_group(kt / kTilesPerGroup + 1);
             }
             const int p0 = kt * kPagesPerTile;
             const int np = min(kPagesPerTile, last_page - p0);
             const int nv = max(0, min(np, full_pages - p0));  // V pages by TMA
-            int page = 0;
-            if (lane < np) {
-                page = bt[p0 + lane];
-                if (static_cast<uint32_t>(page) >= static_cast<uint64_t>(a.num_blocks)) {
-                    flag_error(a.err, kDevBadBlock);
-                    page = 0;
-                }
+            int page = __shfl_sync(0xffffffffu, cur_grp, (slot * kPagesPerTile + lane) & 31);
+            if (lane < np && static_cast<uint32_t>(page) >= static_cast<uint64_t>(a.num_blocks)) {
+                flag_error(a.err, kDevBadBlock);
+                page = 0;
             }
-            const uint32_t sk = base + S::kK0 + st * S::kStage;
-            const uint32_t sv = base + S::kV0 + st * S::kStage;
+            // ---- K(kt)
+            const int kst = kt % kKStages;
+            if (kt >= kKStages && !warp_wait(bar(kKEmpty0 + kst), (kt / kKStages - 1) & 1, s_abort)) {
+                ok = false;
+                break;
+            }
+            const uint32_t sk = base + S::kK0 + kst * S::kTile;
+            if (lane == 0) tc::mbar_arrive_expect_tx(bar(kKFull0 + kst), np * S::kHalves * 2048);
+            __syncwarp();
+            if (lane < np) {
+#pragma unroll
+                for (int hf = 0; hf < S::kHalves; ++hf)
+                    tc::tma_load_4d(sk + hf * kHalfBytes + lane * 2048, &tm_k, bar(kKFull0 + kst), hf * 64, h, 0,
+                                    page);
+            }
+            // ---- V(kt)
+            const int vst = kt % kVStages;
+            if (kt >= kVStages && !warp_wait(bar(kVEmpty0 + vst), (kt / kVStages - 1) & 1, s_abort)) {
+                ok = false;
+                break;
+            }
+            const uint32_t sv = base + S::kV0 + vst * S::kTile;
             if (nv < np) {
                 // The page holding the sequence end: plain loads, slots >= L as zeros.
                 const int pi = np - 1;
                 const int pg = __shfl_sync(0xffffffffu, page, pi);
-                const __nv_bfloat16* vc = reinterpret_cast<const __nv_bfloat16*>(a.v_cache);
                 for (int c = lane; c < kPage * (D / 8); c += 32) {
                     const int t = c / (D / 8), ch = c % (D / 8);
                     const int row = pi * kPage + t;
@@ -238,18 +285,13 @@ __global__ void __launch_bounds__(kThreads, 1)
                 tc::fence_proxy_async_smem();
             }
             __syncwarp();
-            if (lane == 0)
-                tc::mbar_arrive_expect_tx(bar(kKvFull0 + st), (np + nv) * S::kHalves * 2048);
+            if (lane == 0) tc::mbar_arrive_expect_tx(bar(kVFull0 + vst), nv * S::kHalves * 2048);
             __syncwarp();
-            if (lane < np) {
+            if (lane < nv) {
 #pragma unroll
-                for (int hf = 0; hf < S::kHalves; ++hf) {
-                    tc::tma_load_4d(sk + hf * kHalfBytes + lane * 2048, &tm_k, bar(kKvFull0 + st), hf * 64, h, 0,
+                for (int hf = 0; hf < S::kHalves; ++hf)
+                    tc::tma_load_4d(sv + hf * kHalfBytes + lane * 2048, &tm_v, bar(kVFull0 + vst), hf * 64, h, 0,
                                     page);
-                    if (lane < nv)
-                        tc::tma_load_4d(sv + hf * kHalfBytes + lane * 2048, &tm_v, bar(kKvFull0 + st), hf * 64, h,
-                                        0, page);
-                }
             }
         }
         if (!ok && lane == 0) {
@@ -262,36 +304,40 @@ __global__ void __launch_bounds__(kThreads, 1)
             constexpr uint32_t kIdQK = tc::idesc_bf16_f32(kM, kKeys, false, false);
             constexpr uint32_t kIdPV = tc::idesc_bf16_f32(kM, D, false, true);
             auto issue_pv = [&](int j) -> bool {
-                if (!tc::mbar_wait(bar(kPFull), j & 1, s_abort, kTimeoutNs)) return false;
+                if (!tc::mbar_wait(bar(kPFull0 + (j & 1)), (j >> 1) & 1, s_abort, kTimeoutNs)) return false;
+                const int vst = j % kVStages;
+                if (!tc::mbar_wait(bar(kVFull0 + vst), (j / kVStages) & 1, s_abort, kTimeoutNs)) return false;
                 tc::tc_fence_after();
                 const int npj = min(kPagesPerTile, last_page - j * kPagesPerTile);
-                const uint32_t sv = base + S::kV0 + (j & 1) * S::kStage;
-                for (int ks = 0; ks < npj; ++ks) {  // one 16-key step per page
-                    const uint64_t ad = tc::desc_sw128(base + S::kP + (ks >> 2) * kHalfBytes + (ks & 3) * 32, 16, 1024);
+                const uint32_t sv = base + S::kV0 + vst * S::kTile;
+                const uint32_t pa = tmem + ((j & 1) ? kTmemP1 : kTmemP0);
+                for (int ks = 0; ks < npj; ++ks) {  // one 16-key step per page; P: 8 columns per step
                     const uint64_t bd = tc::desc_sw128(sv + ks * 2048, kHalfBytes, 1024);
-                    tc::mma_bf16(tmem + kTmemO, ad, bd, kIdPV, (j > 0 || ks > 0) ? 1u : 0u);
+                    tc::mma_bf16_tmem_a(tmem + kTmemO, pa + ks * 8, bd, kIdPV, (j > 0 || ks > 0) ? 1u : 0u);
                 }
-                tc::mma_commit(bar(kPvDone));
-                tc::mma_commit(bar(kKvEmpty0 + (j & 1)));
+                tc::mma_commit(bar(kPvDone0 + (j & 1)));
+                tc::mma_commit(bar(kVEmpty0 + vst));
                 return true;
             };
             ok = tc::mbar_wait(bar(kQFull), 0, s_abort, kTimeoutNs);
             tc::tc_fence_after();
             for (int kt = 0; kt < ntiles && ok; ++kt) {
-                const int st = kt & 1;
-                ok = tc::mbar_wait(bar(kKvFull0 + st), (kt >> 1) & 1, s_abort, kTimeoutNs);
-                if (ok && kt >= 2) ok = tc::mbar_wait(bar(kSFree0 + st), ((kt >> 1) - 1) & 1, s_abort, kTimeoutNs);
+                const int sb = kt & 1;
+                const int kst = kt % kKStages;
+                ok = tc::mbar_wait(bar(kKFull0 + kst), (kt / kKStages) & 1, s_abort, kTimeoutNs);
+                if (ok && kt >= 2) ok = tc::mbar_wait(bar(kSFree0 + sb), ((kt >> 1) - 1) & 1, s_abort, kTimeoutNs);
                 if (!ok) break;
                 tc::tc_fence_after();
-                const uint32_t sk = base + S::kK0 + st * S::kStage;
+                const uint32_t sk = base + S::kK0 + kst * S::kTile;
 #pragma unroll
                 for (int ks = 0; ks < D / 16; ++ks) {
                     const uint32_t off = (ks >> 2) * kHalfBytes + (ks & 3) * 32;
                     const uint64_t ad = tc::desc_sw128(base + S::kQ + off, 16, 1024);
                     const uint64_t bd = tc::desc_sw128(sk + off, 16, 1024);
-                    tc::mma_bf16(tmem + (st ? kTmemS1 : kTmemS0), ad, bd, kIdQK, ks > 0 ? 1u : 0u);
+                    tc::mma_bf16(tmem + (sb ? kTmemS1 : kTmemS0), ad, bd, kIdQK, ks > 0 ? 1u : 0u);
                 }
-                tc::mma_commit(bar(kSFull0 + st));
+                tc::mma_commit(bar(kSFull0 + sb));
+                tc::mma_commit(bar(kKEmpty0 + kst));
                 if (kt >= 1) ok = issue_pv(kt - 1);
             }
             if (ok) ok = issue_pv(ntiles - 1);
@@ -313,10 +359,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int pos = valid ? prefix + i0 + r / G : -1;  // causal limit of this row
         const float c = a.scale_log2;
         float m_used = -INFINITY;  // running max, log2 units
-        float l = 0.f;
+        float lsum[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};  // split to keep the adds independent
         for (int kt = 0; kt < ntiles; ++kt) {
-            const int st = kt & 1;
-            if (!warp_wait(bar(kSFull0 + st), (kt >> 1) & 1, s_abort)) {
+            const int sb = kt & 1;
+            if (!warp_wait(bar(kSFull0 + sb), (kt >> 1) & 1, s_abort)) {
                 ok = false;
                 break;
             }
@@ -324,14 +370,16 @@ __global__ void __launch_bounds__(kThreads, 1)
             uint32_t sr[kKeys];
 #pragma unroll
             for (int q = 0; q < kKeys / 32; ++q)
-                tc::tmem_ld32(lane_addr + (st ? kTmemS1 : kTmemS0) + q * 32,
+                tc::tmem_ld32(lane_addr + (sb ? kTmemS1 : kTmemS0) + q * 32,
                               *reinterpret_cast<uint32_t(*)[32]>(&sr[q * 32]));
             tc::tc_fence_before();
             __syncwarp();
-            if (lane == 0) tc::mbar_arrive(bar(kSFree0 + st));
+            if (lane == 0) tc::mbar_arrive(bar(kSFree0 + sb));
 
             const int j0 = kt * kKeys;
-            float mx = -INFINITY;
+            float mx8[8];
+#pragma unroll
+            for (int e = 0; e < 8; ++e) mx8[e] = -INFINITY;
             const bool diag = __any_sync(0xffffffffu, j0 + kKeys - 1 > pos);
             if (diag) {
 #pragma unroll
@@ -339,24 +387,25 @@ __global__ void __launch_bounds__(kThreads, 1)
                     const float s = __uint_as_float(sr[j]);
                     const float v = (j0 + j <= pos) ? s : -INFINITY;
                     sr[j] = __float_as_uint(v);
-                    mx = fmaxf(mx, v);
+                    mx8[j & 7] = fmaxf(mx8[j & 7], v);
                 }
             } else {
 #pragma unroll
-                for (int j = 0; j < kKeys; ++j) mx = fmaxf(mx, __uint_as_float(sr[j]));
+                for (int j = 0; j < kKeys; ++j) mx8[j & 7] = fmaxf(mx8[j & 7], __uint_as_float(sr[j]));
             }
+            const float mx = fmaxf(fmaxf(fmaxf(mx8[0], mx8[1]), fmaxf(mx8[2], mx8[3])),
+                                   fmaxf(fmaxf(mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7])));
             const float mnew = mx * c;  // scale > 0, so the max commutes with it
-            bool waited_pv = false;
             if (kt == 0) {
                 m_used = mnew;
             } else {
                 const bool need = mnew > m_used + 8.f;
                 if (__any_sync(0xffffffffu, need)) {
-                    if (!warp_wait(bar(kPvDone), (kt - 1) & 1, s_abort)) {
+                    // O is final for tiles < kt once P V(kt-1) is done
+                    if (!warp_wait(bar(kPvDone0 + ((kt - 1) & 1)), ((kt - 1) >> 1) & 1, s_abort)) {
                         ok = false;
                         break;
                     }
-                    waited_pv = true;
                     tc::tc_fence_after();
                     const float alpha = need ? fast_exp2(m_used - mnew) : 1.f;
 #pragma unroll
@@ -367,42 +416,41 @@ __global__ void __launch_bounds__(kThreads, 1)
                         for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
                         tc::tmem_st32(lane_addr + kTmemO + q * 32, o);
                     }
-                    l *= alpha;
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) lsum[e] *= alpha;
                     if (need) m_used = mnew;
                 }
             }
             const float mu = m_used == -INFINITY ? 0.f : m_used;
-            if (kt >= 1 && !waited_pv) {  // the P buffer is free once P V of the previous tile is done
-                if (!warp_wait(bar(kPvDone), (kt - 1) & 1, s_abort)) {
-                    ok = false;
-                    break;
-                }
+            // P buffer sb is free once P V(kt-2) is done
+            if (kt >= 2 && !warp_wait(bar(kPvDone0 + sb), ((kt >> 1) - 1) & 1, s_abort)) {
+                ok = false;
+                break;
             }
-            // P = 2^(s*c - m) in bf16; l sums the rounded values the MMA will use.
-            const uint32_t prow = base + S::kP;
+            tc::tc_fence_after();
+            // P = 2^(s*c - m) as bf16 pairs; l sums the rounded values the MMA will use.
+            const uint32_t pcol = lane_addr + (sb ? kTmemP1 : kTmemP0);
 #pragma unroll
-            for (int ch = 0; ch < kKeys / 8; ++ch) {
-                uint32_t pk[4];
+            for (int hlf = 0; hlf < 2; ++hlf) {
+                uint32_t pk[32];
 #pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    const float x0 = fast_exp2(fmaf(__uint_as_float(sr[ch * 8 + 2 * e]), c, -mu));
-                    const float x1 = fast_exp2(fmaf(__uint_as_float(sr[ch * 8 + 2 * e + 1]), c, -mu));
+                for (int e = 0; e < 32; ++e) {
+                    const int j = hlf * 64 + 2 * e;
+                    const float x0 = fast_exp2(fmaf(__uint_as_float(sr[j]), c, -mu));
+                    const float x1 = fast_exp2(fmaf(__uint_as_float(sr[j + 1]), c, -mu));
                     pk[e] = pack_bf16(x0, x1);
-                    l += bf16_lo(pk[e]) + bf16_hi(pk[e]);
+                    lsum[e & 7] += bf16_lo(pk[e]) + bf16_hi(pk[e]);
                 }
-                const uint32_t dst = prow + (ch >> 3) * kHalfBytes + sw128(r, ch & 7);
-                asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};\n" ::"r"(dst), "r"(pk[0]), "r"(pk[1]),
-                             "r"(pk[2]), "r"(pk[3])
-                             : "memory");
+                tc::tmem_st32(pcol + hlf * 32, pk);
             }
-            tc::fence_proxy_async_smem();
             tc::tc_fence_before();
             __syncwarp();
-            if (lane == 0) tc::mbar_arrive(bar(kPFull));
+            if (lane == 0) tc::mbar_arrive(bar(kPFull0 + sb));
         }
-        if (ok) ok = warp_wait(bar(kPvDone), (ntiles - 1) & 1, s_abort);
+        if (ok) ok = warp_wait(bar(kPvDone0 + ((ntiles - 1) & 1)), ((ntiles - 1) >> 1) & 1, s_abort);
         if (ok) {
             tc::tc_fence_after();
+            const float l = ((lsum[0] + lsum[1]) + (lsum[2] + lsum[3])) + ((lsum[4] + lsum[5]) + (lsum[6] + lsum[7]));
             const float inv = valid ? 1.f / l : 0.f;
             __nv_bfloat16* orow =
                 out + (static_cast<int64_t>(q0 + i0 + (valid ? r / G : 0)) * a.num_q_heads + h * G + r % G) * D;

@@ -1,0 +1,166 @@
+"""Offline sweep that produces the split table (csrc/lut_gb300.inc).
+
+The Triton unified-attention page (section "What three things the IBM paper got
+right", third item) replaces run-time autotuning by offline micro-benchmarks
+distilled into a small decision tree keyed on GPU, sequence length and batch.
+This is that step for GB300: for every (context bound, batch size) cell of a
+grid it times pa_forward on Llama-3.1-8B-shaped decode batches (32 query heads,
+8 KV heads, head_dim 128, every sequence at the context bound) for a set of
+split sizes, and keeps the fastest.  The result is written as a table that the
+library compiles in; nothing is tuned at run time.
+
+    python -m paged_kv_cache_forward_gb300.sweep [--out csrc/lut_gb300.inc] [--log profiles/...md]
+
+Needs a GPU.  Inputs are random bf16 drawn on the device (values do not change
+the timing of this HBM-bound kernel); steps rotate over enough KV pool copies
+that no step finds its pages in L2.
+"""
+
+from __future__ import annotations
+
+import argparse
+import datetime
+import math
+import os
+import sys
+
+import torch
+
+HERE = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, os.path.dirname(HERE))
+
+import paged_kv_cache_forward_gb300 as pa  # noqa: E402
+
+BOUNDS = [1024, 2048, 4096, 8192, 16384, 32768, 65536, 131072]
+BATCHES = [1, 2, 4, 8, 16, 32, 64, 128, 256]
+HQ, HKV, D, PAGE = 32, 8, 128, 16
+MAX_KV_BYTES = 6 << 30
+
+
+def candidates(bound: int, batch: int, slots: int):
+    base = {64, 128, 256, 512, 1024, 2048, 4096, 8192, 16384}
+    # split sizes that give exactly k full waves of CTAs
+    for k in (1, 2, 3, 4):
+        pages = math.ceil(bound * batch * HKV / (k * slots) / PAGE)
+        base.add(max(1, pages) * PAGE)
+    return sorted(c for c in base if 16 <= c <= bound)
+
+
+def time_shape(bound, batch, chunk, pools, stream, steps_per_graph=16, reps=30):
+    q, ks, vs, bt, sl, qsl, out = pools
+    R = len(ks)
+    pa.prepare(q, ks[0], bt, sl, kv_chunk=chunk, stream=stream)
+    with torch.cuda.stream(stream):
+        for i in range(2):
+            pa.forward(q, ks[i % R], vs[i % R], bt, sl, qsl, out, kv_chunk=chunk, stream=stream)
+    stream.synchronize()
+    M = max(R, (steps_per_graph // R) * R)
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=stream):
+        for i in range(M):
+            pa.forward(q, ks[i % R], vs[i % R], bt, sl, qsl, out, kv_chunk=chunk, stream=stream)
+    for _ in range(3):
+        g.replay()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        e0.record()
+        for _ in range(reps):
+            g.replay()
+        e1.record()
+    stream.synchronize()
+    if pa.device_error(stream):
+        raise RuntimeError("device error during the sweep")
+    return e0.elapsed_time(e1) * 1e3 / (reps * M)  # us per step
+
+
+def make_pools(bound, batch, l2_bytes, gen):
+    pages = bound // PAGE
+    kv = batch * bound * HKV * D * 2 * 2
+    R = 1 if kv > 3 * l2_bytes else int(math.ceil(3 * l2_bytes / kv)) + 1
+    nb = batch * pages + 1
+    dev = "cuda"
+    q = torch.randn(batch, HQ, D, device=dev, generator=gen).to(torch.bfloat16)
+    ks, vs = [], []
+    for _ in range(R):
+        ks.append(torch.randn(nb, PAGE, HKV, D, device=dev, generator=gen).to(torch.bfloat16))
+        vs.append(torch.randn(nb, PAGE, HKV, D, device=dev, generator=gen).to(torch.bfloat16))
+    perm = torch.randperm(nb, device=dev, generator=gen).to(torch.int32)
+    bt = perm[: batch * pages].reshape(batch, pages).contiguous()
+    sl = torch.full((batch,), bound, dtype=torch.int32, device=dev)
+    qsl = torch.arange(batch + 1, dtype=torch.int32, device=dev)
+    out = torch.empty_like(q)
+    return (q, ks, vs, bt, sl, qsl, out), kv
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--out", default=os.path.join(HERE, "csrc", "lut_gb300.inc"))
+    ap.add_argument("--log", default=os.path.join(os.path.dirname(HERE), "profiles", "split_table_sweep__gb300.md"))
+    ap.add_argument("--bounds", default=",".join(map(str, BOUNDS)))
+    ap.add_argument("--batches", default=",".join(map(str, BATCHES)))
+    args = ap.parse_args(argv)
+    bounds = [int(x) for x in args.bounds.split(",")]
+    batches = [int(x) for x in args.batches.split(",")]
+
+    from paged_kv_cache_forward_gb300 import build
+    build.build()
+    pa.load()
+    props = torch.cuda.get_device_properties(0)
+    slots = props.multi_processor_count * 2  # two decode CTAs fit per SM
+    l2 = getattr(props, "L2_cache_size", 128 << 20)
+    stream = torch.cuda.Stream()
+    gen = torch.Generator(device="cuda").manual_seed(0)
+    best = {}
+    lines = []
+    for batch in batches:
+        for bound in bounds:
+            if batch * bound * HKV * D * 4 > MAX_KV_BYTES:
+                continue
+            pools, kv = make_pools(bound, batch, l2, gen)
+            res = []
+            for chunk in candidates(bound, batch, slots):
+                us = time_shape(bound, batch, chunk, pools, stream)
+                res.append((us, chunk))
+            res.sort()
+            us, chunk = res[0]
+            best[(bound, batch)] = chunk
+            row = " ".join(f"{c}:{kv / u / 1e3:.0f}" for u, c in sorted(res, key=lambda x: x[1]))
+            lines.append(f"| {batch} | {bound} | {chunk} | {us:.1f} | {kv / us / 1e3:.0f} | {row} |")
+            print(lines[-1], flush=True)
+            del pools
+            torch.cuda.empty_cache()
+
+    # table: (max_bound, max_seqs) cells, batch-major, so the first match is the
+    # smallest swept batch >= B and, within it, the smallest swept bound >= bound
+    entries = []
+    for batch in batches:
+        for bound in bounds:
+            if (bound, batch) in best:
+                entries.append((bound, batch, best[(bound, batch)]))
+    last_batch = max(b for _, b, _ in entries)
+    fallback = max(entries, key=lambda e: (e[1], e[0]))[2]
+    stamp = datetime.date.today().isoformat()
+    with open(args.out, "w") as f:
+        f.write("// Keys per split for the decode kernel, keyed on the context bound\n"
+                "// (max_pages * page_size) and the number of sequences.  First entry that\n"
+                "// matches wins; the last entry is the fallback.  Written by\n"
+                f"// paged_kv_cache_forward_gb300/sweep.py on {props.name} ({stamp}).\n"
+                "static const LutEntry kSplitTable[] = {\n")
+        for bound, batch, chunk in entries:
+            mb = (1 << 30) if batch == last_batch else batch
+            f.write(f"    {{{bound}, {mb}, {chunk}}},\n")
+        f.write(f"    {{1 << 30, 1 << 30, {fallback}}},\n}};\n")
+    with open(args.log, "w") as f:
+        f.write(f"# Split-size sweep on {props.name} ({stamp})\n\n"
+                "Command: `python -m paged_kv_cache_forward_gb300.sweep`\n\n"
+                "Llama-3.1-8B-shaped decode (Hq 32, Hkv 8, D 128), every sequence at the bound,\n"
+                "graph-replayed pa_forward steps rotating over KV pool copies larger than 3 x L2.\n"
+                "GB/s = KV bytes per step / step time.\n\n"
+                "| batch | bound | best split | us/step | GB/s | split:GB/s for every candidate |\n"
+                "|---|---|---|---|---|---|\n")
+        f.write("\n".join(lines) + "\n")
+    print(f"wrote {args.out} and {args.log}")
+
+
+if __name__ == "__main__":
+    main()
