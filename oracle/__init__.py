@@ -80,6 +80,9 @@ def _declare(lib: ctypes.CDLL) -> ctypes.CDLL:
     lib.oracle_attention_weights.restype = ctypes.c_int
     lib.oracle_validate.argtypes = [ctypes.POINTER(_Dims), P, P, P]
     lib.oracle_validate.restype = ctypes.c_int
+    lib.oracle_cache_write.argtypes = [P, P, P, P, P, ctypes.c_int64, ctypes.c_int64, ctypes.c_int64,
+                                       ctypes.c_int64, ctypes.c_int64]
+    lib.oracle_cache_write.restype = ctypes.c_int
     lib.oracle_max_threads.argtypes = []
     lib.oracle_max_threads.restype = ctypes.c_int
     return lib
@@ -197,3 +200,19 @@ def batch_attention(batch, rows=None, threads: int = 0, lib=None):
 
 def max_threads() -> int:
     return int(load().oracle_max_threads())
+
+
+def cache_write(k_new, v_new, slot_mapping, k_cache, v_cache, lib=None):
+    """Paged KV-cache write on copies of the caches; returns (k_cache, v_cache) as
+    uint16 (bf16 bit) arrays.  Negative slots write nothing."""
+    kn, vn = _bf16_bits(k_new), _bf16_bits(v_new)
+    kc, vc = _bf16_bits(k_cache).copy(), _bf16_bits(v_cache).copy()
+    sm = slot_mapping if isinstance(slot_mapping, np.ndarray) else slot_mapping.detach().cpu().numpy()
+    sm = np.ascontiguousarray(sm.astype(np.int64))
+    T = kn.shape[0]
+    NB, P, Hkv, D = kc.shape
+    assert kn.shape == (T, Hkv, D) and vn.shape == kn.shape and vc.shape == kc.shape and sm.shape == (T,)
+    rc = (lib or load()).oracle_cache_write(kn.ctypes.data, vn.ctypes.data, sm.ctypes.data, kc.ctypes.data,
+                                            vc.ctypes.data, T, NB, P, Hkv, D)
+    _check(rc)
+    return kc, vc

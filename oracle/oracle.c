@@ -252,3 +252,29 @@ int oracle_max_threads(void) {
     return 1;
 #endif
 }
+
+/*
+ * Paged KV-cache write: for every new token t with slot_mapping[t] = s >= 0,
+ * copy k_new[t] and v_new[t] ([Hkv, D] each) into page s / page_size, slot
+ * s % page_size of k_cache and v_cache.  A negative slot means "no write"
+ * (padding).  This is how the new tokens' K and V reach the paged KV cache of
+ * the Triton unified-attention page (section "Why is switching the card so
+ * hard": the paged KV cache) before attention reads them through the block
+ * table.  bf16 values are copied bit for bit.  Returns ORACLE_BAD_BLOCK, with
+ * nothing written, if a slot lies past num_blocks * page_size.
+ */
+int oracle_cache_write(const uint16_t* k_new, const uint16_t* v_new, const int64_t* slot_mapping,
+                       uint16_t* k_cache, uint16_t* v_cache, int64_t num_tokens, int64_t num_blocks,
+                       int64_t page_size, int64_t num_kv_heads, int64_t head_dim) {
+    const int64_t row = num_kv_heads * head_dim;  /* values of one token */
+    for (int64_t t = 0; t < num_tokens; ++t)
+        if (slot_mapping[t] >= num_blocks * page_size) return ORACLE_BAD_BLOCK;
+    for (int64_t t = 0; t < num_tokens; ++t) {
+        const int64_t s = slot_mapping[t];
+        if (s < 0) continue;
+        const int64_t page = s / page_size, slot = s % page_size;
+        memcpy(k_cache + (page * page_size + slot) * row, k_new + t * row, sizeof(uint16_t) * (size_t)row);
+        memcpy(v_cache + (page * page_size + slot) * row, v_new + t * row, sizeof(uint16_t) * (size_t)row);
+    }
+    return ORACLE_OK;
+}

@@ -339,6 +339,44 @@ def pin_validation(lib):
     del ctypes
 
 
+# --------------------------------------------------------- paged cache write
+
+def _slots_for(b: W.Batch, seq: int, positions):
+    return [int(b.block_table[seq, j // b.page_size]) * b.page_size + j % b.page_size for j in positions]
+
+
+def pin_cache_write_round_trip(lib):
+    """Writing new tokens through the slot mapping puts them where the block table
+    says logical position j lives (torch indexing of [NB, P, Hkv, D]); negative
+    slots leave the cache untouched; slots past the pool are refused."""
+    b = W.make_batch([3, 1, 5], [40, 17, 5], 8, 2, 64, seed=41, pool_factor=2.0, max_pages=4)
+    g = torch.Generator().manual_seed(9)
+    qsl = b.query_start_loc.tolist()
+    T = b.num_tokens
+    k_new = torch.randn(T, 2, 64, generator=g).to(torch.bfloat16)
+    v_new = torch.randn(T, 2, 64, generator=g).to(torch.bfloat16)
+    slots = []
+    for s_, (n, L) in enumerate(zip(b.q_lens(), b.seq_lens.tolist())):
+        slots += _slots_for(b, s_, range(L - n, L))
+    slots[1] = -1  # padding: no write
+    kc, vc = oracle.cache_write(k_new, v_new, torch.tensor(slots), b.k_cache, b.v_cache, lib=lib)
+    want_k = b.k_cache.clone()
+    want_v = b.v_cache.clone()
+    for t, sl in enumerate(slots):
+        if sl >= 0:
+            want_k[sl // 16, sl % 16] = k_new[t]
+            want_v[sl // 16, sl % 16] = v_new[t]
+    bits = lambda x: x.view(torch.int16).numpy().view(np.uint16)
+    assert np.array_equal(kc, bits(want_k)) and np.array_equal(vc, bits(want_v))
+    bad = torch.tensor([0] * (T - 1) + [b.num_blocks * 16])
+    try:
+        oracle.cache_write(k_new, v_new, bad, b.k_cache, b.v_cache, lib=lib)
+    except oracle.OracleError:
+        pass
+    else:
+        raise AssertionError("a slot past the pool was accepted")
+
+
 ALL_PINS = [
     pin_single_key,
     pin_constant_v,
@@ -350,4 +388,5 @@ ALL_PINS = [
     pin_causal_hiding,
     pin_position_code_spike,
     pin_sdpa_identity_table,
+    pin_cache_write_round_trip,
 ]

@@ -39,6 +39,11 @@ MUTANTS = [
     ("owner_seq_off_by_one", "if (qsl[mid] <= t) lo = mid;", "if (qsl[mid] < t) lo = mid;", False),
     ("wrong_seq_row", "int64_t page = block_table[b * d->max_pages + j / d->page_size];",
      "int64_t page = block_table[j / d->page_size];", False),
+    ("cache_write_page_slot_swapped", "const int64_t page = s / page_size, slot = s % page_size;",
+     "const int64_t page = s % page_size, slot = s / page_size;", False),
+    ("cache_write_v_from_k", "memcpy(v_cache + (page * page_size + slot) * row, v_new + t * row",
+     "memcpy(v_cache + (page * page_size + slot) * row, k_new + t * row", False),
+    ("cache_write_ignores_padding", "        if (s < 0) continue;\n", "", False),
 ]
 
 _CHILD = r"""
