@@ -50,6 +50,7 @@ DESCRIPTIONS = {
     "batched_decode": "batch 64, Hq 32 / Hkv 8, head_dim 128, page 16, context U[512, 8192], K x0.5",
     "varlen_prefill": "batch 8, Hq 32 / Hkv 8, head_dim 128, causal, new U[128, 2048], prefix U[0, 4096]",
     "mixed": "4 prefill x 512 + 60 decode ctx U[1024, 16384] + 1 decode ctx 131072, Hq 32 / Hkv 8, D 128",
+    "spec_decode": "batch 16 x 4 new tokens (speculative decoding), ctx U[2048, 8192], Hq 32 / Hkv 8, D 128",
 }
 
 
@@ -121,8 +122,9 @@ def work_of(batch):
     pages = sum((L + batch.page_size - 1) // batch.page_size for L in batch.seq_lens.tolist())
     flops = 4 * D * Hq * batch.causal_pairs()
     q_lens = batch.q_lens()
-    dec_kv = sum(L for n, L in zip(q_lens, batch.seq_lens.tolist()) if n == 1) * 2 * batch.num_kv_heads * D * 2
-    dec_tokens = sum(1 for n in q_lens if n == 1)
+    qmax = 16 // (Hq // batch.num_kv_heads) if Hq // batch.num_kv_heads <= 16 else 1  # decode-path tokens
+    dec_kv = sum(L for n, L in zip(q_lens, batch.seq_lens.tolist()) if 1 <= n <= qmax) * 2 * batch.num_kv_heads * D * 2
+    dec_tokens = sum(n for n in q_lens if 1 <= n <= qmax)
     return dict(kv_bytes=kv, flops=flops, tokens=batch.num_tokens,
                 decode_bytes=dec_kv + dec_tokens * Hq * D * 2 + pages * 4,
                 algorithmic_bytes=kv + 2 * q_bytes + pages * 4)
@@ -346,8 +348,9 @@ def run_ours(args):
     stream = torch.cuda.Stream(device=dev)
     plan = pa.plan_for(d.q, d.k_cache, d.block_table, d.seq_lens, kv_chunk=args.kv_chunk)
     pa.prepare(d.q, d.k_cache, d.block_table, d.seq_lens, kv_chunk=args.kv_chunk, stream=stream)
-    has_decode = any(n == 1 for n in batch.q_lens())
-    has_prefill = any(n >= 2 for n in batch.q_lens())
+    G = batch.num_q_heads // batch.num_kv_heads
+    qmax = 16 // G if G <= 16 else 1
+    has_decode = any(1 <= n <= qmax for n in batch.q_lens())
     dominant = "prefill" if (args.config == "varlen_prefill" or not has_decode) else "decode_splitkv"
 
     def call(i, events=None):

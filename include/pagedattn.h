@@ -185,6 +185,34 @@ pa_status pa_forward_noalloc(const void* q, const void* k_cache, const void* v_c
                              const int32_t* query_start_loc, void* out, float scale,
                              const pa_dims* dims, int32_t* device_error, void* stream);
 
+/* Shapes of a paged KV-cache write. */
+typedef struct {
+    int64_t num_tokens;    /* T: rows of k_new, v_new and slot_mapping           */
+    int64_t num_blocks;    /* NB: pages in each of k_cache and v_cache           */
+    int32_t num_kv_heads;  /* Hkv                                                */
+    int32_t head_dim;      /* D (Hkv * D must be a multiple of 8)                */
+    int32_t page_size;     /* P                                                  */
+    int32_t reserved;
+} pa_cache_dims;
+
+/*
+ * Paged KV-cache write: the step that brings the new tokens' K and V into the
+ * paged KV cache (the Triton unified-attention page, section "Why is switching
+ * the card so hard": paged KV cache) before pa_forward reads them through the
+ * block table.  For every token t with s = slot_mapping[t] >= 0, k_new[t] and
+ * v_new[t] are copied to page s / P, slot s % P of k_cache and v_cache; a
+ * negative slot is padding and writes nothing.
+ *   k_new, v_new     [T, Hkv, D]      bf16, device, 16-byte aligned
+ *   slot_mapping     [T]              int64, device, 8-byte aligned
+ *   k_cache, v_cache [NB, P, Hkv, D]  bf16, device, 16-byte aligned (written)
+ * Two tokens with the same slot race (the caller's contract).  A slot at or past
+ * NB * P is not written and sets device error 1 (see pa_device_error).  Stream
+ * ordered and graph-capturable (its error word lives in the stream's workspace,
+ * so call pa_prepare, or any pa_forward, on the stream before capturing).
+ */
+pa_status pa_cache_write(const void* k_new, const void* v_new, const int64_t* slot_mapping, void* k_cache,
+                         void* v_cache, const pa_cache_dims* dims, void* stream);
+
 /* Library version, major * 10000 + minor * 100 + patch. */
 int32_t pa_version(void);
 

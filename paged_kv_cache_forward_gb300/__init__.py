@@ -15,6 +15,8 @@ from .binding import (  # noqa: F401
     device_error,
     forward,
     forward_noalloc,
+    cache_write,
+    CacheDims,
     load,
     make_dims,
     plan,

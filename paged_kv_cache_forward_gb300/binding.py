@@ -25,6 +25,7 @@ PA_OK, PA_ERR_INVALID_ARG, PA_ERR_UNSUPPORTED, PA_ERR_NOT_PREPARED, PA_ERR_CUDA 
 EXPORTED = (
     "pa_forward", "pa_forward_ex", "pa_plan", "pa_prepare", "pa_device_error",
     "pa_release_workspaces", "pa_status_string", "pa_last_error", "pa_version", "pa_forward_noalloc",
+    "pa_cache_write",
 )
 
 DEVICE_ERRORS = {
@@ -67,6 +68,17 @@ class Options(ctypes.Structure):
     ]
 
 
+class CacheDims(ctypes.Structure):
+    _fields_ = [
+        ("num_tokens", ctypes.c_int64),
+        ("num_blocks", ctypes.c_int64),
+        ("num_kv_heads", ctypes.c_int32),
+        ("head_dim", ctypes.c_int32),
+        ("page_size", ctypes.c_int32),
+        ("reserved", ctypes.c_int32),
+    ]
+
+
 class PlanInfo(ctypes.Structure):
     _fields_ = [
         ("kv_chunk", ctypes.c_int32),
@@ -100,6 +112,7 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.pa_forward.argtypes = fwd + [P]
     lib.pa_forward_ex.argtypes = fwd + [ctypes.POINTER(Options), P]
     lib.pa_forward_noalloc.argtypes = fwd + [P, P]
+    lib.pa_cache_write.argtypes = [P, P, P, P, P, ctypes.POINTER(CacheDims), P]
     lib.pa_plan.argtypes = [ctypes.POINTER(Dims), ctypes.POINTER(Options), ctypes.POINTER(PlanInfo)]
     lib.pa_prepare.argtypes = [ctypes.POINTER(Dims), ctypes.POINTER(Options), P]
     lib.pa_device_error.argtypes = [P, ctypes.POINTER(ctypes.c_int32)]
@@ -110,7 +123,7 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.pa_last_error.restype = ctypes.c_char_p
     lib.pa_version.argtypes = []
     for name in ("pa_forward", "pa_forward_ex", "pa_plan", "pa_prepare", "pa_device_error",
-                 "pa_release_workspaces", "pa_version", "pa_forward_noalloc"):
+                 "pa_release_workspaces", "pa_version", "pa_forward_noalloc", "pa_cache_write"):
         getattr(lib, name).restype = I32
     _lib = lib
     return lib
@@ -220,6 +233,28 @@ def forward_noalloc(q, k_cache, v_cache, block_table, seq_lens, query_start_loc,
         _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(block_table), _ptr(seq_lens), _ptr(query_start_loc),
         _ptr(out), ctypes.c_float(scale), ctypes.byref(dims), _ptr(device_error), _stream_handle(stream)))
     return out
+
+
+def cache_write(k_new, v_new, slot_mapping, k_cache, v_cache, stream=None):
+    """pa_cache_write: copy each new token's K and V ([T, Hkv, D] bf16) to page
+    slot_mapping[t] // P, slot slot_mapping[t] % P of the caches (int64 slots;
+    negative = padding, no write).  The caches are updated in place."""
+    for name, t, dt in (("k_new", k_new, torch.bfloat16), ("v_new", v_new, torch.bfloat16),
+                        ("slot_mapping", slot_mapping, torch.int64), ("k_cache", k_cache, torch.bfloat16),
+                        ("v_cache", v_cache, torch.bfloat16)):
+        if t.dtype != dt:
+            raise TypeError(f"{name} must be {dt}, got {t.dtype}")
+        if not t.is_contiguous() or not t.is_cuda:
+            raise ValueError(f"{name} must be a contiguous CUDA tensor")
+    if k_new.dim() != 3 or v_new.shape != k_new.shape or k_cache.dim() != 4 or v_cache.shape != k_cache.shape:
+        raise ValueError("k_new, v_new must be [T, Hkv, D] and the caches [NB, P, Hkv, D]")
+    T, Hkv, D = k_new.shape
+    if tuple(k_cache.shape[2:]) != (Hkv, D) or tuple(slot_mapping.shape) != (T,):
+        raise ValueError("shapes of the new rows, the caches and slot_mapping disagree")
+    dims = CacheDims(num_tokens=T, num_blocks=k_cache.shape[0], num_kv_heads=Hkv, head_dim=D,
+                     page_size=k_cache.shape[1])
+    _check(load().pa_cache_write(_ptr(k_new), _ptr(v_new), _ptr(slot_mapping), _ptr(k_cache), _ptr(v_cache),
+                                 ctypes.byref(dims), _stream_handle(stream)))
 
 
 def plan(dims: Dims, kv_chunk: int = 0) -> dict:

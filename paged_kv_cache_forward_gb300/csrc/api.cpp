@@ -75,7 +75,7 @@ pa_status check_dims(const pa_dims* d) {
 
 struct Plan {
     int32_t kv_chunk = 0, splits = 0, row_groups = 0;
-    int64_t decode_ctas = 0, combine_ctas = 0, prefill_ctas = 0, ws_bytes = 0;
+    int64_t decode_ctas = 0, combine_ctas = 0, prefill_ctas = 0, ws_bytes = 0, counter_bytes = 0;
     int32_t launches = 0;
     pa::Args args{};
 };
@@ -105,6 +105,7 @@ pa_status make_plan(const pa_dims* d, const pa_options* o, Plan* p) {
     a.kv_chunk = static_cast<int32_t>(chunk);
     a.splits = static_cast<int32_t>((bound + chunk - 1) / chunk);
     a.row_groups = (group + 15) / 16;
+    a.decode_max_q = pa::decode_max_q(group);
     p->kv_chunk = a.kv_chunk;
     p->splits = a.splits;
     p->row_groups = a.row_groups;
@@ -118,8 +119,9 @@ pa_status make_plan(const pa_dims* d, const pa_options* o, Plan* p) {
     if (p->decode_ctas > kMaxCtas || p->prefill_ctas > kMaxCtas)
         return fail(PA_ERR_UNSUPPORTED, "launch grid above 2^31-1 CTAs; use a larger kv_chunk");
     p->launches = (p->decode_ctas > 0) + (p->prefill_ctas > 0);
-    p->ws_bytes = pa::workspace_layout(d->num_seqs, d->num_kv_heads, a.row_groups, a.splits, d->num_q_heads,
-                                       d->head_dim)
+    p->counter_bytes = pa::counter_bytes_needed(d->num_seqs, d->num_kv_heads, a.row_groups, a.splits);
+    p->ws_bytes = pa::workspace_layout(d->num_seqs, d->num_q_heads, a.splits, d->head_dim, a.decode_max_q,
+                                       p->counter_bytes)
                       .bytes;
     return PA_OK;
 }
@@ -130,15 +132,20 @@ struct Workspace {
     cudaStream_t stream;
     void* ptr;
     int64_t bytes;
+    int64_t counter_bytes;  // size of the counter area (fixed for the buffer's life)
 };
 
 std::mutex g_ws_mutex;
 std::vector<Workspace> g_ws;       // live, one per (device, stream)
 std::vector<Workspace> g_retired;  // outgrown buffers, kept for captured graphs
 
-// Returns the workspace of (device, stream) with at least `bytes`, growing it if
-// allowed.  A new buffer is zeroed (error word and split counters start at 0).
-pa_status get_workspace(cudaStream_t stream, int64_t bytes, bool may_grow, void** out) {
+// Returns the workspace of (device, stream) able to hold a call that needs a
+// counter area of `counter_bytes` and `bytes` in all (at that counter size),
+// growing it if allowed.  A new buffer is zeroed (error word and split counters
+// start at 0) and keeps its counter area size for life, so partials never land
+// on counter bytes.  *counter_area receives the buffer's counter area size.
+pa_status get_workspace(cudaStream_t stream, int64_t bytes, int64_t counter_bytes, bool may_grow, void** out,
+                        int64_t* counter_area) {
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
@@ -146,14 +153,20 @@ pa_status get_workspace(cudaStream_t stream, int64_t bytes, bool may_grow, void*
     Workspace* w = nullptr;
     for (Workspace& x : g_ws)
         if (x.device == dev && x.stream == stream) w = &x;
-    if (w && w->bytes >= bytes) {
+    if (w && w->counter_bytes >= counter_bytes && w->bytes >= bytes + (w->counter_bytes - counter_bytes)) {
         *out = w->ptr;
+        if (counter_area) *counter_area = w->counter_bytes;
         return PA_OK;
     }
     if (!may_grow)
         return fail(PA_ERR_NOT_PREPARED,
                     "workspace of %lld bytes needed while the stream is capturing; call pa_prepare first",
                     static_cast<long long>(bytes));
+    // a new buffer: counter area at least as large as before, total at least as large
+    const int64_t new_counters = w ? (w->counter_bytes > counter_bytes ? w->counter_bytes : counter_bytes) : counter_bytes;
+    int64_t new_bytes = bytes + (new_counters - counter_bytes);
+    if (w && w->bytes > new_bytes) new_bytes = w->bytes;
+    bytes = new_bytes;
     void* p = nullptr;
     e = cudaMalloc(&p, static_cast<size_t>(bytes));
     if (e != cudaSuccess) return cuda_fail(e, "cudaMalloc(workspace)");
@@ -170,10 +183,12 @@ pa_status get_workspace(cudaStream_t stream, int64_t bytes, bool may_grow, void*
         g_retired.push_back(*w);
         w->ptr = p;
         w->bytes = bytes;
+        w->counter_bytes = new_counters;
     } else {
-        g_ws.push_back(Workspace{dev, stream, p, bytes});
+        g_ws.push_back(Workspace{dev, stream, p, bytes, new_counters});
     }
     *out = p;
+    if (counter_area) *counter_area = new_counters;
     return PA_OK;
 }
 
@@ -231,7 +246,8 @@ pa_status pa_prepare(const pa_dims* dims, const pa_options* opts, void* stream) 
     if (e != cudaSuccess) return cuda_fail(e, "cudaStreamIsCapturing");
     if (cs != cudaStreamCaptureStatusNone) return fail(PA_ERR_INVALID_ARG, "pa_prepare called during capture");
     void* ws = nullptr;
-    return get_workspace(s, p.ws_bytes > kErrWordBytes ? p.ws_bytes : kErrWordBytes, true, &ws);
+    return get_workspace(s, p.ws_bytes > kErrWordBytes ? p.ws_bytes : kErrWordBytes, p.counter_bytes, true, &ws,
+                         nullptr);
 }
 
 pa_status pa_forward_ex(const void* q, const void* k_cache, const void* v_cache, const int32_t* block_table,
@@ -250,7 +266,8 @@ pa_status pa_forward_ex(const void* q, const void* k_cache, const void* v_cache,
     cudaError_t e = cudaStreamIsCapturing(s, &cs);
     if (e != cudaSuccess) return cuda_fail(e, "cudaStreamIsCapturing");
     void* ws = nullptr;
-    st = get_workspace(s, p.ws_bytes, cs == cudaStreamCaptureStatusNone, &ws);
+    int64_t counter_area = 0;
+    st = get_workspace(s, p.ws_bytes, p.counter_bytes, cs == cudaStreamCaptureStatusNone, &ws, &counter_area);
     if (st != PA_OK) return st;
 
     pa::Args a = p.args;
@@ -263,7 +280,7 @@ pa_status pa_forward_ex(const void* q, const void* k_cache, const void* v_cache,
     a.out = out;
     a.err = static_cast<int32_t*>(ws);
     const pa::WorkspaceLayout wl =
-        pa::workspace_layout(a.num_seqs, a.num_kv_heads, a.row_groups, a.splits, a.num_q_heads, a.head_dim);
+        pa::workspace_layout(a.num_seqs, a.num_q_heads, a.splits, a.head_dim, a.decode_max_q, counter_area);
     a.counters = reinterpret_cast<int32_t*>(static_cast<char*>(ws) + wl.counters_off);
     a.ws_o = reinterpret_cast<float*>(static_cast<char*>(ws) + wl.o_off);
     a.ws_ml = reinterpret_cast<float*>(static_cast<char*>(ws) + wl.ml_off);
@@ -287,12 +304,38 @@ pa_status pa_forward(const void* q, const void* k_cache, const void* v_cache, co
                          stream);
 }
 
+pa_status pa_cache_write(const void* k_new, const void* v_new, const int64_t* slot_mapping, void* k_cache,
+                         void* v_cache, const pa_cache_dims* d, void* stream) {
+    if (!d) return fail(PA_ERR_INVALID_ARG, "dims is NULL");
+    if (d->num_tokens < 0 || d->num_blocks <= 0 || d->num_kv_heads <= 0 || d->head_dim <= 0 || d->page_size <= 0)
+        return fail(PA_ERR_INVALID_ARG, "cache dims must be positive (num_tokens >= 0)");
+    if ((static_cast<int64_t>(d->num_kv_heads) * d->head_dim) % 8)
+        return fail(PA_ERR_UNSUPPORTED, "num_kv_heads * head_dim must be a multiple of 8");
+    if (d->num_tokens > 0x7fffffffLL) return fail(PA_ERR_UNSUPPORTED, "more than 2^31-1 tokens");
+    if (d->num_tokens == 0) return PA_OK;
+    if (!k_new || !v_new || !slot_mapping || !k_cache || !v_cache)
+        return fail(PA_ERR_INVALID_ARG, "NULL data pointer");
+    if (!aligned(k_new, 16) || !aligned(v_new, 16) || !aligned(k_cache, 16) || !aligned(v_cache, 16) ||
+        !aligned(slot_mapping, 8))
+        return fail(PA_ERR_INVALID_ARG, "k/v tensors must be 16-byte aligned and slot_mapping 8-byte aligned");
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+    cudaError_t e = cudaStreamIsCapturing(s, &cs);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaStreamIsCapturing");
+    void* ws = nullptr;
+    pa_status st = get_workspace(s, kErrWordBytes, 0, cs == cudaStreamCaptureStatusNone, &ws, nullptr);
+    if (st != PA_OK) return st;
+    e = pa::launch_cache_write(k_new, v_new, slot_mapping, k_cache, v_cache, d->num_tokens, d->num_blocks,
+                               d->page_size, d->num_kv_heads, d->head_dim, static_cast<int32_t*>(ws), s);
+    return e == cudaSuccess ? PA_OK : cuda_fail(e, "cache write launch");
+}
+
 pa_status pa_device_error(void* stream, int32_t* code) {
     if (!code) return fail(PA_ERR_INVALID_ARG, "code is NULL");
     *code = 0;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     void* ws = nullptr;
-    pa_status st = get_workspace(s, kErrWordBytes, true, &ws);
+    pa_status st = get_workspace(s, kErrWordBytes, 0, true, &ws, nullptr);
     if (st != PA_OK) return st;
     cudaError_t e = cudaStreamSynchronize(s);
     if (e != cudaSuccess) return cuda_fail(e, "cudaStreamSynchronize");

@@ -1,12 +1,16 @@
 // decode.cu -- GQA Q-block split-KV decode kernel.
 //
-// One CTA owns (sequence b, KV head h, row group rg, split s): the query heads
-// h*G + rg*16 .. +16 of b's single new token (the "Q-Block" item of the five-step
-// list on the Triton unified-attention page, section "What three things the IBM
-// paper got right": query heads sharing a KV head are computed together, so each
-// KV page is read once per KV head, not once per query head) against keys
-// [s*kv_chunk, min((s+1)*kv_chunk, L_b)) -- one tile of the "Parallel Tiled
-// Softmax" item of the same list.
+// One CTA owns (sequence b, KV head h, row group rg, split s).  Its query rows
+// are the G query heads sharing h times the n_b new tokens of b (n_b * G <= 16:
+// a single decode token, or a few speculative-decoding tokens), row r = (token
+// r / G, head h*G + r % G); with more than 16 heads per KV head, single-token
+// sequences only, in row groups of 16 heads.  This is the "Q-Block" item of the
+// five-step list on the Triton unified-attention page, section "What three things
+// the IBM paper got right": query heads sharing a KV head are computed together,
+// so each KV page is read once per KV head, not once per query head.  The CTA
+// covers keys [s*kv_chunk, min((s+1)*kv_chunk, L_b)) -- one tile of the
+// "Parallel Tiled Softmax" item of the same list -- with each row masked
+// causally at its own position L_b - n_b + token.
 //
 // Inside the CTA, 4 warps take pages round-robin.  Each warp runs its own
 // 2-stage cp.async pipeline of one 16-token page of K and V (16-byte copies into
@@ -67,22 +71,28 @@ __device__ __forceinline__ uint32_t swz(int r, int c) {
     return r * DecodeTile<D>::kRowBytes + ((c ^ (r & 7)) << 4);
 }
 
-// Log-sum-exp merge of the nsplits partials of rows hq0 .. hq0+rows-1 of
-// sequence b (the last step of "Parallel Tiled Softmax"): M = max_s m_s,
-// w_s = 2^(m_s - M), out = sum_s w_s O_s / sum_s w_s l_s.  The partials were
-// written by other CTAs, so they are read with L2-coherent loads.
+// Partial-row index of (sequence b, split s, new token i, query head hq).
+__device__ __forceinline__ int64_t partial_row(const Args& a, int b, int s, int i, int hq) {
+    return ((static_cast<int64_t>(b) * a.splits + s) * a.decode_max_q + i) * a.num_q_heads + hq;
+}
+
+// Log-sum-exp merge of the nsplits partials of the CTA's rows (row r = token
+// tok[r], query head head[r]) of sequence b (the last step of "Parallel Tiled
+// Softmax"): M = max_s m_s, w_s = 2^(m_s - M), out = sum_s w_s O_s / sum_s w_s l_s.
+// A split that saw no visible key of a row has m_s = -inf and weight 0.  The
+// partials were written by other CTAs, so they are read with L2-coherent loads.
 template <int D>
-__device__ __forceinline__ void merge_splits(const Args& a, int b, int hq0, int rows, int nsplits, int q0,
-                                             float* sm) {
+__device__ __forceinline__ void merge_splits(const Args& a, int b, const int* tok, const int* head, int rows,
+                                             int nsplits, int q0, float* sm) {
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
     float* s_m = sm;         // per-row max
     float* s_inv = sm + kRows;  // per-row 1 / denominator
-    const int64_t split_ml = static_cast<int64_t>(a.num_q_heads) * 2;  // stride between splits in ws_ml
-    const int64_t split_o = static_cast<int64_t>(a.num_q_heads) * D;   // ... and in ws_o
-    const int64_t row0 = static_cast<int64_t>(b) * a.splits * a.num_q_heads + hq0;
+    const int64_t split_rows = static_cast<int64_t>(a.decode_max_q) * a.num_q_heads;
+    const int64_t split_ml = split_rows * 2;  // stride between splits in ws_ml
+    const int64_t split_o = split_rows * D;   // ... and in ws_o
     for (int r = warp; r < rows; r += kWarps) {
-        const float* ml = a.ws_ml + (row0 + r) * 2;
+        const float* ml = a.ws_ml + partial_row(a, b, 0, tok[r], head[r]) * 2;
         float M = -INFINITY;
         for (int s = lane; s < nsplits; s += 32) M = fmaxf(M, __ldcg(ml + s * split_ml));
         M = warp_max(M);
@@ -102,8 +112,9 @@ __device__ __forceinline__ void merge_splits(const Args& a, int b, int hq0, int 
         const int r = it / kGroups;
         const int d4 = (it % kGroups) * 4;
         const float M = s_m[r];
-        const float* ml = a.ws_ml + (row0 + r) * 2;
-        const float* os = a.ws_o + (row0 + r) * D + d4;
+        const int64_t row = partial_row(a, b, 0, tok[r], head[r]);
+        const float* ml = a.ws_ml + row * 2;
+        const float* os = a.ws_o + row * D + d4;
         float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
         int s = 0;
         for (; s + 8 <= nsplits; s += 8) {  // 8 independent loads in flight
@@ -135,7 +146,8 @@ __device__ __forceinline__ void merge_splits(const Args& a, int b, int hq0, int 
         uint2 packed;
         packed.x = pack_bf16(acc.x * inv, acc.y * inv);
         packed.y = pack_bf16(acc.z * inv, acc.w * inv);
-        *reinterpret_cast<uint2*>(out + (static_cast<int64_t>(q0) * a.num_q_heads + hq0 + r) * D + d4) = packed;
+        *reinterpret_cast<uint2*>(out + (static_cast<int64_t>(q0 + tok[r]) * a.num_q_heads + head[r]) * D + d4) =
+            packed;
     }
 }
 
@@ -158,8 +170,8 @@ __global__ void __launch_bounds__(kWarps * 32) decode_splitkv_kernel(const Args 
 
     const int q0 = a.query_start_loc[b];
     const int n = a.query_start_loc[b + 1] - q0;
-    if (n != 1) return;  // not a decode sequence (prefill kernel, or empty)
-    if (q0 < 0 || q0 >= a.num_tokens) {
+    if (n < 1 || n > a.decode_max_q) return;  // empty, or the prefill kernel's
+    if (q0 < 0 || static_cast<int64_t>(q0) + n > a.num_tokens) {
         flag_error(a.err, kDevBadQueryStart);
         return;
     }
@@ -170,15 +182,24 @@ __global__ void __launch_bounds__(kWarps * 32) decode_splitkv_kernel(const Args 
         flag_error(a.err, kDevSeqTooLong);
         L = cap;
     }
-    const int rows = min(kRows, a.group - rg * kRows);
-    const int hq0 = h * a.group + rg * kRows;
+    // Rows of this CTA: r -> (new token tok, query head head).
+    const bool packed = a.row_groups == 1;  // tokens x G heads in one tile
+    const int rows = packed ? n * a.group : min(kRows, a.group - rg * kRows);
+    __shared__ int s_tok[kRows], s_head[kRows];
+    if (threadIdx.x < kRows) {
+        const int r = threadIdx.x;
+        s_tok[r] = packed ? r / a.group : 0;
+        s_head[r] = packed ? h * a.group + r % a.group : h * a.group + rg * kRows + r;
+    }
+    __syncthreads();
     __nv_bfloat16* out = reinterpret_cast<__nv_bfloat16*>(a.out);
-    if (L < 1) {
+    if (L < n) {
         // A query must see at least itself; the caller broke the contract.
         if (s == 0) {
             flag_error(a.err, kDevQueryTooLong);
             for (int i = threadIdx.x; i < rows * D; i += blockDim.x)
-                out[(static_cast<int64_t>(q0) * a.num_q_heads + hq0 + i / D) * D + i % D] = __float2bfloat16(0.f);
+                out[(static_cast<int64_t>(q0 + s_tok[i / D]) * a.num_q_heads + s_head[i / D]) * D + i % D] =
+                    __float2bfloat16(0.f);
         }
         return;
     }
@@ -189,11 +210,17 @@ __global__ void __launch_bounds__(kWarps * 32) decode_splitkv_kernel(const Args 
     const int nsplits = (L + a.kv_chunk - 1) / a.kv_chunk;
     const int my_pages = warp < npages ? (npages - warp + kWarps - 1) / kWarps : 0;
 
-    // Q fragments for all D/16 k-steps; rows >= `rows` are zero.
+    // Q fragments for all D/16 k-steps; rows >= `rows` are zero.  Each of this
+    // thread's two rows (g, g + 8) has its own causal limit.
     const __nv_bfloat16* q = reinterpret_cast<const __nv_bfloat16*>(a.q);
-    const __nv_bfloat16* qg = q + (static_cast<int64_t>(q0) * a.num_q_heads + hq0 + g) * D;
-    const __nv_bfloat16* qg8 = qg + 8 * D;
     const bool row_lo = g < rows, row_hi = g + 8 < rows;
+    const __nv_bfloat16* qg =
+        q + (static_cast<int64_t>(q0 + (row_lo ? s_tok[g] : 0)) * a.num_q_heads + (row_lo ? s_head[g] : 0)) * D;
+    const __nv_bfloat16* qg8 =
+        q + (static_cast<int64_t>(q0 + (row_hi ? s_tok[g + 8] : 0)) * a.num_q_heads + (row_hi ? s_head[g + 8] : 0)) *
+                D;
+    const int lim_lo = L - n + (row_lo ? s_tok[g] : 0);      // last key row g may see
+    const int lim_hi = L - n + (row_hi ? s_tok[g + 8] : 0);
     uint32_t qa[D / 16][4];
 #pragma unroll
     for (int ks = 0; ks < D / 16; ++ks) {
@@ -212,10 +239,22 @@ __global__ void __launch_bounds__(kWarps * 32) decode_splitkv_kernel(const Args 
 
     // Issue the copies of this warp's it-th page into stage it % kStages; always
     // commit a group so that the wait count below stays uniform.
+    // Block-table entries of this warp's pages, 32 at a time in registers (lane l
+    // holds the entry of the warp's page 32 * round + l), the next round loaded
+    // ahead, so that the copies do not wait on them.
+    auto bt_entry = [&](int i) { return i < my_pages ? bt[start / kPage + warp + kWarps * i] : 0; };
+    int bt_cur = bt_entry(lane), bt_nxt = bt_entry(32 + lane);
+    auto page_of = [&](int it) {  // every lane calls it with the same it
+        if (it > 0 && (it & 31) == 0) {
+            bt_cur = bt_nxt;
+            bt_nxt = bt_entry(it + 32 + lane);
+        }
+        return __shfl_sync(0xffffffffu, bt_cur, it & 31);
+    };
     auto issue = [&](int it) {
         if (it < my_pages) {
             const int lp = start / kPage + warp + kWarps * it;
-            const int page = bt[lp];
+            const int page = page_of(it);
             const bool ok = static_cast<uint32_t>(page) < static_cast<uint64_t>(a.num_blocks);
             if (!ok) flag_error(a.err, kDevBadBlock);
             const int valid = ok ? min(kPage, end - lp * kPage) : 0;
@@ -272,7 +311,7 @@ __global__ void __launch_bounds__(kWarps * 32) decode_splitkv_kernel(const Args 
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
                 const int j = tok0 + nt * 8 + 2 * tq + (e & 1);
-                sc[nt][e] = j < end ? sc[nt][e] * a.scale_log2 : -INFINITY;
+                sc[nt][e] = (j < end && j <= (e < 2 ? lim_lo : lim_hi)) ? sc[nt][e] * a.scale_log2 : -INFINITY;
             }
         const float mx_lo = quad_max(fmaxf(fmaxf(sc[0][0], sc[0][1]), fmaxf(sc[1][0], sc[1][1])));
         const float mx_hi = quad_max(fmaxf(fmaxf(sc[0][2], sc[0][3]), fmaxf(sc[1][2], sc[1][3])));
@@ -351,9 +390,9 @@ __global__ void __launch_bounds__(kWarps * 32) decode_splitkv_kernel(const Args 
             l += sc * mwr[kRows * D + kRows + r];
         }
         if (nsplits == 1) {
-            out[(static_cast<int64_t>(q0) * a.num_q_heads + hq0 + r) * D + d] = __float2bfloat16(acc / l);
+            out[(static_cast<int64_t>(q0 + s_tok[r]) * a.num_q_heads + s_head[r]) * D + d] = __float2bfloat16(acc / l);
         } else {
-            const int64_t slot = (static_cast<int64_t>(b) * a.splits + s) * a.num_q_heads + hq0 + r;
+            const int64_t slot = partial_row(a, b, s, s_tok[r], s_head[r]);
             a.ws_o[slot * D + d] = acc;
             if (d == 0) {
                 a.ws_ml[slot * 2] = M;
@@ -374,7 +413,7 @@ __global__ void __launch_bounds__(kWarps * 32) decode_splitkv_kernel(const Args 
     __syncthreads();
     if (!s_last) return;
     __threadfence();
-    merge_splits<D>(a, b, hq0, rows, nsplits, q0, reinterpret_cast<float*>(smem));
+    merge_splits<D>(a, b, s_tok, s_head, rows, nsplits, q0, reinterpret_cast<float*>(smem));
     if (threadIdx.x == 0) *counter = 0;
 }
 

@@ -35,26 +35,42 @@ struct Args {
     int32_t kv_chunk;    // tokens per split (multiple of the page size)
     int32_t splits;      // splits in the static decode grid
     int32_t row_groups;  // ceil(group / 16): 16 query-head rows per decode CTA
+    int32_t decode_max_q;  // sequences with 1..decode_max_q new tokens take the decode path
     float scale;         // softmax scale
     float scale_log2;    // scale * log2(e)
 };
 
 cudaError_t launch_decode(const Args& a, cudaStream_t stream);
 cudaError_t launch_prefill(const Args& a, cudaStream_t stream);
+cudaError_t launch_cache_write(const void* k_new, const void* v_new, const int64_t* slot_mapping, void* k_cache,
+                               void* v_cache, int64_t num_tokens, int64_t num_blocks, int32_t page_size,
+                               int32_t num_kv_heads, int32_t head_dim, int32_t* err, cudaStream_t stream);
+
+// New tokens a sequence may have and still take the decode path: its query rows
+// (tokens x the G heads of a KV head) must fit one 16-row MMA tile.  With more
+// than 16 heads per KV head the decode path takes single-token queries only.
+inline int32_t decode_max_q(int32_t group) { return group <= 16 ? 16 / group : 1; }
 
 // Workspace layout shared by pa_forward and pa_forward_noalloc: a 256-byte
-// header (sticky error word), the split ticket counters (must be zero before a
-// call; each call leaves them zero), then the partials O and (m, l).
+// header (sticky error word), an area of split ticket counters (zero before and
+// after every call: the last CTA of each ticket resets it), then the partials O
+// and (m, l) of [B, splits, decode_max_q, Hq] rows.  The counter area never
+// overlaps bytes that held partials: its size is a property of the buffer
+// (counter_area_bytes, at least what the call needs), not of the call.
 struct WorkspaceLayout {
-    int64_t counters_off, o_off, ml_off, bytes;
+    int64_t counters_off, counter_bytes, o_off, ml_off, bytes;
 };
-inline WorkspaceLayout workspace_layout(int64_t num_seqs, int32_t num_kv_heads, int32_t row_groups, int32_t splits,
-                                        int32_t num_q_heads, int32_t head_dim) {
-    WorkspaceLayout w{};
+inline int64_t counter_bytes_needed(int64_t num_seqs, int32_t num_kv_heads, int32_t row_groups, int32_t splits) {
     const int64_t counters = splits > 1 ? num_seqs * num_kv_heads * row_groups : 0;
-    const int64_t rows = splits > 1 ? num_seqs * splits * num_q_heads : 0;
+    return ((counters * 4 + 255) / 256) * 256;
+}
+inline WorkspaceLayout workspace_layout(int64_t num_seqs, int32_t num_q_heads, int32_t splits, int32_t head_dim,
+                                        int32_t decode_max_q, int64_t counter_area_bytes) {
+    WorkspaceLayout w{};
+    const int64_t rows = splits > 1 ? num_seqs * splits * decode_max_q * num_q_heads : 0;
     w.counters_off = 256;
-    w.o_off = w.counters_off + ((counters * 4 + 255) / 256) * 256;
+    w.counter_bytes = counter_area_bytes;
+    w.o_off = w.counters_off + counter_area_bytes;
     w.ml_off = w.o_off + rows * head_dim * 4;
     w.bytes = w.ml_off + rows * 2 * 4;
     return w;

@@ -41,6 +41,7 @@
 #include "pa_device.cuh"
 #include "pa_internal.h"
 #include "tc_device.cuh"
+#include "tmap.h"
 
 namespace pa {
 namespace {
@@ -85,7 +86,8 @@ enum Bar {
     kDrain = 21,
 };
 
-__device__ __forceinline__ int tiles_of(int n, int tq) { return n >= 2 ? (n + tq - 1) / tq : 0; }
+// Tiles of a sequence with n new tokens (the decode path takes n <= qmax).
+__device__ __forceinline__ int tiles_of(int n, int tq, int qmax) { return n > qmax ? (n + tq - 1) / tq : 0; }
 
 // Bounded wait by every lane of a warp; the result is made warp-uniform so that a
 // timeout can never leave some lanes at a warp-collective instruction alone.
@@ -121,7 +123,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         int found_b = -1, found_t = 0, base_t = 0;
         for (int b0 = 0; b0 < a.num_seqs && found_b < 0; b0 += 32) {
             const int b = b0 + lane;
-            const int cnt = b < a.num_seqs ? tiles_of(a.query_start_loc[b + 1] - a.query_start_loc[b], tq_tokens) : 0;
+            const int cnt = b < a.num_seqs ? tiles_of(a.query_start_loc[b + 1] - a.query_start_loc[b], tq_tokens, a.decode_max_q) : 0;
             int inc = cnt;
 #pragma unroll
             for (int o = 1; o < 32; o <<= 1) {
@@ -486,23 +488,6 @@ __global__ void __launch_bounds__(kThreads, 1)
 }
 
 // --------------------------------------------------------------- host side
-using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
-                                   const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
-                                   CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
-
-EncodeTiledFn encode_fn() {
-    static EncodeTiledFn fn = nullptr;
-    if (!fn) {
-        void* p = nullptr;
-        cudaDriverEntryPointQueryResult q;
-        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
-                cudaSuccess &&
-            q == cudaDriverEntryPointSuccess)
-            fn = reinterpret_cast<EncodeTiledFn>(p);
-    }
-    return fn;
-}
-
 int tokens_per_tile(int group) { return group <= kM ? kM / group : 0; }
 
 int tiles_bound(const Args& a) {
@@ -525,41 +510,12 @@ cudaError_t launch_d(const Args& a, cudaStream_t stream) {
     }
     const int64_t ctas = prefill_ctas(a);
     if (ctas == 0) return cudaSuccess;
-    EncodeTiledFn enc = encode_fn();
-    if (!enc) return cudaErrorNotSupported;
     const int G = a.group, tq = tokens_per_tile(G);
     CUtensorMap tq_map, tk_map, tv_map;
-    {
-        // q [T, Hq, D] as (D, Hq, T); one box = 64 columns x G heads x TQ tokens
-        const cuuint64_t dims[3] = {static_cast<cuuint64_t>(D), static_cast<cuuint64_t>(a.num_q_heads),
-                                    static_cast<cuuint64_t>(a.num_tokens)};
-        const cuuint64_t strides[2] = {static_cast<cuuint64_t>(D) * 2,
-                                       static_cast<cuuint64_t>(a.num_q_heads) * D * 2};
-        const cuuint32_t box[3] = {64, static_cast<cuuint32_t>(G), static_cast<cuuint32_t>(tq)};
-        const cuuint32_t es[3] = {1, 1, 1};
-        if (enc(&tq_map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(a.q), dims, strides, box, es,
-                CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
-            return cudaErrorInvalidValue;
-    }
-    {
-        // cache [NB, P, Hkv, D] as (D, Hkv, P, NB); one box = 64 columns x 1 head x 16 slots of one page
-        const cuuint64_t dims[4] = {static_cast<cuuint64_t>(D), static_cast<cuuint64_t>(a.num_kv_heads),
-                                    static_cast<cuuint64_t>(kPage), static_cast<cuuint64_t>(a.num_blocks)};
-        const cuuint64_t strides[3] = {static_cast<cuuint64_t>(D) * 2,
-                                       static_cast<cuuint64_t>(a.num_kv_heads) * D * 2,
-                                       static_cast<cuuint64_t>(kPage) * a.num_kv_heads * D * 2};
-        const cuuint32_t box[4] = {64, 1, kPage, 1};
-        const cuuint32_t es[4] = {1, 1, 1, 1};
-        if (enc(&tk_map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(a.k_cache), dims, strides, box, es,
-                CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
-            return cudaErrorInvalidValue;
-        if (enc(&tv_map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(a.v_cache), dims, strides, box, es,
-                CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
-            return cudaErrorInvalidValue;
-    }
+    if (!encode_q_map(&tq_map, a.q, D, a.num_q_heads, a.num_tokens, G, tq) ||
+        !encode_cache_map(&tk_map, a.k_cache, D, a.num_kv_heads, a.num_blocks) ||
+        !encode_cache_map(&tv_map, a.v_cache, D, a.num_kv_heads, a.num_blocks))
+        return cudaErrorInvalidValue;
     prefill_tc_kernel<D><<<static_cast<unsigned>(ctas), kThreads, S::kAlloc, stream>>>(tq_map, tk_map, tv_map, a, tq,
                                                                                        tiles_bound(a));
     return cudaGetLastError();

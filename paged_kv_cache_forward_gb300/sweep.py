@@ -37,12 +37,13 @@ HQ, HKV, D, PAGE = 32, 8, 128, 16
 MAX_KV_BYTES = 6 << 30
 
 
-def candidates(bound: int, batch: int, slots: int):
+def candidates(bound: int, batch: int, sms: int):
     base = {64, 128, 256, 512, 1024, 2048, 4096, 8192, 16384}
-    # split sizes that give exactly k full waves of CTAs
-    for k in (1, 2, 3, 4):
-        pages = math.ceil(bound * batch * HKV / (k * slots) / PAGE)
-        base.add(max(1, pages) * PAGE)
+    # split sizes that give whole waves of CTAs at 2 or 3 resident CTAs per SM
+    for per_sm in (2, 3):
+        for k in (1, 2, 3):
+            pages = math.ceil(bound * batch * HKV / (k * per_sm * sms) / PAGE)
+            base.add(max(1, pages) * PAGE)
     return sorted(c for c in base if 16 <= c <= bound)
 
 
@@ -68,8 +69,10 @@ def time_shape(bound, batch, chunk, pools, stream, steps_per_graph=16, reps=30):
             g.replay()
         e1.record()
     stream.synchronize()
-    if pa.device_error(stream):
-        raise RuntimeError("device error during the sweep")
+    code = pa.device_error(stream)
+    if code:
+        raise RuntimeError(f"device error {code} ({pa.DEVICE_ERRORS.get(code)}) at bound {bound}, batch {batch}, "
+                           f"split {chunk}")
     return e0.elapsed_time(e1) * 1e3 / (reps * M)  # us per step
 
 
@@ -106,7 +109,7 @@ def main(argv=None):
     build.build()
     pa.load()
     props = torch.cuda.get_device_properties(0)
-    slots = props.multi_processor_count * 2  # two decode CTAs fit per SM
+    sms = props.multi_processor_count
     l2 = getattr(props, "L2_cache_size", 128 << 20)
     stream = torch.cuda.Stream()
     gen = torch.Generator(device="cuda").manual_seed(0)
@@ -118,8 +121,12 @@ def main(argv=None):
                 continue
             pools, kv = make_pools(bound, batch, l2, gen)
             res = []
-            for chunk in candidates(bound, batch, slots):
-                us = time_shape(bound, batch, chunk, pools, stream)
+            for chunk in candidates(bound, batch, sms):
+                try:
+                    us = time_shape(bound, batch, chunk, pools, stream)
+                except RuntimeError as e:  # reported, and the candidate is not used
+                    print(f"skipped: {e}", flush=True)
+                    continue
                 res.append((us, chunk))
             res.sort()
             us, chunk = res[0]

@@ -276,6 +276,16 @@ def mixed_batch(seed: int = 0, n_prefill: int = 4, prefill_len: int = 512, n_dec
                       name="mixed")
 
 
+def spec_decode(seed: int = 0, batch: int = 16, n: int = 4, lo: int = 2048, hi: int = 8192,
+                poison: bool = True) -> Batch:
+    """Speculative decoding: 16 sequences each verifying 4 draft tokens, context
+    uniform on [2048, 8192] (the 4 new tokens included)."""
+    g = torch.Generator().manual_seed(seed)
+    lens = _uniform_ints(g, lo, hi, batch)
+    return make_batch([n] * batch, lens, **LLAMA, seed=seed, g=g,
+                      max_pages=(hi + PAGE_SIZE - 1) // PAGE_SIZE, poison=poison, name="spec_decode")
+
+
 CONFIGS = {
     "tiny_decode": tiny_decode,
     "llama_decode_1024": lambda seed=0, poison=True: llama_decode(1024, seed, poison),
@@ -284,6 +294,7 @@ CONFIGS = {
     "batched_decode": batched_decode,
     "varlen_prefill": varlen_prefill,
     "mixed": mixed_batch,
+    "spec_decode": spec_decode,
 }
 
 

@@ -123,3 +123,14 @@ def test_library_has_no_oracle_dependency():
         if f.endswith(".py") and f != "workloads.py":
             src = open(os.path.join(ROOT, "paged_kv_cache_forward_gb300", f)).read()
             assert "import oracle" not in src and "from oracle" not in src, f
+
+
+def test_cache_write_rejects_before_cuda(lib):
+    d = B.CacheDims(num_tokens=4, num_blocks=0, num_kv_heads=8, head_dim=128, page_size=16)
+    assert lib.pa_cache_write(None, None, None, None, None, ctypes.byref(d), None) == B.PA_ERR_INVALID_ARG
+    d = B.CacheDims(num_tokens=4, num_blocks=8, num_kv_heads=1, head_dim=12, page_size=16)
+    assert lib.pa_cache_write(None, None, None, None, None, ctypes.byref(d), None) == B.PA_ERR_UNSUPPORTED
+    d = B.CacheDims(num_tokens=0, num_blocks=8, num_kv_heads=8, head_dim=128, page_size=16)
+    assert lib.pa_cache_write(None, None, None, None, None, ctypes.byref(d), None) == B.PA_OK
+    d = B.CacheDims(num_tokens=4, num_blocks=8, num_kv_heads=8, head_dim=128, page_size=16)
+    assert lib.pa_cache_write(None, None, None, None, None, ctypes.byref(d), None) == B.PA_ERR_INVALID_ARG

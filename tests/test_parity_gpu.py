@@ -271,3 +271,58 @@ def test_query_longer_than_context_flagged():
     got = run(b, check_errors=False)
     assert pa.device_error() == 3
     assert torch.isfinite(got.float()).all()
+
+
+def test_many_splits_long_context():
+    # 1024 splits of 64 keys for each of two 65536-key sequences: the split merge
+    # reads a long run of partials and the ticket counters see many arrivals
+    b = W.make_batch([1, 1], [65536, 65536], 32, 8, 128, seed=71, max_pages=4096)
+    got = run(b, kv_chunk=64)
+    rows = [(0, h) for h in range(32)] + [(1, h) for h in range(0, 32, 3)]
+    ref = oracle.batch_attention(b, rows=rows)
+    assert_close(torch.stack([got[t, h] for t, h in rows]), ref, "65536 x 2, 64-key splits")
+
+
+# ------------------------------------------------- multi-token (speculative) decode
+
+@pytest.mark.parametrize("Hq,Hkv,D", [(32, 8, 128), (8, 8, 128), (16, 2, 64), (12, 4, 128)])
+def test_multi_token_decode(Hq, Hkv, D):
+    """Sequences with 1 .. 16/G new tokens take the decode path (rows = tokens x
+    G heads, each row masked at its own position); one more token goes to the
+    prefill kernel."""
+    G = Hq // Hkv
+    nmax = 16 // G
+    q_lens = list(range(1, nmax + 1)) + [nmax, nmax + 1]
+    seq_lens = [300 + 37 * i for i in range(nmax)] + [5000, 700]
+    b = W.make_batch(q_lens, seq_lens, Hq, Hkv, D, seed=80 + G, max_pages=320)
+    ref = oracle.batch_attention(b)
+    for chunk in (0, 64):
+        assert_close(run(b, kv_chunk=chunk), ref, f"G {G} chunk {chunk}")
+
+
+def test_multi_token_decode_spikes_bit_exact():
+    b, exp = W.spike_batch([2, 3, 4, 1, 4], [40, 1000, 5000, 17, 4], 32, 8, 128, seed=26, max_pages=320)
+    want = _codes(exp, 128)
+    for chunk in (0, 64, 1024):
+        got = run(b, kv_chunk=chunk)
+        bad = (got.view(torch.int16) != want.view(torch.int16)).any(-1)
+        assert not bad.any(), (chunk, torch.nonzero(bad)[:5].tolist())
+
+
+def test_workspace_reuse_across_growing_batches():
+    """Calls on one stream whose split-ticket counter area grows (more sequences)
+    after calls that wrote partials: the counters must never land on bytes that
+    held partials."""
+    s = torch.cuda.Stream()
+    for B in (2, 9, 40, 3, 64):
+        g = torch.Generator().manual_seed(200 + B)
+        lens = torch.randint(600, 3000, (B,), generator=g).tolist()
+        b = W.make_batch([1] * B, lens, 32, 8, 128, seed=200 + B, max_pages=200)
+        d = b.to("cuda")
+        out = torch.full_like(d.q, float("nan"))
+        with torch.cuda.stream(s):
+            pa.forward(d.q, d.k_cache, d.v_cache, d.block_table, d.seq_lens, d.query_start_loc, out,
+                       scale=b.scale, kv_chunk=256)
+        s.synchronize()
+        assert pa.device_error(s) == 0
+        assert_close(out.cpu(), oracle.batch_attention(b), f"B {B}")
