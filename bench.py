@@ -66,6 +66,9 @@ def parse_args(argv=None):
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=10.0, help="target CPU time of the oracle leg")
+    ap.add_argument("--layers", type=int, default=0,
+                    help="model-step mode: L layers, each with its own KV cache, one pa_forward per layer; "
+                         "times one CUDA graph of all L layers against L one-layer graphs and eager calls")
     ap.add_argument("--min-warm-ms", type=float, default=500.0,
                     help="graph warm-up time before the timed region (clocks settle); 0 for profiling runs")
     return ap.parse_args(argv)
@@ -375,13 +378,18 @@ def run_ours(args):
     est_ms = e0.elapsed_time(e1) / 10
     steps = args.steps if args.steps else int(min(200000, max(200, 2000.0 / max(est_ms, 1e-3))))
 
-    # graphs of M consecutive steps each, rotating over the R pool copies; every
-    # step's dominant kernel bracketed by its own pair of external events
-    M = min(steps, max(R, 64))
+    # graphs of M consecutive steps each, rotating over the R pool copies.  One
+    # step in EVERY has its dominant kernel bracketed by a pair of external
+    # events (event nodes between kernels cost the graph a few microseconds, so
+    # not every step carries them); their durations give roofline.achieved.
+    EVERY = 8
+    M = min(steps, max(R, 256))
     M = max(R, (M // R) * R) if M >= R else M
+    key = "prefill" if dominant == "prefill" else "decode"
 
     def make_graph(n):
-        evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(n)]
+        evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+               for _ in range(0, n, EVERY)]
         # torch creates the CUDA event on its first record(); do that outside the
         # capture so that the library receives real handles to re-record.
         for e_a, e_b in evs:
@@ -391,8 +399,11 @@ def run_ours(args):
         g = torch.cuda.CUDAGraph()
         with torch.cuda.graph(g, stream=stream):
             for i in range(n):
-                key = "prefill" if dominant == "prefill" else "decode"
-                call(i, events={f"{key}_start_event": evs[i][0], f"{key}_stop_event": evs[i][1]})
+                ev = None
+                if i % EVERY == 0:
+                    e_a, e_b = evs[i // EVERY]
+                    ev = {f"{key}_start_event": e_a, f"{key}_stop_event": e_b}
+                call(i, events=ev)
         return g, evs
 
     full, rem = divmod(steps, M)
@@ -423,6 +434,7 @@ def run_ours(args):
     barrier(world)
     sampler.stop()
     region_ms = start.elapsed_time(stop)
+    # the last replay of each graph left its events' times
     kernel_ms = [a.elapsed_time(b) for a, b in ev_main + ev_rem]
     assert pa.device_error(stream) == 0
 
@@ -503,6 +515,9 @@ def run_ours(args):
                 "l2": f"inputs rotate over {R} KV pool copies ({R} x {work['kv_bytes'] / 2**20:.0f} MiB "
                       f"> 3 x L2 {l2 / 2**20:.0f} MiB)" if R > 1 else "KV bytes per step > 3 x L2",
                 "graph": f"CUDA graphs of {M} steps", "kv_chunk": plan["kv_chunk"], "splits": plan["splits"],
+                "decode_stages": plan["decode_stages"],
+                "kernel_timing": f"CUDA events around the dominant kernel of one step in {EVERY} of the "
+                                 f"timed graphs ({len(kernel_ms)} launches of the last replays)",
                 "parallelism": f"dp{world}" if world > 1 else "single GPU",
             },
             "tok_s": total_tokens * steps / (region_ms_max / 1e3),
@@ -520,10 +535,144 @@ def run_ours(args):
     return 0
 
 
+def run_layers(args):
+    """A decoder step of L attention layers: every layer has its own paged KV
+    cache (same shape, same block table), its own queries and output, and one
+    pa_forward call.  Times three ways of launching the same L calls: one CUDA
+    graph of the whole step, L one-layer graphs replayed back to back, and L
+    eager calls.  value = KV bytes of all layers per second in the one-graph mode."""
+    import torch
+    import paged_kv_cache_forward_gb300 as pa
+    from paged_kv_cache_forward_gb300 import build as build_mod
+    from paged_kv_cache_forward_gb300 import workloads as W
+
+    rank, world, local = dist_env()
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    build_mod.build()
+    pa.load()
+
+    L = args.layers
+    batch = W.CONFIGS[args.config](seed=rank_seed(args.seed, rank))
+    work = work_of(batch)
+    metric, unit, _ = metric_of(args.config)
+    pool_bytes = 2 * batch.k_cache.numel() * batch.k_cache.element_size()
+    if L * pool_bytes > (96 << 30):
+        raise SystemExit(f"{L} layers x {pool_bytes / 2**30:.1f} GiB of KV pool exceed 96 GiB")
+    d = batch.to(dev)
+    gen = torch.Generator(device=dev).manual_seed(rank_seed(args.seed, rank) + 1)
+    ks = [d.k_cache] + [torch.randn(d.k_cache.shape, generator=gen, device=dev).to(torch.bfloat16)
+                        for _ in range(L - 1)]
+    vs = [d.v_cache] + [torch.randn(d.v_cache.shape, generator=gen, device=dev).to(torch.bfloat16)
+                        for _ in range(L - 1)]
+    qs = [d.q] + [torch.randn(d.q.shape, generator=gen, device=dev).to(torch.bfloat16) for _ in range(L - 1)]
+    outs = [torch.empty_like(d.q) for _ in range(L)]
+    stream = torch.cuda.Stream(device=dev)
+    plan = pa.plan_for(d.q, d.k_cache, d.block_table, d.seq_lens, kv_chunk=args.kv_chunk)
+    pa.prepare(d.q, d.k_cache, d.block_table, d.seq_lens, kv_chunk=args.kv_chunk, stream=stream)
+
+    def layer(i):
+        pa.forward(qs[i], ks[i], vs[i], d.block_table, d.seq_lens, d.query_start_loc, outs[i],
+                   scale=batch.scale, kv_chunk=args.kv_chunk, stream=stream)
+
+    def model_step():
+        for i in range(L):
+            layer(i)
+
+    with torch.cuda.stream(stream):
+        for _ in range(max(3, args.warmup)):
+            model_step()
+    stream.synchronize()
+    assert pa.device_error(stream) == 0
+
+    g_full = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g_full, stream=stream):
+        model_step()
+    g_layers = []
+    for i in range(L):
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            layer(i)
+        g_layers.append(g)
+
+    modes = {
+        "graph_full": lambda: g_full.replay(),
+        "graph_per_layer": lambda: [g.replay() for g in g_layers],
+        "eager": model_step,
+    }
+    steps = args.steps or 50
+    sampler = ClockSampler(local).start()
+    times = {}
+    t0 = time.time()
+    for name, fn in modes.items():
+        with torch.cuda.stream(stream):
+            for _ in range(max(3, args.warmup)):
+                fn()
+        stream.synchronize()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        barrier(world)
+        torch.cuda.synchronize(dev)
+        with torch.cuda.stream(stream):
+            a.record()
+            for _ in range(steps):
+                fn()
+            b.record()
+        stream.synchronize()
+        torch.cuda.synchronize(dev)
+        barrier(world)
+        times[name] = reduce_max(a.elapsed_time(b), world, dev) / steps
+    t1 = time.time()
+    sampler.stop()
+    assert pa.device_error(stream) == 0
+
+    # the one-graph step must give the eager step's outputs
+    ref = [o.clone() for o in outs]
+    g_full.replay()
+    stream.synchronize()
+    identical = all(torch.equal(a, b) for a, b in zip(ref, outs))
+
+    total_kv = reduce_sum(work["kv_bytes"], world, dev) * L
+    total_flops = reduce_sum(work["flops"], world, dev) * L
+    ms = times["graph_full"]
+    value = value_of(args.config, {"kv_bytes": total_kv, "flops": total_flops}, ms / 1e3)
+    peaks = measured_peaks()
+    if rank == 0:
+        line = {
+            "metric": metric, "value": value, "unit": unit, "n_gpus": world, "steps": steps,
+            "warmup": max(3, args.warmup), "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+            "config": {
+                "workload": f"{L} layers x {args.config}: {DESCRIPTIONS.get(args.config, '')}",
+                "layers": L, "kv_bytes_per_step": int(total_kv), "kv_chunk": plan["kv_chunk"],
+                "splits": plan["splits"], "l2": f"KV bytes per step {total_kv / 2**20:.0f} MiB "
+                                                 f"({'>' if total_kv > 3 * (128 << 20) else '<='} 3 x L2)",
+                "parallelism": f"dp{world}" if world > 1 else "single GPU",
+            },
+            "graph_modes_ms_per_step": times,
+            "launch_overhead_us_per_layer": {
+                k: (v - times["graph_full"]) * 1e3 / L for k, v in times.items() if k != "graph_full"},
+            "us_per_layer": ms * 1e3 / L,
+            "hbm_frac_step": (total_kv / world) / (ms / 1e3) / 1e9 / peaks["hbm"][0],
+            "graph_matches_eager": identical,
+            "gpu_launches": plan["launches"] * L * steps,
+            "clocks": sampler.summary(t0, t1),
+        }
+        print(json.dumps(line))
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+    return 0 if identical else 1
+
+
 def main(argv=None):
     args = parse_args(argv)
     if args.impl == "reference":
         return run_reference(args)
+    if args.layers:
+        return run_layers(args)
     return run_ours(args)
 
 

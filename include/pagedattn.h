@@ -96,7 +96,15 @@ typedef struct {
 typedef struct {
     int32_t kv_chunk;  /* 0: from the tuned table; else keys per split (multiple
                           of page_size); a chunk >= max_pages * P means no split */
-    int32_t reserved;
+    int32_t decode_stages;  /* decode kernel variant: pipeline depth in pages per  */
+    int32_t decode_warps;   /* warp, and warps per CTA.  Both 0: from the tuned
+                               table; either set: that variant, the other field
+                               defaulting to 2 stages / 4 warps.  Built variants
+                               (warps, stages): (4, 2..4), (8, 2..3), (12, 2);
+                               others are PA_ERR_INVALID_ARG.  Deeper pipelines
+                               and more warps keep more bytes in flight per CTA
+                               but fit fewer CTAs on an SM. */
+    int32_t reserved;       /* 0 */
     /* cudaEvent_t handles recorded on the stream immediately before and after
        the decode kernel and the prefill kernel (NULL: not recorded). */
     void* decode_start_event;
@@ -115,6 +123,8 @@ typedef struct {
     int64_t prefill_ctas;     /* prefill kernel grid                           */
     int64_t workspace_bytes;  /* scratch this call needs                       */
     int32_t launches;         /* kernels launched per pa_forward               */
+    int32_t decode_stages;    /* decode pipeline depth (pages per warp)        */
+    int32_t decode_warps;     /* warps per decode CTA                          */
     int32_t reserved;
 } pa_plan_info;
 

@@ -37,13 +37,17 @@ struct LutEntry {
     int32_t max_bound;  // applies when context bound <= max_bound
     int32_t max_seqs;   // ... and num_seqs <= max_seqs
     int32_t kv_chunk;
+    int32_t decode_stages;  // 0: the default depth
+    int32_t decode_warps;   // 0: the default warps per CTA
 };
 #include "lut_gb300.inc"
 
-int32_t table_chunk(int64_t bound, int32_t num_seqs) {
+constexpr int32_t kDefaultDecodeStages = 2, kDefaultDecodeWarps = 4;
+
+const LutEntry& table_entry(int64_t bound, int32_t num_seqs) {
     for (const LutEntry& e : kSplitTable)
-        if (bound <= e.max_bound && num_seqs <= e.max_seqs) return e.kv_chunk;
-    return kSplitTable[sizeof(kSplitTable) / sizeof(kSplitTable[0]) - 1].kv_chunk;
+        if (bound <= e.max_bound && num_seqs <= e.max_seqs) return e;
+    return kSplitTable[sizeof(kSplitTable) / sizeof(kSplitTable[0]) - 1];
 }
 
 // ----------------------------------------------------------------- validation
@@ -86,10 +90,22 @@ pa_status make_plan(const pa_dims* d, const pa_options* o, Plan* p) {
     pa_status st = check_dims(d);
     if (st != PA_OK) return st;
     const int64_t bound = static_cast<int64_t>(d->max_pages) * d->page_size;
-    int64_t chunk = (o && o->kv_chunk) ? o->kv_chunk : table_chunk(bound, d->num_seqs);
+    const LutEntry& te = table_entry(bound, d->num_seqs);
+    int64_t chunk = (o && o->kv_chunk) ? o->kv_chunk : te.kv_chunk;
     if (chunk < d->page_size || chunk % d->page_size)
         return fail(PA_ERR_INVALID_ARG, "kv_chunk %lld must be a positive multiple of page_size",
                     static_cast<long long>(chunk));
+    // the table's variant, unless the caller forces one (fully or in part)
+    int32_t stages = te.decode_stages ? te.decode_stages : kDefaultDecodeStages;
+    int32_t warps = te.decode_warps ? te.decode_warps : kDefaultDecodeWarps;
+    if (o && (o->decode_stages || o->decode_warps)) {
+        stages = o->decode_stages ? o->decode_stages : kDefaultDecodeStages;
+        warps = o->decode_warps ? o->decode_warps : kDefaultDecodeWarps;
+    }
+    if (!pa::decode_variant_supported(warps, stages))
+        return fail(PA_ERR_INVALID_ARG,
+                    "decode variant (%d warps, %d stages) is not one of (4, 2..4), (8, 2..3), (12, 2)", warps,
+                    stages);
     if (chunk > bound) chunk = bound;
     const int32_t group = d->num_q_heads / d->num_kv_heads;
     pa::Args& a = p->args;
@@ -106,6 +122,8 @@ pa_status make_plan(const pa_dims* d, const pa_options* o, Plan* p) {
     a.splits = static_cast<int32_t>((bound + chunk - 1) / chunk);
     a.row_groups = (group + 15) / 16;
     a.decode_max_q = pa::decode_max_q(group);
+    a.decode_stages = stages;
+    a.decode_warps = warps;
     p->kv_chunk = a.kv_chunk;
     p->splits = a.splits;
     p->row_groups = a.row_groups;
@@ -232,7 +250,8 @@ pa_status pa_plan(const pa_dims* dims, const pa_options* opts, pa_plan_info* inf
     info->prefill_ctas = p.prefill_ctas;
     info->workspace_bytes = p.ws_bytes;
     info->launches = p.launches;
-    info->reserved = 0;
+    info->decode_stages = p.args.decode_stages;
+    info->decode_warps = p.args.decode_warps;
     return PA_OK;
 }
 
@@ -383,6 +402,6 @@ const char* pa_status_string(pa_status status) {
 
 const char* pa_last_error(void) { return g_last_error; }
 
-int32_t pa_version(void) { return 100; }
+int32_t pa_version(void) { return 101; }
 
 }  // extern "C"

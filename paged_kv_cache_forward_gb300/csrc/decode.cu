@@ -38,20 +38,15 @@
 namespace pa {
 namespace {
 
-// Warps per CTA and pipeline stages per warp (the offline sweep's choice; a
-// build may override them with -DPA_DECODE_WARPS=.. -DPA_DECODE_STAGES=..).
-#ifndef PA_DECODE_WARPS
-#define PA_DECODE_WARPS 4
-#endif
-#ifndef PA_DECODE_STAGES
-#define PA_DECODE_STAGES 2
-#endif
-constexpr int kWarps = PA_DECODE_WARPS;
-constexpr int kStages = PA_DECODE_STAGES;
+// Warps per CTA and pipeline depth per warp are template parameters chosen per
+// call (from the offline table): a warp keeps kStages - 1 pages in flight while
+// it computes one, and the shared memory of a CTA (kStages pages of K and V per
+// warp) sets how many CTAs share an SM.  Few long sequences want many warps per
+// CTA (few splits, so a short merge); large batches want small CTAs.
 constexpr int kPage = 16;
 constexpr int kRows = 16;  // MMA M: query-head rows per CTA
 
-template <int D>
+template <int D, int kWarps, int kStages>
 struct DecodeTile {
     static constexpr int kRowBytes = D * 2;
     static constexpr int kChunksPerRow = D / 8;                 // 16-byte chunks
@@ -68,7 +63,7 @@ struct DecodeTile {
 // Byte offset of 16-byte chunk c of row r: chunks are XOR-permuted by r % 8.
 template <int D>
 __device__ __forceinline__ uint32_t swz(int r, int c) {
-    return r * DecodeTile<D>::kRowBytes + ((c ^ (r & 7)) << 4);
+    return r * (D * 2) + ((c ^ (r & 7)) << 4);
 }
 
 // Partial-row index of (sequence b, split s, new token i, query head hq).
@@ -91,7 +86,8 @@ __device__ __forceinline__ void merge_splits(const Args& a, int b, const int* to
     const int64_t split_rows = static_cast<int64_t>(a.decode_max_q) * a.num_q_heads;
     const int64_t split_ml = split_rows * 2;  // stride between splits in ws_ml
     const int64_t split_o = split_rows * D;   // ... and in ws_o
-    for (int r = warp; r < rows; r += kWarps) {
+    const int nwarps = blockDim.x >> 5;
+    for (int r = warp; r < rows; r += nwarps) {
         const float* ml = a.ws_ml + partial_row(a, b, 0, tok[r], head[r]) * 2;
         float M = -INFINITY;
         for (int s = lane; s < nsplits; s += 32) M = fmaxf(M, __ldcg(ml + s * split_ml));
@@ -151,9 +147,9 @@ __device__ __forceinline__ void merge_splits(const Args& a, int b, const int* to
     }
 }
 
-template <int D>
+template <int D, int kWarps, int kStages>
 __global__ void __launch_bounds__(kWarps * 32) decode_splitkv_kernel(const Args a) {
-    using Tile = DecodeTile<D>;
+    using Tile = DecodeTile<D, kWarps, kStages>;
     extern __shared__ __align__(128) uint8_t smem[];
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
@@ -315,12 +311,28 @@ __global__ void __launch_bounds__(kWarps * 32) decode_splitkv_kernel(const Args 
             }
         const float mx_lo = quad_max(fmaxf(fmaxf(sc[0][0], sc[0][1]), fmaxf(sc[1][0], sc[1][1])));
         const float mx_hi = quad_max(fmaxf(fmaxf(sc[0][2], sc[0][3]), fmaxf(sc[1][2], sc[1][3])));
-        const float mn_lo = fmaxf(m_lo, mx_lo), mn_hi = fmaxf(m_hi, mx_hi);
-        const float mu_lo = mn_lo == -INFINITY ? 0.f : mn_lo;
-        const float mu_hi = mn_hi == -INFINITY ? 0.f : mn_hi;
-        const float al_lo = fast_exp2(m_lo - mu_lo), al_hi = fast_exp2(m_hi - mu_hi);
-        m_lo = mn_lo;
-        m_hi = mn_hi;
+        // The running max only moves when a row's max grows by more than 2^8
+        // (log2 units), and only then are O and l rescaled; P <= 2^8 otherwise,
+        // and the final O / l is the same.  The four threads of a row hold the
+        // same max, so they take the same decision.
+        const bool need_lo = mx_lo > m_lo + 8.f, need_hi = mx_hi > m_hi + 8.f;
+        if (__any_sync(0xffffffffu, need_lo || need_hi)) {
+            const float al_lo = need_lo ? fast_exp2(m_lo - mx_lo) : 1.f;  // 0 when m was -inf
+            const float al_hi = need_hi ? fast_exp2(m_hi - mx_hi) : 1.f;
+            if (need_lo) m_lo = mx_lo;
+            if (need_hi) m_hi = mx_hi;
+            l_lo *= al_lo;
+            l_hi *= al_hi;
+#pragma unroll
+            for (int i = 0; i < D / 8; ++i) {
+                o[i][0] *= al_lo;
+                o[i][1] *= al_lo;
+                o[i][2] *= al_hi;
+                o[i][3] *= al_hi;
+            }
+        }
+        const float mu_lo = m_lo == -INFINITY ? 0.f : m_lo;
+        const float mu_hi = m_hi == -INFINITY ? 0.f : m_hi;
 
         // P in bf16 as the A operand of P V; the sums use the same rounded P.
         uint32_t pa[4];
@@ -328,15 +340,8 @@ __global__ void __launch_bounds__(kWarps * 32) decode_splitkv_kernel(const Args 
         pa[1] = pack_bf16(fast_exp2(sc[0][2] - mu_hi), fast_exp2(sc[0][3] - mu_hi));
         pa[2] = pack_bf16(fast_exp2(sc[1][0] - mu_lo), fast_exp2(sc[1][1] - mu_lo));
         pa[3] = pack_bf16(fast_exp2(sc[1][2] - mu_hi), fast_exp2(sc[1][3] - mu_hi));
-        l_lo = l_lo * al_lo + ((bf16_lo(pa[0]) + bf16_hi(pa[0])) + (bf16_lo(pa[2]) + bf16_hi(pa[2])));
-        l_hi = l_hi * al_hi + ((bf16_lo(pa[1]) + bf16_hi(pa[1])) + (bf16_lo(pa[3]) + bf16_hi(pa[3])));
-#pragma unroll
-        for (int i = 0; i < D / 8; ++i) {
-            o[i][0] *= al_lo;
-            o[i][1] *= al_lo;
-            o[i][2] *= al_hi;
-            o[i][3] *= al_hi;
-        }
+        l_lo += (bf16_lo(pa[0]) + bf16_hi(pa[0])) + (bf16_lo(pa[2]) + bf16_hi(pa[2]));
+        l_hi += (bf16_lo(pa[1]) + bf16_hi(pa[1])) + (bf16_lo(pa[3]) + bf16_hi(pa[3]));
         // O += P V: V rows are tokens, so the B fragments come from transposed loads.
         {
             const int mi = lane >> 3;
@@ -417,25 +422,44 @@ __global__ void __launch_bounds__(kWarps * 32) decode_splitkv_kernel(const Args 
     if (threadIdx.x == 0) *counter = 0;
 }
 
-template <int D>
+template <int D, int kWarps, int kStages>
 cudaError_t launch_decode_d(const Args& a, cudaStream_t stream) {
-    using Tile = DecodeTile<D>;
+    using Tile = DecodeTile<D, kWarps, kStages>;
     static bool configured[64] = {};  // the attribute is set once per device
     int dev = 0;
     cudaGetDevice(&dev);
     if (!configured[dev & 63]) {
-        cudaError_t e = cudaFuncSetAttribute(decode_splitkv_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             Tile::kSmemBytes);
+        cudaError_t e = cudaFuncSetAttribute(decode_splitkv_kernel<D, kWarps, kStages>,
+                                             cudaFuncAttributeMaxDynamicSharedMemorySize, Tile::kSmemBytes);
         if (e != cudaSuccess) return e;
         configured[dev & 63] = true;
     }
     const int64_t ctas = decode_ctas(a);
     if (ctas == 0) return cudaSuccess;
-    decode_splitkv_kernel<D><<<static_cast<unsigned>(ctas), kWarps * 32, Tile::kSmemBytes, stream>>>(a);
+    decode_splitkv_kernel<D, kWarps, kStages>
+        <<<static_cast<unsigned>(ctas), kWarps * 32, Tile::kSmemBytes, stream>>>(a);
     return cudaGetLastError();
 }
 
+template <int D>
+cudaError_t launch_decode_variant(const Args& a, cudaStream_t stream) {
+    switch (a.decode_warps * 16 + a.decode_stages) {
+        case 4 * 16 + 2: return launch_decode_d<D, 4, 2>(a, stream);
+        case 4 * 16 + 3: return launch_decode_d<D, 4, 3>(a, stream);
+        case 4 * 16 + 4: return launch_decode_d<D, 4, 4>(a, stream);
+        case 8 * 16 + 2: return launch_decode_d<D, 8, 2>(a, stream);
+        case 8 * 16 + 3: return launch_decode_d<D, 8, 3>(a, stream);
+        case 12 * 16 + 2: return launch_decode_d<D, 12, 2>(a, stream);
+        default: return cudaErrorInvalidValue;
+    }
+}
+
 }  // namespace
+
+bool decode_variant_supported(int warps, int stages) {
+    return (warps == 4 && stages >= 2 && stages <= 4) || (warps == 8 && (stages == 2 || stages == 3)) ||
+           (warps == 12 && stages == 2);
+}
 
 int64_t decode_ctas(const Args& a) {
     return static_cast<int64_t>(a.num_seqs) * a.num_kv_heads * a.row_groups * a.splits;
@@ -443,8 +467,8 @@ int64_t decode_ctas(const Args& a) {
 
 cudaError_t launch_decode(const Args& a, cudaStream_t stream) {
     switch (a.head_dim) {
-        case 64: return launch_decode_d<64>(a, stream);
-        case 128: return launch_decode_d<128>(a, stream);
+        case 64: return launch_decode_variant<64>(a, stream);
+        case 128: return launch_decode_variant<128>(a, stream);
         default: return cudaErrorInvalidValue;
     }
 }

@@ -123,6 +123,8 @@ extern "C" pa_status pa_forward_noalloc(const void* q, const void* k_cache, cons
     a.splits = info.splits;
     a.row_groups = (a.group + 15) / 16;
     a.decode_max_q = pa::decode_max_q(a.group);
+    a.decode_stages = info.decode_stages;
+    a.decode_warps = info.decode_warps;
     a.scale = scale;
     a.scale_log2 = scale * 1.4426950408889634f;
     const pa::WorkspaceLayout wl =

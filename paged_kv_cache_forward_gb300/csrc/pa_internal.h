@@ -36,6 +36,8 @@ struct Args {
     int32_t splits;      // splits in the static decode grid
     int32_t row_groups;  // ceil(group / 16): 16 query-head rows per decode CTA
     int32_t decode_max_q;  // sequences with 1..decode_max_q new tokens take the decode path
+    int32_t decode_stages; // cp.async pipeline depth per decode warp (pages)
+    int32_t decode_warps;  // warps per decode CTA
     float scale;         // softmax scale
     float scale_log2;    // scale * log2(e)
 };
@@ -78,6 +80,10 @@ inline WorkspaceLayout workspace_layout(int64_t num_seqs, int32_t num_q_heads, i
 
 // Sets the calling thread's pa_last_error() text.
 void set_last_error(const char* msg);
+
+// (warps per CTA, pipeline depth) pairs the decode kernel is built for:
+// (4, 2..4), (8, 2..3), (12, 2).
+bool decode_variant_supported(int warps, int stages);
 
 // Static grid sizes (functions of shapes only), shared with the planner.
 int64_t decode_ctas(const Args& a);

@@ -1,35 +1,42 @@
 // prefill_tc.cu -- causal varlen chunked prefill on the 5th-generation tensor
 // cores (tcgen05 + TMEM + TMA), sm_103a.
 //
-// One CTA owns (query tile, KV head h).  The tile packs TQ = floor(128 / G)
-// consecutive new tokens of one sequence times the G query heads sharing h into
-// the M = 128 rows of one MMA tile, row r = (token r / G, head h*G + r % G): the
-// "Q-Block" item of the five-step list on the Triton unified-attention page
-// (section "What three things the IBM paper got right"), so each KV tile is
-// loaded once for all G heads.  Keys are walked in tiles of 128 (8 pages) up to
-// the tile's last causal position, with the FlashAttention recurrence of "The
-// Flash Attention revolution" (GPU programming guide page): S = Q K^T, causal
-// -inf mask bottom-right aligned ("Flash Attention in Triton"), online softmax,
+// One CTA owns (a pair of query tiles, KV head h).  A tile packs TQ =
+// floor(128 / G) consecutive new tokens of one sequence times the G query heads
+// sharing h into the M = 128 rows of one MMA tile, row r = (token r / G, head
+// h*G + r % G): the "Q-Block" item of the five-step list on the Triton
+// unified-attention page (section "What three things the IBM paper got right"),
+// so each KV tile is loaded once for all G heads.  The two tiles of the pair (A:
+// tokens [i0, i0 + TQ), B: the next TQ tokens) share every K and V tile in
+// shared memory.  Keys are walked in tiles of 128 (8 pages) up to each tile's
+// last causal position, with the FlashAttention recurrence of "The Flash
+// Attention revolution" (GPU programming guide page): S = Q K^T, causal -inf
+// mask bottom-right aligned ("Flash Attention in Triton"), online softmax,
 // O += P V, out = O / l.
 //
-// Warp roles (192 threads):
-//   warp 0      TMA producer: Q once, then per KV tile the K page boxes and the
-//               V page boxes (64 columns x 16 slots of one page and head, 128-byte
-//               swizzle) into separate 3-stage K and V rings, so a K stage is
-//               refilled as soon as its S MMA is done.  Block-table entries are
-//               fetched one group of 4 tiles ahead.  The one page of V that holds
-//               the sequence end is copied by plain loads with zero fill, so no
-//               slot past seq_len reaches the MMA.
-//   warp 1      allocates all 512 TMEM columns (S double buffer, O, P double
-//               buffer); its lane 0 issues the MMAs: S(kt) = Q K(kt)^T (M=128,
-//               N=128, K=D, both operands from shared memory) into TMEM, then
-//               O += P(kt-1) V(kt-1) (A = P read from TMEM, B = V MN-major in shared
-//               memory), so that the softmax of tile kt overlaps the MMAs.
-//   warps 2-5   softmax, one thread per row (TMEM lane): load S from TMEM,
-//               mask, running max in log2 units, P = 2^(x - m) as bf16 pairs
-//               stored straight into TMEM.  The running max is only moved (and O
-//               in TMEM rescaled) when the row max grows by more than 2^8; the
-//               final O / l is exact either way.
+// Warp roles (320 threads):
+//   warp 0      TMA producer: both Q tiles once, then per KV tile the K page
+//               boxes and the V page boxes (64 columns x 16 slots of one page and
+//               head, 128-byte swizzle) into 2-stage K and V rings.  Block-table
+//               entries are fetched one group of 4 tiles ahead.  The one page of
+//               V that holds the sequence end is copied by plain loads with zero
+//               fill, so no slot past seq_len reaches the MMA.
+//   warp 1      allocates all 512 TMEM columns (S and O of each tile); its lane 0
+//               issues the MMAs in the order
+//                   O_A += P_A(j) V(j),  S_A(j+1) = Q_A K(j+1)^T,
+//                   O_B += P_B(j) V(j),  S_B(j+1) = Q_B K(j+1)^T,
+//               so that while the softmax of one tile runs, the tensor cores work
+//               on the other (ping-pong).  P is written as bf16 pairs over the
+//               last 64 columns of its tile's S; the MMA that next overwrites S
+//               is issued after the P V that reads it, and tcgen05 operations of
+//               one thread execute in issue order.
+//   warps 2-5   softmax of tile A, warps 6-9 softmax of tile B: one thread per
+//               row (TMEM lane).  Load S from TMEM in two 64-column halves,
+//               mask, running max in log2 units, P = 2^(x - m) stored straight
+//               into TMEM (keys 64-127 from registers, then keys 0-63 loaded
+//               again, so only half of S is in registers).  The running max
+//               is only moved (and O in TMEM rescaled) when the row max grows by
+//               more than 2^8; the final O / l is exact either way.
 // Every wait on an mbarrier is bounded (2 s); on timeout the CTA records
 // kDevWaitTimeout, stops all roles, drains the MMAs it issued, frees TMEM and
 // exits.
@@ -46,7 +53,7 @@
 namespace pa {
 namespace {
 
-constexpr int kThreads = 192;
+constexpr int kThreads = 320;
 constexpr int kM = 128;            // rows per tile
 constexpr int kKeys = 128;         // keys per KV tile
 constexpr int kPage = 16;
@@ -54,19 +61,21 @@ constexpr int kPagesPerTile = kKeys / kPage;
 constexpr int kHalfBytes = 128 * 128;  // 128 rows x 128 B: one 64-column half of a tile
 constexpr uint64_t kTimeoutNs = 2000000000ull;
 constexpr uint32_t kTmemCols = 512;
-constexpr uint32_t kTmemS0 = 0, kTmemS1 = 128, kTmemO = 256, kTmemP0 = 384, kTmemP1 = 448;
-constexpr int kKStages = 3, kVStages = 3;
+// TMEM columns of tile x: S at 128 x (P over its last 64 columns), O at 256 + 128 x.
+__device__ __forceinline__ uint32_t tmem_s(int x) { return x ? 128u : 0u; }
+__device__ __forceinline__ uint32_t tmem_o(int x) { return x ? 384u : 256u; }
+constexpr int kKStages = 2, kVStages = 2;
 constexpr int kTilesPerGroup = 4;  // block-table prefetch: 4 tiles x 8 pages = one entry per lane
 
 template <int D>
 struct Smem {
     static constexpr int kHalves = D / 64;
-    static constexpr int kTile = kHalves * kHalfBytes;  // one K or V tile (128 keys x D)
-    static constexpr int kQ = 0;
-    static constexpr int kK0 = kQ + kTile;
+    static constexpr int kTile = kHalves * kHalfBytes;  // one Q, K or V tile (128 rows x D)
+    static constexpr int kQ0 = 0;                       // Q_A, then Q_B
+    static constexpr int kK0 = kQ0 + 2 * kTile;
     static constexpr int kV0 = kK0 + kKStages * kTile;
     static constexpr int kBar = kV0 + kVStages * kTile;
-    static constexpr int kNumBars = 22;
+    static constexpr int kNumBars = 16;
     static constexpr int kMisc = kBar + kNumBars * 8;  // tmem address, abort flag, tile info
     static constexpr int kBytes = kMisc + 64;
     static constexpr int kAlloc = kBytes + 1024;  // slack to align the base to 1024
@@ -75,19 +84,20 @@ struct Smem {
 // barrier indices
 enum Bar {
     kQFull = 0,
-    kKFull0 = 1,     // [3]
-    kKEmpty0 = 4,    // [3]
-    kVFull0 = 7,     // [3]
-    kVEmpty0 = 10,   // [3]
-    kSFull0 = 13,    // [2]
-    kSFree0 = 15,    // [2]
-    kPFull0 = 17,    // [2]
-    kPvDone0 = 19,   // [2]
-    kDrain = 21,
+    kKFull0 = 1,    // [2]
+    kKEmpty0 = 3,   // [2]
+    kVFull0 = 5,    // [2]
+    kVEmpty0 = 7,   // [2]
+    kSFull0 = 9,    // [2] per tile: S(j) in TMEM
+    kPFull0 = 11,   // [2] per tile: P(j) in TMEM (4 softmax warps arrive)
+    kODone0 = 13,   // [2] per tile: O += P(j) V(j) done
+    kDrain = 15,
 };
 
-// Tiles of a sequence with n new tokens (the decode path takes n <= qmax).
+// Tiles of a sequence with n new tokens (the decode path takes n <= qmax), and
+// the CTAs (pairs of tiles) they need.
 __device__ __forceinline__ int tiles_of(int n, int tq, int qmax) { return n > qmax ? (n + tq - 1) / tq : 0; }
+__device__ __forceinline__ int pairs_of(int n, int tq, int qmax) { return (tiles_of(n, tq, qmax) + 1) >> 1; }
 
 // Bounded wait by every lane of a warp; the result is made warp-uniform so that a
 // timeout can never leave some lanes at a warp-collective instruction alone.
@@ -99,10 +109,26 @@ __device__ __forceinline__ bool warp_wait(uint32_t addr, uint32_t parity, const 
 // Byte offset of 16-byte chunk c (0..7) of row r inside a 128-byte-swizzled half.
 __device__ __forceinline__ uint32_t sw128(int r, int c) { return r * 128 + ((c ^ (r & 7)) << 4); }
 
+__device__ __forceinline__ float max3(float a, float b, float c) {
+    float d;
+    asm("max.f32 %0, %1, %2, %3;\n" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+    return d;
+}
+
+// (a0, a1) * (b, b) + (c, c) on the packed f32x2 FMA.
+__device__ __forceinline__ void fma2(float& y0, float& y1, float a0, float a1, float b, float c) {
+    uint64_t a, bb, cc, y;
+    asm("mov.b64 %0, {%1, %2};\n" : "=l"(a) : "f"(a0), "f"(a1));
+    asm("mov.b64 %0, {%1, %1};\n" : "=l"(bb) : "f"(b));
+    asm("mov.b64 %0, {%1, %1};\n" : "=l"(cc) : "f"(c));
+    asm("fma.rn.f32x2 %0, %1, %2, %3;\n" : "=l"(y) : "l"(a), "l"(bb), "l"(cc));
+    asm("mov.b64 {%0, %1}, %2;\n" : "=f"(y0), "=f"(y1) : "l"(y));
+}
+
 template <int D>
 __global__ void __launch_bounds__(kThreads, 1)
     prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
-                      const __grid_constant__ CUtensorMap tm_v, const Args a, int tq_tokens, int tiles_bound) {
+                      const __grid_constant__ CUtensorMap tm_v, const Args a, int tq_tokens, int pairs_bound) {
     using S = Smem<D>;
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = smem_u32(smem_raw);
@@ -115,15 +141,17 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
-    const int tile = blockIdx.x % tiles_bound;
-    const int h = blockIdx.x / tiles_bound;
+    const int pair = blockIdx.x % pairs_bound;
+    const int h = blockIdx.x / pairs_bound;
 
-    // ---- which sequence owns this tile (prefix sum of per-sequence tile counts)
+    // ---- which sequence owns this pair (prefix sum of per-sequence pair counts)
     if (warp == 0) {
         int found_b = -1, found_t = 0, base_t = 0;
         for (int b0 = 0; b0 < a.num_seqs && found_b < 0; b0 += 32) {
             const int b = b0 + lane;
-            const int cnt = b < a.num_seqs ? tiles_of(a.query_start_loc[b + 1] - a.query_start_loc[b], tq_tokens, a.decode_max_q) : 0;
+            const int cnt =
+                b < a.num_seqs ? pairs_of(a.query_start_loc[b + 1] - a.query_start_loc[b], tq_tokens, a.decode_max_q)
+                               : 0;
             int inc = cnt;
 #pragma unroll
             for (int o = 1; o < 32; o <<= 1) {
@@ -131,11 +159,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (lane >= o) inc += v;
             }
             const int excl = base_t + inc - cnt;
-            const unsigned m = __ballot_sync(0xffffffffu, cnt > 0 && tile >= excl && tile < excl + cnt);
+            const unsigned m = __ballot_sync(0xffffffffu, cnt > 0 && pair >= excl && pair < excl + cnt);
             if (m) {
                 const int src = __ffs(m) - 1;
                 found_b = b0 + src;
-                found_t = tile - __shfl_sync(0xffffffffu, excl, src);
+                // the sequence's last pair first: its tiles see the most keys
+                found_t = __shfl_sync(0xffffffffu, excl + cnt - 1, src) - pair;
             }
             base_t += __shfl_sync(0xffffffffu, inc, 31);
         }
@@ -148,7 +177,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncthreads();
     const int b = s_info[0];
     if (b < 0) return;  // surplus CTA of the static grid (uniform for the block)
-    const int t_in_seq = s_info[1];
+    const int p_in_seq = s_info[1];
 
     const int q0 = a.query_start_loc[b];
     const int n = a.query_start_loc[b + 1] - q0;
@@ -163,21 +192,28 @@ __global__ void __launch_bounds__(kThreads, 1)
         L = cap;
     }
     const int G = a.group;
-    const int i0 = t_in_seq * tq_tokens;
-    const int ntok = min(tq_tokens, n - i0);
+    const int i0 = p_in_seq * 2 * tq_tokens;       // first new token of tile A
+    const int ntok_pair = min(2 * tq_tokens, n - i0);
     const int prefix = L - n;
     __nv_bfloat16* const out = reinterpret_cast<__nv_bfloat16*>(a.out);
     if (prefix < 0) {
         if (threadIdx.x == 0) flag_error(a.err, kDevQueryTooLong);
-        for (int i = threadIdx.x; i < ntok * G * D; i += blockDim.x) {
+        for (int i = threadIdx.x; i < ntok_pair * G * D; i += blockDim.x) {
             const int r = i / D;
             out[(static_cast<int64_t>(q0 + i0 + r / G) * a.num_q_heads + h * G + r % G) * D + i % D] =
                 __float2bfloat16(0.f);
         }
         return;
     }
-    const int kv_end = prefix + i0 + ntok;  // keys [0, kv_end) are visible to some row
-    const int ntiles = (kv_end + kKeys - 1) / kKeys;
+    // per tile x: new tokens, and KV tiles up to its last causal position
+    int ntok[2], nkv[2];
+#pragma unroll
+    for (int x = 0; x < 2; ++x) {
+        ntok[x] = max(0, min(tq_tokens, n - (i0 + x * tq_tokens)));
+        nkv[x] = ntok[x] > 0 ? (prefix + i0 + x * tq_tokens + ntok[x] + kKeys - 1) / kKeys : 0;
+    }
+    const int ntiles = max(nkv[0], nkv[1]);
+    const int kv_end = prefix + i0 + ntok_pair;          // keys [0, kv_end) are visible to some row
     const int last_page = (kv_end + kPage - 1) / kPage;  // pages [0, last_page) are read
     const int full_pages = L / kPage;                    // pages with no slot past L
 
@@ -192,11 +228,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             tc::mbar_init(bar(kVFull0 + i), 1);
             tc::mbar_init(bar(kVEmpty0 + i), 1);
         }
-        for (int i = 0; i < 2; ++i) {
-            tc::mbar_init(bar(kSFull0 + i), 1);
-            tc::mbar_init(bar(kSFree0 + i), 4);
-            tc::mbar_init(bar(kPFull0 + i), 4);
-            tc::mbar_init(bar(kPvDone0 + i), 1);
+        for (int x = 0; x < 2; ++x) {
+            tc::mbar_init(bar(kSFull0 + x), 1);
+            tc::mbar_init(bar(kPFull0 + x), 4);
+            tc::mbar_init(bar(kODone0 + x), 1);
         }
         tc::mbar_init(bar(kDrain), 1);
         tc::fence_mbar_init();
@@ -217,10 +252,13 @@ __global__ void __launch_bounds__(kThreads, 1)
             tc::prefetch_tmap(&tm_q);
             tc::prefetch_tmap(&tm_k);
             tc::prefetch_tmap(&tm_v);
-            tc::mbar_arrive_expect_tx(bar(kQFull), S::kHalves * 64 * 2 * G * tq_tokens);
+            const int nq = ntok[1] > 0 ? 2 : 1;
+            tc::mbar_arrive_expect_tx(bar(kQFull), nq * S::kHalves * 64 * 2 * G * tq_tokens);
+            for (int x = 0; x < nq; ++x)
 #pragma unroll
-            for (int hf = 0; hf < S::kHalves; ++hf)
-                tc::tma_load_3d(base + S::kQ + hf * kHalfBytes, &tm_q, bar(kQFull), hf * 64, h * G, q0 + i0);
+                for (int hf = 0; hf < S::kHalves; ++hf)
+                    tc::tma_load_3d(base + S::kQ0 + x * S::kTile + hf * kHalfBytes, &tm_q, bar(kQFull), hf * 64,
+                                    h * G, q0 + i0 + x * tq_tokens);
         }
         const int32_t* bt = a.block_table + static_cast<int64_t>(b) * a.max_pages;
         // lane l holds the block-table entry of page (group * 32 + l); the next
@@ -305,44 +343,56 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (lane == 0) {
             constexpr uint32_t kIdQK = tc::idesc_bf16_f32(kM, kKeys, false, false);
             constexpr uint32_t kIdPV = tc::idesc_bf16_f32(kM, D, false, true);
-            auto issue_pv = [&](int j) -> bool {
-                if (!tc::mbar_wait(bar(kPFull0 + (j & 1)), (j >> 1) & 1, s_abort, kTimeoutNs)) return false;
-                const int vst = j % kVStages;
-                if (!tc::mbar_wait(bar(kVFull0 + vst), (j / kVStages) & 1, s_abort, kTimeoutNs)) return false;
-                tc::tc_fence_after();
-                const int npj = min(kPagesPerTile, last_page - j * kPagesPerTile);
-                const uint32_t sv = base + S::kV0 + vst * S::kTile;
-                const uint32_t pa = tmem + ((j & 1) ? kTmemP1 : kTmemP0);
-                for (int ks = 0; ks < npj; ++ks) {  // one 16-key step per page; P: 8 columns per step
-                    const uint64_t bd = tc::desc_sw128(sv + ks * 2048, kHalfBytes, 1024);
-                    tc::mma_bf16_tmem_a(tmem + kTmemO, pa + ks * 8, bd, kIdPV, (j > 0 || ks > 0) ? 1u : 0u);
-                }
-                tc::mma_commit(bar(kPvDone0 + (j & 1)));
-                tc::mma_commit(bar(kVEmpty0 + vst));
-                return true;
-            };
-            ok = tc::mbar_wait(bar(kQFull), 0, s_abort, kTimeoutNs);
-            tc::tc_fence_after();
-            for (int kt = 0; kt < ntiles && ok; ++kt) {
-                const int sb = kt & 1;
-                const int kst = kt % kKStages;
-                ok = tc::mbar_wait(bar(kKFull0 + kst), (kt / kKStages) & 1, s_abort, kTimeoutNs);
-                if (ok && kt >= 2) ok = tc::mbar_wait(bar(kSFree0 + sb), ((kt >> 1) - 1) & 1, s_abort, kTimeoutNs);
-                if (!ok) break;
-                tc::tc_fence_after();
-                const uint32_t sk = base + S::kK0 + kst * S::kTile;
+            auto issue_s = [&](int x, int j) {  // S_x(j) = Q_x K(j)^T, K(j) already resident
+                const uint32_t sk = base + S::kK0 + (j % kKStages) * S::kTile;
+                const uint32_t sq = base + S::kQ0 + x * S::kTile;
 #pragma unroll
                 for (int ks = 0; ks < D / 16; ++ks) {
                     const uint32_t off = (ks >> 2) * kHalfBytes + (ks & 3) * 32;
-                    const uint64_t ad = tc::desc_sw128(base + S::kQ + off, 16, 1024);
-                    const uint64_t bd = tc::desc_sw128(sk + off, 16, 1024);
-                    tc::mma_bf16(tmem + (sb ? kTmemS1 : kTmemS0), ad, bd, kIdQK, ks > 0 ? 1u : 0u);
+                    tc::mma_bf16(tmem + tmem_s(x), tc::desc_sw128(sq + off, 16, 1024),
+                                 tc::desc_sw128(sk + off, 16, 1024), kIdQK, ks > 0 ? 1u : 0u);
                 }
-                tc::mma_commit(bar(kSFull0 + sb));
-                tc::mma_commit(bar(kKEmpty0 + kst));
-                if (kt >= 1) ok = issue_pv(kt - 1);
+                tc::mma_commit(bar(kSFull0 + x));
+            };
+            auto issue_pv = [&](int x, int j) -> bool {  // O_x += P_x(j) V(j), V(j) already resident
+                if (!tc::mbar_wait(bar(kPFull0 + x), j & 1, s_abort, kTimeoutNs)) return false;
+                tc::tc_fence_after();
+                const int npj = min(kPagesPerTile, last_page - j * kPagesPerTile);
+                const uint32_t sv = base + S::kV0 + (j % kVStages) * S::kTile;
+                for (int ks = 0; ks < npj; ++ks) {  // one 16-key step per page; P: 8 columns per step
+                    const uint64_t bd = tc::desc_sw128(sv + ks * 2048, kHalfBytes, 1024);
+                    tc::mma_bf16_tmem_a(tmem + tmem_o(x), tmem + tmem_s(x) + 64 + ks * 8, bd, kIdPV,
+                                        (j > 0 || ks > 0) ? 1u : 0u);
+                }
+                tc::mma_commit(bar(kODone0 + x));
+                return true;
+            };
+            ok = tc::mbar_wait(bar(kQFull), 0, s_abort, kTimeoutNs);
+            if (ok && ntiles > 0) ok = tc::mbar_wait(bar(kKFull0), 0, s_abort, kTimeoutNs);
+            if (ok && ntiles > 0) {
+                tc::tc_fence_after();
+                if (nkv[0] > 0) issue_s(0, 0);
+                if (nkv[1] > 0) issue_s(1, 0);
+                tc::mma_commit(bar(kKEmpty0));
             }
-            if (ok) ok = issue_pv(ntiles - 1);
+            for (int j = 0; j < ntiles && ok; ++j) {
+                const bool nxt0 = j + 1 < nkv[0], nxt1 = j + 1 < nkv[1];
+                ok = tc::mbar_wait(bar(kVFull0 + j % kVStages), (j / kVStages) & 1, s_abort, kTimeoutNs);
+                if (!ok) break;
+                tc::tc_fence_after();
+                if (j < nkv[0] && !(ok = issue_pv(0, j))) break;
+                if (nxt0 || nxt1) {
+                    const int js = j + 1;
+                    ok = tc::mbar_wait(bar(kKFull0 + js % kKStages), (js / kKStages) & 1, s_abort, kTimeoutNs);
+                    if (!ok) break;
+                    tc::tc_fence_after();
+                }
+                if (nxt0) issue_s(0, j + 1);
+                if (j < nkv[1] && !(ok = issue_pv(1, j))) break;
+                tc::mma_commit(bar(kVEmpty0 + j % kVStages));
+                if (nxt1) issue_s(1, j + 1);
+                if (nxt0 || nxt1) tc::mma_commit(bar(kKEmpty0 + (j + 1) % kKStages));
+            }
             if (!ok) {
                 *s_abort = 1;
                 flag_error(a.err, kDevWaitTimeout);
@@ -354,57 +404,56 @@ __global__ void __launch_bounds__(kThreads, 1)
         __syncwarp();
     } else {
         // ======================================================== softmax
-        const int quarter = warp & 3;
-        const int r = quarter * 32 + lane;  // row == TMEM lane
+        const int x = (warp - 2) >> 2;        // tile: warps 2-5 -> A, 6-9 -> B
+        const int quarter = warp & 3;         // TMEM lanes 32 * (warp % 4) ..
+        const int r = quarter * 32 + lane;    // row == TMEM lane
         const uint32_t lane_addr = tmem + (static_cast<uint32_t>(quarter * 32) << 16);
-        const bool valid = r < ntok * G;
-        const int pos = valid ? prefix + i0 + r / G : -1;  // causal limit of this row
+        const uint32_t s_addr = lane_addr + tmem_s(x);
+        const uint32_t o_addr = lane_addr + tmem_o(x);
+        const int nt = nkv[x];
+        const bool valid = r < ntok[x] * G;
+        const int pos = valid ? prefix + i0 + x * tq_tokens + r / G : -1;  // causal limit of this row
         const float c = a.scale_log2;
         float m_used = -INFINITY;  // running max, log2 units
-        float lsum[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};  // split to keep the adds independent
-        for (int kt = 0; kt < ntiles; ++kt) {
-            const int sb = kt & 1;
-            if (!warp_wait(bar(kSFull0 + sb), (kt >> 1) & 1, s_abort)) {
+        float lsum[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};  // independent partial sums
+        for (int kt = 0; kt < nt; ++kt) {
+            if (!warp_wait(bar(kSFull0 + x), kt & 1, s_abort)) {
                 ok = false;
                 break;
             }
             tc::tc_fence_after();
-            uint32_t sr[kKeys];
-#pragma unroll
-            for (int q = 0; q < kKeys / 32; ++q)
-                tc::tmem_ld32(lane_addr + (sb ? kTmemS1 : kTmemS0) + q * 32,
-                              *reinterpret_cast<uint32_t(*)[32]>(&sr[q * 32]));
-            tc::tc_fence_before();
-            __syncwarp();
-            if (lane == 0) tc::mbar_arrive(bar(kSFree0 + sb));
-
             const int j0 = kt * kKeys;
+            const bool diag = __any_sync(0xffffffffu, j0 + kKeys - 1 > pos);
+            uint32_t sh[64];
+            // masked running max of 64 keys starting at key k0 of the tile
+            auto half_max = [&](int k0, float (&mx8)[8]) {
+                if (diag) {
+#pragma unroll
+                    for (int j = 0; j < 64; ++j)
+                        if (j0 + k0 + j > pos) sh[j] = __float_as_uint(-INFINITY);
+                }
+#pragma unroll
+                for (int j = 0; j < 64; j += 16)
+#pragma unroll
+                    for (int e = 0; e < 8; ++e)
+                        mx8[e] = max3(mx8[e], __uint_as_float(sh[j + e]), __uint_as_float(sh[j + 8 + e]));
+            };
             float mx8[8];
 #pragma unroll
             for (int e = 0; e < 8; ++e) mx8[e] = -INFINITY;
-            const bool diag = __any_sync(0xffffffffu, j0 + kKeys - 1 > pos);
-            if (diag) {
-#pragma unroll
-                for (int j = 0; j < kKeys; ++j) {
-                    const float s = __uint_as_float(sr[j]);
-                    const float v = (j0 + j <= pos) ? s : -INFINITY;
-                    sr[j] = __float_as_uint(v);
-                    mx8[j & 7] = fmaxf(mx8[j & 7], v);
-                }
-            } else {
-#pragma unroll
-                for (int j = 0; j < kKeys; ++j) mx8[j & 7] = fmaxf(mx8[j & 7], __uint_as_float(sr[j]));
-            }
-            const float mx = fmaxf(fmaxf(fmaxf(mx8[0], mx8[1]), fmaxf(mx8[2], mx8[3])),
-                                   fmaxf(fmaxf(mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7])));
+            tc::tmem_ld64(s_addr, sh);
+            half_max(0, mx8);
+            tc::tmem_ld64(s_addr + 64, sh);  // keys 64-127 stay in registers
+            half_max(64, mx8);
+            const float mx = max3(max3(mx8[0], mx8[1], mx8[2]), max3(mx8[3], mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7]));
             const float mnew = mx * c;  // scale > 0, so the max commutes with it
             if (kt == 0) {
                 m_used = mnew;
             } else {
                 const bool need = mnew > m_used + 8.f;
                 if (__any_sync(0xffffffffu, need)) {
-                    // O is final for tiles < kt once P V(kt-1) is done
-                    if (!warp_wait(bar(kPvDone0 + ((kt - 1) & 1)), ((kt - 1) >> 1) & 1, s_abort)) {
+                    // O holds tiles < kt once P V(kt-1) is done
+                    if (!warp_wait(bar(kODone0 + x), (kt - 1) & 1, s_abort)) {
                         ok = false;
                         break;
                     }
@@ -413,53 +462,59 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                     for (int q = 0; q < D / 32; ++q) {
                         uint32_t o[32];
-                        tc::tmem_ld32(lane_addr + kTmemO + q * 32, o);
+                        tc::tmem_ld32(o_addr + q * 32, o);
 #pragma unroll
                         for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
-                        tc::tmem_st32(lane_addr + kTmemO + q * 32, o);
+                        tc::tmem_st32(o_addr + q * 32, o);
                     }
 #pragma unroll
                     for (int e = 0; e < 8; ++e) lsum[e] *= alpha;
                     if (need) m_used = mnew;
                 }
             }
-            const float mu = m_used == -INFINITY ? 0.f : m_used;
-            // P buffer sb is free once P V(kt-2) is done
-            if (kt >= 2 && !warp_wait(bar(kPvDone0 + sb), ((kt >> 1) - 1) & 1, s_abort)) {
-                ok = false;
-                break;
-            }
-            tc::tc_fence_after();
-            // P = 2^(s*c - m) as bf16 pairs; l sums the rounded values the MMA will use.
-            const uint32_t pcol = lane_addr + (sb ? kTmemP1 : kTmemP0);
-#pragma unroll
-            for (int hlf = 0; hlf < 2; ++hlf) {
+            const float nmu = m_used == -INFINITY ? 0.f : -m_used;
+            // P = 2^(s*c - m) as bf16 pairs into the last 64 columns of S: keys
+            // 64-127 (in registers) to columns 96-127, then keys 0-63 (loaded
+            // again) to columns 64-95; every column written has been read.  The
+            // P V that read the previous P finished before this S was written.
+            // l sums the fp32 values.
+            auto half_p = [&](uint32_t col) {
                 uint32_t pk[32];
 #pragma unroll
                 for (int e = 0; e < 32; ++e) {
-                    const int j = hlf * 64 + 2 * e;
-                    const float x0 = fast_exp2(fmaf(__uint_as_float(sr[j]), c, -mu));
-                    const float x1 = fast_exp2(fmaf(__uint_as_float(sr[j + 1]), c, -mu));
+                    float y0, y1;
+                    fma2(y0, y1, __uint_as_float(sh[2 * e]), __uint_as_float(sh[2 * e + 1]), c, nmu);
+                    const float x0 = fast_exp2(y0), x1 = fast_exp2(y1);
                     pk[e] = pack_bf16(x0, x1);
-                    lsum[e & 7] += bf16_lo(pk[e]) + bf16_hi(pk[e]);
+                    lsum[e & 7] += x0 + x1;
                 }
-                tc::tmem_st32(pcol + hlf * 32, pk);
+                tc::tmem_st32(s_addr + col, pk);
+            };
+            half_p(96);
+            tc::tmem_ld64(s_addr, sh);
+            if (diag) {
+#pragma unroll
+                for (int j = 0; j < 64; ++j)
+                    if (j0 + j > pos) sh[j] = __float_as_uint(-INFINITY);
             }
+            half_p(64);
             tc::tc_fence_before();
             __syncwarp();
-            if (lane == 0) tc::mbar_arrive(bar(kPFull0 + sb));
+            if (lane == 0) tc::mbar_arrive(bar(kPFull0 + x));
         }
-        if (ok) ok = warp_wait(bar(kPvDone0 + ((ntiles - 1) & 1)), ((ntiles - 1) >> 1) & 1, s_abort);
-        if (ok) {
+        if (ok && nt > 0) ok = warp_wait(bar(kODone0 + x), (nt - 1) & 1, s_abort);
+        if (ok && nt > 0) {
             tc::tc_fence_after();
             const float l = ((lsum[0] + lsum[1]) + (lsum[2] + lsum[3])) + ((lsum[4] + lsum[5]) + (lsum[6] + lsum[7]));
             const float inv = valid ? 1.f / l : 0.f;
-            __nv_bfloat16* orow =
-                out + (static_cast<int64_t>(q0 + i0 + (valid ? r / G : 0)) * a.num_q_heads + h * G + r % G) * D;
+            __nv_bfloat16* orow = out + (static_cast<int64_t>(q0 + i0 + x * tq_tokens + (valid ? r / G : 0)) *
+                                             a.num_q_heads +
+                                         h * G + r % G) *
+                                            D;
 #pragma unroll
             for (int q = 0; q < D / 32; ++q) {
                 uint32_t o[32];
-                tc::tmem_ld32(lane_addr + kTmemO + q * 32, o);
+                tc::tmem_ld32(o_addr + q * 32, o);
                 if (valid) {
 #pragma unroll
                     for (int e = 0; e < 32; e += 8) {
@@ -472,7 +527,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     }
                 }
             }
-        } else if (lane == 0) {
+        } else if (!ok && lane == 0) {
             *s_abort = 1;
             flag_error(a.err, kDevWaitTimeout);
         }
@@ -490,10 +545,12 @@ __global__ void __launch_bounds__(kThreads, 1)
 // --------------------------------------------------------------- host side
 int tokens_per_tile(int group) { return group <= kM ? kM / group : 0; }
 
-int tiles_bound(const Args& a) {
+// Upper bound on the pairs of tiles of any batch with these shapes: sum over
+// sequences of ceil(ceil(n_b / TQ) / 2) <= T / (2 TQ) + B.
+int pairs_bound(const Args& a) {
     const int tq = tokens_per_tile(a.group);
     if (tq == 0) return 0;
-    return static_cast<int>((a.num_tokens + tq - 1) / tq + a.num_seqs);
+    return static_cast<int>(a.num_tokens / (2 * tq) + a.num_seqs);
 }
 
 template <int D>
@@ -517,7 +574,7 @@ cudaError_t launch_d(const Args& a, cudaStream_t stream) {
         !encode_cache_map(&tv_map, a.v_cache, D, a.num_kv_heads, a.num_blocks))
         return cudaErrorInvalidValue;
     prefill_tc_kernel<D><<<static_cast<unsigned>(ctas), kThreads, S::kAlloc, stream>>>(tq_map, tk_map, tv_map, a, tq,
-                                                                                       tiles_bound(a));
+                                                                                       pairs_bound(a));
     return cudaGetLastError();
 }
 
@@ -525,7 +582,7 @@ cudaError_t launch_d(const Args& a, cudaStream_t stream) {
 
 int64_t prefill_ctas(const Args& a) {
     if (a.num_tokens < 2) return 0;
-    return static_cast<int64_t>(tiles_bound(a)) * a.num_kv_heads;
+    return static_cast<int64_t>(pairs_bound(a)) * a.num_kv_heads;
 }
 
 cudaError_t launch_prefill(const Args& a, cudaStream_t stream) {

@@ -6,7 +6,8 @@ distilled into a small decision tree keyed on GPU, sequence length and batch.
 This is that step for GB300: for every (context bound, batch size) cell of a
 grid it times pa_forward on Llama-3.1-8B-shaped decode batches (32 query heads,
 8 KV heads, head_dim 128, every sequence at the context bound) for a set of
-split sizes, and keeps the fastest.  The result is written as a table that the
+(split size, decode kernel variant) pairs -- a variant is the warps per CTA
+and the pipeline depth per warp -- and keeps the fastest.  The result is written as a table that the
 library compiles in; nothing is tuned at run time.
 
     python -m paged_kv_cache_forward_gb300.sweep [--out csrc/lut_gb300.inc] [--log profiles/...md]
@@ -37,29 +38,45 @@ HQ, HKV, D, PAGE = 32, 8, 128, 16
 MAX_KV_BYTES = 6 << 30
 
 
-def candidates(bound: int, batch: int, sms: int):
+SMEM_PER_SM = 228 << 10
+REGS_PER_SM = 65536
+REGS_PER_THREAD = 168
+VARIANTS = "4x2,4x3,4x4,8x2,8x3,12x2"  # warps x stages
+
+
+def resident_ctas(warps: int, stages: int) -> int:
+    """Decode CTAs an SM holds: shared memory (K and V of one page per stage per
+    warp, 1 KiB reserved per CTA) and registers (at most 168 per thread)."""
+    per_cta = warps * stages * 2 * PAGE * D * 2 + 1024
+    return max(1, min(SMEM_PER_SM // per_cta, REGS_PER_SM // (warps * 32 * REGS_PER_THREAD)))
+
+
+def candidates(bound: int, batch: int, sms: int, warps: int, stages: int):
     base = {64, 128, 256, 512, 1024, 2048, 4096, 8192, 16384}
-    # split sizes that give whole waves of CTAs at 2 or 3 resident CTAs per SM
-    for per_sm in (2, 3):
-        for k in (1, 2, 3):
-            pages = math.ceil(bound * batch * HKV / (k * per_sm * sms) / PAGE)
-            base.add(max(1, pages) * PAGE)
+    # split sizes that give whole waves of CTAs at this variant's residency
+    per_sm = resident_ctas(warps, stages)
+    for k in (1, 2, 3):
+        pages = math.ceil(bound * batch * HKV / (k * per_sm * sms) / PAGE)
+        base.add(max(1, pages) * PAGE)
     return sorted(c for c in base if 16 <= c <= bound)
 
 
-def time_shape(bound, batch, chunk, pools, stream, steps_per_graph=16, reps=30):
+def time_shape(bound, batch, chunk, pools, stream, warps=0, stages=0, steps_per_graph=16, reps=30):
     q, ks, vs, bt, sl, qsl, out = pools
     R = len(ks)
-    pa.prepare(q, ks[0], bt, sl, kv_chunk=chunk, stream=stream)
+    pa.prepare(q, ks[0], bt, sl, kv_chunk=chunk, stream=stream, decode_stages=stages,
+               decode_warps=warps)
     with torch.cuda.stream(stream):
         for i in range(2):
-            pa.forward(q, ks[i % R], vs[i % R], bt, sl, qsl, out, kv_chunk=chunk, stream=stream)
+            pa.forward(q, ks[i % R], vs[i % R], bt, sl, qsl, out, kv_chunk=chunk, stream=stream,
+                       decode_stages=stages, decode_warps=warps)
     stream.synchronize()
     M = max(R, (steps_per_graph // R) * R)
     g = torch.cuda.CUDAGraph()
     with torch.cuda.graph(g, stream=stream):
         for i in range(M):
-            pa.forward(q, ks[i % R], vs[i % R], bt, sl, qsl, out, kv_chunk=chunk, stream=stream)
+            pa.forward(q, ks[i % R], vs[i % R], bt, sl, qsl, out, kv_chunk=chunk, stream=stream,
+                       decode_stages=stages, decode_warps=warps)
     for _ in range(3):
         g.replay()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
@@ -72,7 +89,7 @@ def time_shape(bound, batch, chunk, pools, stream, steps_per_graph=16, reps=30):
     code = pa.device_error(stream)
     if code:
         raise RuntimeError(f"device error {code} ({pa.DEVICE_ERRORS.get(code)}) at bound {bound}, batch {batch}, "
-                           f"split {chunk}")
+                           f"split {chunk}, variant {warps}x{stages}")
     return e0.elapsed_time(e1) * 1e3 / (reps * M)  # us per step
 
 
@@ -98,12 +115,15 @@ def make_pools(bound, batch, l2_bytes, gen):
 def main(argv=None):
     ap = argparse.ArgumentParser()
     ap.add_argument("--out", default=os.path.join(HERE, "csrc", "lut_gb300.inc"))
+    ap.add_argument("--no-write", action="store_true", help="print the results only")
     ap.add_argument("--log", default=os.path.join(os.path.dirname(HERE), "profiles", "split_table_sweep__gb300.md"))
     ap.add_argument("--bounds", default=",".join(map(str, BOUNDS)))
     ap.add_argument("--batches", default=",".join(map(str, BATCHES)))
+    ap.add_argument("--variants", default=VARIANTS, help="decode variants to try: warps x stages")
     args = ap.parse_args(argv)
     bounds = [int(x) for x in args.bounds.split(",")]
     batches = [int(x) for x in args.batches.split(",")]
+    variants = [tuple(int(y) for y in v.split("x")) for v in args.variants.split(",")]
 
     from paged_kv_cache_forward_gb300 import build
     build.build()
@@ -121,18 +141,20 @@ def main(argv=None):
                 continue
             pools, kv = make_pools(bound, batch, l2, gen)
             res = []
-            for chunk in candidates(bound, batch, sms):
-                try:
-                    us = time_shape(bound, batch, chunk, pools, stream)
-                except RuntimeError as e:  # reported, and the candidate is not used
-                    print(f"skipped: {e}", flush=True)
-                    continue
-                res.append((us, chunk))
+            for w, st in variants:
+                for chunk in candidates(bound, batch, sms, w, st):
+                    try:
+                        us = time_shape(bound, batch, chunk, pools, stream, warps=w, stages=st)
+                    except RuntimeError as e:  # reported, and the candidate is not used
+                        print(f"skipped: {e}", flush=True)
+                        continue
+                    res.append((us, chunk, st, w))
             res.sort()
-            us, chunk = res[0]
-            best[(bound, batch)] = chunk
-            row = " ".join(f"{c}:{kv / u / 1e3:.0f}" for u, c in sorted(res, key=lambda x: x[1]))
-            lines.append(f"| {batch} | {bound} | {chunk} | {us:.1f} | {kv / us / 1e3:.0f} | {row} |")
+            us, chunk, st, w = res[0]
+            best[(bound, batch)] = (chunk, st, w)
+            row = " ".join(f"{c}/{ww}x{t}:{kv / u / 1e3:.0f}"
+                           for u, c, t, ww in sorted(res, key=lambda x: (x[3], x[2], x[1])))
+            lines.append(f"| {batch} | {bound} | {chunk} | {w}x{st} | {us:.1f} | {kv / us / 1e3:.0f} | {row} |")
             print(lines[-1], flush=True)
             del pools
             torch.cuda.empty_cache()
@@ -143,30 +165,36 @@ def main(argv=None):
     for batch in batches:
         for bound in bounds:
             if (bound, batch) in best:
-                entries.append((bound, batch, best[(bound, batch)]))
-    last_batch = max(b for _, b, _ in entries)
-    fallback = max(entries, key=lambda e: (e[1], e[0]))[2]
+                entries.append((bound, batch) + best[(bound, batch)])
+    last_batch = max(e[1] for e in entries)
+    fallback = max(entries, key=lambda e: (e[1], e[0]))[2:]
     stamp = datetime.date.today().isoformat()
-    with open(args.out, "w") as f:
-        f.write("// Keys per split for the decode kernel, keyed on the context bound\n"
-                "// (max_pages * page_size) and the number of sequences.  First entry that\n"
-                "// matches wins; the last entry is the fallback.  Written by\n"
-                f"// paged_kv_cache_forward_gb300/sweep.py on {props.name} ({stamp}).\n"
-                "static const LutEntry kSplitTable[] = {\n")
-        for bound, batch, chunk in entries:
-            mb = (1 << 30) if batch == last_batch else batch
-            f.write(f"    {{{bound}, {mb}, {chunk}}},\n")
-        f.write(f"    {{1 << 30, 1 << 30, {fallback}}},\n}};\n")
+    if not args.no_write:
+        write_table(args.out, entries, last_batch, fallback, props.name, stamp)
     with open(args.log, "w") as f:
         f.write(f"# Split-size sweep on {props.name} ({stamp})\n\n"
-                "Command: `python -m paged_kv_cache_forward_gb300.sweep`\n\n"
+                f"Command: `python -m paged_kv_cache_forward_gb300.sweep {' '.join(argv or sys.argv[1:])}`\n\n"
                 "Llama-3.1-8B-shaped decode (Hq 32, Hkv 8, D 128), every sequence at the bound,\n"
                 "graph-replayed pa_forward steps rotating over KV pool copies larger than 3 x L2.\n"
                 "GB/s = KV bytes per step / step time.\n\n"
-                "| batch | bound | best split | us/step | GB/s | split:GB/s for every candidate |\n"
-                "|---|---|---|---|---|---|\n")
+                "| batch | bound | best split | warps x stages | us/step | GB/s | split/variant:GB/s for every candidate |\n"
+                "|---|---|---|---|---|---|---|\n")
         f.write("\n".join(lines) + "\n")
-    print(f"wrote {args.out} and {args.log}")
+    print(f"wrote {args.log}" + ("" if args.no_write else f" and {args.out}"))
+
+
+def write_table(path, entries, last_batch, fallback, gpu_name, stamp):
+    with open(path, "w") as f:
+        f.write("// Keys per split and decode kernel variant, keyed on the context bound\n"
+                "// (max_pages * page_size) and the number of sequences:\n"
+                "// {max_bound, max_seqs, kv_chunk, decode_stages, decode_warps}.  The first\n"
+                "// entry that matches wins; the last entry is the fallback.  Written by\n"
+                f"// paged_kv_cache_forward_gb300/sweep.py on {gpu_name} ({stamp}).\n"
+                "static const LutEntry kSplitTable[] = {\n")
+        for bound, batch, chunk, st, w in entries:
+            mb = (1 << 30) if batch == last_batch else batch
+            f.write(f"    {{{bound}, {mb}, {chunk}, {st}, {w}}},\n")
+        f.write(f"    {{1 << 30, 1 << 30, {fallback[0]}, {fallback[1]}, {fallback[2]}}},\n}};\n")
 
 
 if __name__ == "__main__":

@@ -38,7 +38,7 @@ def test_every_declared_symbol_is_exported(lib):
 def test_status_strings(lib):
     for st in range(5):
         assert lib.pa_status_string(st)
-    assert lib.pa_version() == 100
+    assert lib.pa_version() == 101
 
 
 def llama_dims(**kw):
@@ -86,6 +86,24 @@ def test_plan_rejects(lib, kw, status):
         B.plan(llama_dims(**kw))
     assert e.value.status == status
     assert lib.pa_last_error().decode()
+
+
+DECODE_VARIANTS = [(4, 2), (4, 3), (4, 4), (8, 2), (8, 3), (12, 2)]  # (warps, stages)
+
+
+def test_decode_variant_option(lib):
+    p = B.plan(llama_dims())
+    assert (p["decode_warps"], p["decode_stages"]) in DECODE_VARIANTS
+    for w, st in DECODE_VARIANTS:
+        p = B.plan(llama_dims(), decode_stages=st, decode_warps=w)
+        assert (p["decode_warps"], p["decode_stages"]) == (w, st)
+    # one field alone: the other takes its default (4 warps / 2 stages)
+    assert B.plan(llama_dims(), decode_stages=3)["decode_warps"] == 4
+    assert B.plan(llama_dims(), decode_warps=8)["decode_stages"] == 2
+    for w, st in [(4, 1), (4, 5), (8, 4), (12, 3), (16, 2), (2, 2), (-4, 2)]:
+        with pytest.raises(B.PagedAttnError) as e:
+            B.plan(llama_dims(), decode_stages=st, decode_warps=w)
+        assert e.value.status == B.PA_ERR_INVALID_ARG
 
 
 def test_bad_chunk_rejected(lib):

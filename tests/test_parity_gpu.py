@@ -109,6 +109,21 @@ def test_split_invariance(chunk):
     assert mx <= 2 * 2 ** -8 * 4, mx  # a few bf16 ulps of |out| <= ~4
 
 
+@pytest.mark.parametrize("warps,stages", [(4, 2), (4, 3), (4, 4), (8, 2), (8, 3), (12, 2)])
+@pytest.mark.parametrize("D", [64, 128])
+def test_decode_variants(warps, stages, D):
+    """Every decode variant (warps per CTA, pipeline depth) against the oracle;
+    the depth does not change which warp reads which page, so variants with the
+    same warp count are bit-identical.  Multi-token rows and a split merge included."""
+    b = W.make_batch([1, 1, 3, 1, 2], [4000, 1, 777, 65, 2500], 32, 8, D, seed=31 + D, max_pages=256)
+    ref = oracle.batch_attention(b)
+    for chunk in (0, 256):
+        got = run(b, kv_chunk=chunk, decode_stages=stages, decode_warps=warps)
+        assert_close(got, ref, f"{warps}x{stages} D {D} chunk {chunk}")
+        base = run(b, kv_chunk=chunk, decode_stages=2, decode_warps=warps)
+        assert torch.equal(got.view(torch.int16), base.view(torch.int16)), (warps, stages, chunk)
+
+
 # ------------------------------------------------------------------- edge cases
 
 def test_edge_lengths():
