@@ -104,7 +104,12 @@ typedef struct {
                                others are PA_ERR_INVALID_ARG.  Deeper pipelines
                                and more warps keep more bytes in flight per CTA
                                but fit fewer CTAs on an SM. */
-    int32_t reserved;       /* 0 */
+    int32_t decode_cluster; /* 0: from the tuned table (unless kv_chunk is set);
+                               1: splits of kv_chunk keys merged through the
+                               workspace; 2..16: the keys of each (sequence, KV
+                               head) are split evenly over a thread-block cluster
+                               of this many CTAs, merged in distributed shared
+                               memory (kv_chunk must then be 0). */
     /* cudaEvent_t handles recorded on the stream immediately before and after
        the decode kernel and the prefill kernel (NULL: not recorded). */
     void* decode_start_event;
@@ -125,7 +130,7 @@ typedef struct {
     int32_t launches;         /* kernels launched per pa_forward               */
     int32_t decode_stages;    /* decode pipeline depth (pages per warp)        */
     int32_t decode_warps;     /* warps per decode CTA                          */
-    int32_t reserved;
+    int32_t decode_cluster;   /* 1, or the CTAs per cluster (= splits)         */
 } pa_plan_info;
 
 /*

@@ -62,7 +62,7 @@ class Options(ctypes.Structure):
         ("kv_chunk", ctypes.c_int32),
         ("decode_stages", ctypes.c_int32),
         ("decode_warps", ctypes.c_int32),
-        ("reserved", ctypes.c_int32),
+        ("decode_cluster", ctypes.c_int32),
         ("decode_start_event", ctypes.c_void_p),
         ("decode_stop_event", ctypes.c_void_p),
         ("prefill_start_event", ctypes.c_void_p),
@@ -92,11 +92,11 @@ class PlanInfo(ctypes.Structure):
         ("launches", ctypes.c_int32),
         ("decode_stages", ctypes.c_int32),
         ("decode_warps", ctypes.c_int32),
-        ("reserved", ctypes.c_int32),
+        ("decode_cluster", ctypes.c_int32),
     ]
 
     def as_dict(self):
-        return {n: getattr(self, n) for n, _ in self._fields_ if n != "reserved"}
+        return {n: getattr(self, n) for n, _ in self._fields_}
 
 
 _lib = None
@@ -181,11 +181,13 @@ def _check_tensors(q, k_cache, v_cache, block_table, seq_lens, query_start_loc, 
         raise ValueError("seq_lens [B], query_start_loc [B+1] and block_table [B, max_pages] disagree on B")
 
 
-def options(kv_chunk: int = 0, events=None, decode_stages: int = 0, decode_warps: int = 0) -> Options:
+def options(kv_chunk: int = 0, events=None, decode_stages: int = 0, decode_warps: int = 0,
+            decode_cluster: int = 0) -> Options:
     o = Options()
     o.kv_chunk = kv_chunk
     o.decode_stages = decode_stages
     o.decode_warps = decode_warps
+    o.decode_cluster = decode_cluster
     if events:
         for key in ("decode_start_event", "decode_stop_event", "prefill_start_event", "prefill_stop_event"):
             ev = events.get(key)
@@ -197,7 +199,7 @@ def options(kv_chunk: int = 0, events=None, decode_stages: int = 0, decode_warps
 
 def forward(q, k_cache, v_cache, block_table, seq_lens, query_start_loc, out=None,
             scale: Optional[float] = None, kv_chunk: int = 0, events=None, stream=None,
-            decode_stages: int = 0, decode_warps: int = 0) -> torch.Tensor:
+            decode_stages: int = 0, decode_warps: int = 0, decode_cluster: int = 0) -> torch.Tensor:
     """Paged attention forward (pa_forward).  Returns ``out`` ([T, Hq, D] bf16).
 
     ``events`` (optional) maps decode_start_event / decode_stop_event /
@@ -214,8 +216,8 @@ def forward(q, k_cache, v_cache, block_table, seq_lens, query_start_loc, out=Non
     s = _stream_handle(stream)
     args = (_ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(block_table), _ptr(seq_lens), _ptr(query_start_loc),
             _ptr(out), ctypes.c_float(scale), ctypes.byref(dims))
-    if kv_chunk or events or decode_stages or decode_warps:
-        opts = options(kv_chunk, events, decode_stages, decode_warps)
+    if kv_chunk or events or decode_stages or decode_warps or decode_cluster:
+        opts = options(kv_chunk, events, decode_stages, decode_warps, decode_cluster)
         _check(lib.pa_forward_ex(*args, ctypes.byref(opts), s))
     else:
         _check(lib.pa_forward(*args, s))
@@ -264,24 +266,25 @@ def cache_write(k_new, v_new, slot_mapping, k_cache, v_cache, stream=None):
                                  ctypes.byref(dims), _stream_handle(stream)))
 
 
-def plan(dims: Dims, kv_chunk: int = 0, decode_stages: int = 0, decode_warps: int = 0) -> dict:
+def plan(dims: Dims, kv_chunk: int = 0, decode_stages: int = 0, decode_warps: int = 0,
+         decode_cluster: int = 0) -> dict:
     info = PlanInfo()
-    opts = options(kv_chunk, decode_stages=decode_stages, decode_warps=decode_warps)
+    opts = options(kv_chunk, decode_stages=decode_stages, decode_warps=decode_warps, decode_cluster=decode_cluster)
     _check(load().pa_plan(ctypes.byref(dims), ctypes.byref(opts), ctypes.byref(info)))
     return info.as_dict()
 
 
 def plan_for(q, k_cache, block_table, seq_lens, kv_chunk: int = 0, decode_stages: int = 0,
-             decode_warps: int = 0) -> dict:
+             decode_warps: int = 0, decode_cluster: int = 0) -> dict:
     return plan(make_dims(q.shape, k_cache.shape, block_table.shape, seq_lens.shape[0]), kv_chunk, decode_stages,
-                decode_warps)
+                decode_warps, decode_cluster)
 
 
 def prepare(q, k_cache, block_table, seq_lens, kv_chunk: int = 0, stream=None, decode_stages: int = 0,
-            decode_warps: int = 0):
+            decode_warps: int = 0, decode_cluster: int = 0):
     """Allocates the workspace for these shapes on the stream (call before capture)."""
     dims = make_dims(q.shape, k_cache.shape, block_table.shape, seq_lens.shape[0])
-    opts = options(kv_chunk, decode_stages=decode_stages, decode_warps=decode_warps)
+    opts = options(kv_chunk, decode_stages=decode_stages, decode_warps=decode_warps, decode_cluster=decode_cluster)
     _check(load().pa_prepare(ctypes.byref(dims), ctypes.byref(opts), _stream_handle(stream)))
 
 

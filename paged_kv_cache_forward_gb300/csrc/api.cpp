@@ -39,10 +39,12 @@ struct LutEntry {
     int32_t kv_chunk;
     int32_t decode_stages;  // 0: the default depth
     int32_t decode_warps;   // 0: the default warps per CTA
+    int32_t decode_cluster; // 0 or 1: splits merge through the workspace; else cluster size (= splits)
 };
 #include "lut_gb300.inc"
 
 constexpr int32_t kDefaultDecodeStages = 2, kDefaultDecodeWarps = 4;
+constexpr int32_t kMaxDecodeCluster = 16;  // largest thread-block cluster (non-portable size)
 
 const LutEntry& table_entry(int64_t bound, int32_t num_seqs) {
     for (const LutEntry& e : kSplitTable)
@@ -106,6 +108,18 @@ pa_status make_plan(const pa_dims* d, const pa_options* o, Plan* p) {
         return fail(PA_ERR_INVALID_ARG,
                     "decode variant (%d warps, %d stages) is not one of (4, 2..4), (8, 2..3), (12, 2)", warps,
                     stages);
+    // cluster mode: the table's, unless the caller forces a split size or a cluster
+    int32_t cluster = te.decode_cluster > 1 ? te.decode_cluster : 1;
+    if (o && (o->kv_chunk || o->decode_cluster)) cluster = o->decode_cluster > 1 ? o->decode_cluster : 1;
+    if (o && o->kv_chunk && o->decode_cluster > 1)
+        return fail(PA_ERR_INVALID_ARG, "kv_chunk and decode_cluster > 1 are exclusive (a cluster splits evenly)");
+    if (o && (o->decode_cluster < 0 || o->decode_cluster > kMaxDecodeCluster))
+        return fail(PA_ERR_INVALID_ARG, "decode_cluster %d is not in 0..%d", o->decode_cluster, kMaxDecodeCluster);
+    if (cluster > 1) {
+        // even split of the longest possible sequence over `cluster` CTAs
+        const int64_t pages = (bound + d->page_size - 1) / d->page_size;
+        chunk = (pages + cluster - 1) / cluster * d->page_size;
+    }
     if (chunk > bound) chunk = bound;
     const int32_t group = d->num_q_heads / d->num_kv_heads;
     pa::Args& a = p->args;
@@ -119,7 +133,8 @@ pa_status make_plan(const pa_dims* d, const pa_options* o, Plan* p) {
     a.page_size = d->page_size;
     a.max_pages = d->max_pages;
     a.kv_chunk = static_cast<int32_t>(chunk);
-    a.splits = static_cast<int32_t>((bound + chunk - 1) / chunk);
+    a.splits = cluster > 1 ? cluster : static_cast<int32_t>((bound + chunk - 1) / chunk);
+    a.decode_cluster = cluster;
     a.row_groups = (group + 15) / 16;
     a.decode_max_q = pa::decode_max_q(group);
     a.decode_stages = stages;
@@ -137,10 +152,10 @@ pa_status make_plan(const pa_dims* d, const pa_options* o, Plan* p) {
     if (p->decode_ctas > kMaxCtas || p->prefill_ctas > kMaxCtas)
         return fail(PA_ERR_UNSUPPORTED, "launch grid above 2^31-1 CTAs; use a larger kv_chunk");
     p->launches = (p->decode_ctas > 0) + (p->prefill_ctas > 0);
-    p->counter_bytes = pa::counter_bytes_needed(d->num_seqs, d->num_kv_heads, a.row_groups, a.splits);
-    p->ws_bytes = pa::workspace_layout(d->num_seqs, d->num_q_heads, a.splits, d->head_dim, a.decode_max_q,
-                                       p->counter_bytes)
-                      .bytes;
+    const int32_t wss = pa::ws_splits(a.splits, a.decode_cluster);
+    p->counter_bytes = pa::counter_bytes_needed(d->num_seqs, d->num_kv_heads, a.row_groups, wss);
+    p->ws_bytes =
+        pa::workspace_layout(d->num_seqs, d->num_q_heads, wss, d->head_dim, a.decode_max_q, p->counter_bytes).bytes;
     return PA_OK;
 }
 
@@ -252,6 +267,7 @@ pa_status pa_plan(const pa_dims* dims, const pa_options* opts, pa_plan_info* inf
     info->launches = p.launches;
     info->decode_stages = p.args.decode_stages;
     info->decode_warps = p.args.decode_warps;
+    info->decode_cluster = p.args.decode_cluster;
     return PA_OK;
 }
 
@@ -299,7 +315,8 @@ pa_status pa_forward_ex(const void* q, const void* k_cache, const void* v_cache,
     a.out = out;
     a.err = static_cast<int32_t*>(ws);
     const pa::WorkspaceLayout wl =
-        pa::workspace_layout(a.num_seqs, a.num_q_heads, a.splits, a.head_dim, a.decode_max_q, counter_area);
+        pa::workspace_layout(a.num_seqs, a.num_q_heads, pa::ws_splits(a.splits, a.decode_cluster), a.head_dim,
+                             a.decode_max_q, counter_area);
     a.counters = reinterpret_cast<int32_t*>(static_cast<char*>(ws) + wl.counters_off);
     a.ws_o = reinterpret_cast<float*>(static_cast<char*>(ws) + wl.o_off);
     a.ws_ml = reinterpret_cast<float*>(static_cast<char*>(ws) + wl.ml_off);

@@ -45,6 +45,7 @@ namespace {
 // CTA (few splits, so a short merge); large batches want small CTAs.
 constexpr int kPage = 16;
 constexpr int kRows = 16;  // MMA M: query-head rows per CTA
+constexpr int kMaxCluster = 16;  // CTAs of one (sequence, KV head, row group) in cluster mode
 
 template <int D, int kWarps, int kStages>
 struct DecodeTile {
@@ -54,9 +55,13 @@ struct DecodeTile {
     static constexpr int kStageBytes = 2 * kPageBytes;          // K then V
     static constexpr int kWarpBytes = kStages * kStageBytes;
     static constexpr int kPipeBytes = kWarps * kWarpBytes;
-    // merge area: per warp O[16][D] fp32 + m[16] + l[16]
-    static constexpr int kMergeWarpFloats = kRows * D + 2 * kRows;
-    static constexpr int kMergeBytes = kWarps * kMergeWarpFloats * 4;
+    // merge area: per warp O[16][D + 8] fp32 (the padding makes the fragment
+    // stores bank-conflict free) + m[16] + l[16]; then the CTA's merged partial
+    // O[16][D] + m[16] + l[16] (read by the other CTAs of a cluster)
+    static constexpr int kMS = D + 8;  // row stride of a warp's O
+    static constexpr int kMergeWarpFloats = kRows * kMS + 2 * kRows;
+    static constexpr int kCtaPartialOffFloats = kWarps * kMergeWarpFloats;
+    static constexpr int kMergeBytes = (kWarps * kMergeWarpFloats + kRows * D + 2 * kRows) * 4;
     static constexpr int kSmemBytes = kPipeBytes > kMergeBytes ? kPipeBytes : kMergeBytes;
 };
 
@@ -76,69 +81,58 @@ __device__ __forceinline__ int64_t partial_row(const Args& a, int b, int s, int 
 // Softmax"): M = max_s m_s, w_s = 2^(m_s - M), out = sum_s w_s O_s / sum_s w_s l_s.
 // A split that saw no visible key of a row has m_s = -inf and weight 0.  The
 // partials were written by other CTAs, so they are read with L2-coherent loads.
-template <int D>
+// One thread per (row, 4 columns) loads the (m, l) and O of kBatch splits at
+// a time (8, or 16 for 8-warp CTAs, which have the registers), so a merge
+// of that many splits takes one round trip to L2.
+template <int D, int kBatch>
 __device__ __forceinline__ void merge_splits(const Args& a, int b, const int* tok, const int* head, int rows,
-                                             int nsplits, int q0, float* sm) {
-    const int warp = threadIdx.x >> 5;
-    const int lane = threadIdx.x & 31;
-    float* s_m = sm;         // per-row max
-    float* s_inv = sm + kRows;  // per-row 1 / denominator
-    const int64_t split_rows = static_cast<int64_t>(a.decode_max_q) * a.num_q_heads;
-    const int64_t split_ml = split_rows * 2;  // stride between splits in ws_ml
-    const int64_t split_o = split_rows * D;   // ... and in ws_o
-    const int nwarps = blockDim.x >> 5;
-    for (int r = warp; r < rows; r += nwarps) {
-        const float* ml = a.ws_ml + partial_row(a, b, 0, tok[r], head[r]) * 2;
-        float M = -INFINITY;
-        for (int s = lane; s < nsplits; s += 32) M = fmaxf(M, __ldcg(ml + s * split_ml));
-        M = warp_max(M);
-        float den = 0.f;
-        for (int s = lane; s < nsplits; s += 32)
-            den += fast_exp2(__ldcg(ml + s * split_ml) - M) * __ldcg(ml + s * split_ml + 1);
-        den = warp_sum(den);
-        if (lane == 0) {
-            s_m[r] = M;
-            s_inv[r] = 1.f / den;
-        }
-    }
-    __syncthreads();
+                                             int nsplits, int q0) {
+    const int64_t split_rows = static_cast<int64_t>(a.decode_max_q) * a.num_q_heads;  // rows per split
+    const int64_t split_o = split_rows * D;
     __nv_bfloat16* out = reinterpret_cast<__nv_bfloat16*>(a.out);
     constexpr int kGroups = D / 4;  // 4 consecutive columns per work item
     for (int it = threadIdx.x; it < rows * kGroups; it += blockDim.x) {
         const int r = it / kGroups;
         const int d4 = (it % kGroups) * 4;
-        const float M = s_m[r];
         const int64_t row = partial_row(a, b, 0, tok[r], head[r]);
-        const float* ml = a.ws_ml + row * 2;
+        const float2* ml = reinterpret_cast<const float2*>(a.ws_ml) + row;  // (m, l) of split 0
         const float* os = a.ws_o + row * D + d4;
+        float M = -INFINITY, den = 0.f;
         float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-        int s = 0;
-        for (; s + 8 <= nsplits; s += 8) {  // 8 independent loads in flight
-            float m8[8];
-            float4 v8[8];
+        for (int s0 = 0; s0 < nsplits; s0 += kBatch) {
+            float2 mlv[kBatch];
+            float4 ov[kBatch];
 #pragma unroll
-            for (int k = 0; k < 8; ++k) {
-                m8[k] = __ldcg(ml + (s + k) * split_ml);
-                v8[k] = __ldcg(reinterpret_cast<const float4*>(os + (s + k) * split_o));
+            for (int k = 0; k < kBatch; ++k) {
+                if (s0 + k < nsplits) {
+                    mlv[k] = __ldcg(ml + (s0 + k) * split_rows);
+                    ov[k] = __ldcg(reinterpret_cast<const float4*>(os + (s0 + k) * split_o));
+                } else {
+                    mlv[k] = make_float2(-INFINITY, 0.f);
+                    ov[k] = make_float4(0.f, 0.f, 0.f, 0.f);
+                }
             }
+            float Mn = M;
 #pragma unroll
-            for (int k = 0; k < 8; ++k) {
-                const float w = fast_exp2(m8[k] - M);
-                acc.x += w * v8[k].x;
-                acc.y += w * v8[k].y;
-                acc.z += w * v8[k].z;
-                acc.w += w * v8[k].w;
+            for (int k = 0; k < kBatch; ++k) Mn = fmaxf(Mn, mlv[k].x);
+            const float sc = M == -INFINITY ? 0.f : fast_exp2(M - Mn);  // earlier batches, rebased
+            den *= sc;
+            acc.x *= sc;
+            acc.y *= sc;
+            acc.z *= sc;
+            acc.w *= sc;
+#pragma unroll
+            for (int k = 0; k < kBatch; ++k) {
+                const float w = mlv[k].x == -INFINITY ? 0.f : fast_exp2(mlv[k].x - Mn);
+                den += w * mlv[k].y;
+                acc.x += w * ov[k].x;
+                acc.y += w * ov[k].y;
+                acc.z += w * ov[k].z;
+                acc.w += w * ov[k].w;
             }
+            M = Mn;
         }
-        for (; s < nsplits; ++s) {
-            const float w = fast_exp2(__ldcg(ml + s * split_ml) - M);
-            const float4 v = __ldcg(reinterpret_cast<const float4*>(os + s * split_o));
-            acc.x += w * v.x;
-            acc.y += w * v.y;
-            acc.z += w * v.z;
-            acc.w += w * v.w;
-        }
-        const float inv = s_inv[r];
+        const float inv = 1.f / den;
         uint2 packed;
         packed.x = pack_bf16(acc.x * inv, acc.y * inv);
         packed.y = pack_bf16(acc.z * inv, acc.w * inv);
@@ -147,8 +141,31 @@ __device__ __forceinline__ void merge_splits(const Args& a, int b, const int* to
     }
 }
 
+// A 32-bit global load issued where it is written (the asm is not moved past
+// the branches that follow, so independent loads are in flight together).
+__device__ __forceinline__ int ldg_s32(const int32_t* p) {
+    int v;
+    asm volatile("ld.global.nc.s32 %0, [%1];\n" : "=r"(v) : "l"(p));
+    return v;
+}
+
+// Thread-block cluster helpers: the cluster's CTAs are resident together, so a
+// cluster barrier always completes; ld.shared::cluster reads a peer CTA's
+// shared memory at the same offset as `local` in this CTA.
+__device__ __forceinline__ void cluster_sync() {
+    asm volatile("barrier.cluster.arrive.release.aligned;\nbarrier.cluster.wait.acquire.aligned;\n" ::: "memory");
+}
+__device__ __forceinline__ float ld_peer(const float* local, uint32_t peer) {
+    uint32_t addr = smem_u32(local), remote;
+    float v;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;\n" : "=r"(remote) : "r"(addr), "r"(peer));
+    asm volatile("ld.shared::cluster.f32 %0, [%1];\n" : "=f"(v) : "r"(remote) : "memory");
+    return v;
+}
+
+// 4-warp CTAs are sized to share an SM three at a time (at most 170 registers).
 template <int D, int kWarps, int kStages>
-__global__ void __launch_bounds__(kWarps * 32) decode_splitkv_kernel(const Args a) {
+__global__ void __launch_bounds__(kWarps * 32, kWarps == 4 ? 3 : 1) decode_splitkv_kernel(const Args a) {
     using Tile = DecodeTile<D, kWarps, kStages>;
     extern __shared__ __align__(128) uint8_t smem[];
     const int warp = threadIdx.x >> 5;
@@ -163,60 +180,98 @@ __global__ void __launch_bounds__(kWarps * 32) decode_splitkv_kernel(const Args 
     idx /= a.row_groups;
     const int h = static_cast<int>(idx % a.num_kv_heads);
     const int b = static_cast<int>(idx / a.num_kv_heads);
+    // Cluster mode: the a.splits == a.decode_cluster CTAs of (b, h, rg) form one
+    // thread-block cluster, split the sequence's pages evenly and merge through
+    // distributed shared memory.  Otherwise split s covers keys
+    // [s * kv_chunk, (s + 1) * kv_chunk) and the splits merge through the workspace.
+    const bool clustered = a.decode_cluster > 1;
 
-    const int q0 = a.query_start_loc[b];
-    const int n = a.query_start_loc[b + 1] - q0;
+    // Every exit before the cluster barriers below depends on b alone, so the
+    // CTAs of a cluster take it together.  The metadata loads and (with static
+    // splits, whose page range does not depend on the sequence length) the first
+    // block-table entries are issued together, before anything waits on them.
+    const int32_t* bt = a.block_table + static_cast<int64_t>(b) * a.max_pages;
+    int bt_cur = 0, bt_nxt = 0;
+    if (!clustered) {
+        const int p0 = s * (a.kv_chunk / kPage);
+        const int pe = min(a.max_pages, p0 + a.kv_chunk / kPage);
+        const int i0 = p0 + warp + kWarps * lane, i1 = i0 + 32 * kWarps;
+        if (i0 < pe) bt_cur = ldg_s32(bt + i0);
+        if (i1 < pe) bt_nxt = ldg_s32(bt + i1);
+    }
+    const int q0 = ldg_s32(a.query_start_loc + b);
+    const int q1 = ldg_s32(a.query_start_loc + b + 1);
+    int L = ldg_s32(a.seq_lens + b);
+    const int n = q1 - q0;
     if (n < 1 || n > a.decode_max_q) return;  // empty, or the prefill kernel's
     if (q0 < 0 || static_cast<int64_t>(q0) + n > a.num_tokens) {
         flag_error(a.err, kDevBadQueryStart);
         return;
     }
-
     const int cap = a.max_pages * kPage;
-    int L = a.seq_lens[b];
     if (L > cap) {
         flag_error(a.err, kDevSeqTooLong);
         L = cap;
     }
-    // Rows of this CTA: r -> (new token tok, query head head).
+    // Rows of this CTA: r -> (new token, query head).
     const bool packed = a.row_groups == 1;  // tokens x G heads in one tile
     const int rows = packed ? n * a.group : min(kRows, a.group - rg * kRows);
+    auto tok_of = [&](int r) { return packed ? r / a.group : 0; };
+    auto head_of = [&](int r) { return packed ? h * a.group + r % a.group : h * a.group + rg * kRows + r; };
     __shared__ int s_tok[kRows], s_head[kRows];
-    if (threadIdx.x < kRows) {
-        const int r = threadIdx.x;
-        s_tok[r] = packed ? r / a.group : 0;
-        s_head[r] = packed ? h * a.group + r % a.group : h * a.group + rg * kRows + r;
+    if (threadIdx.x < kRows) {  // for the workspace merge; read after later barriers
+        s_tok[threadIdx.x] = tok_of(threadIdx.x);
+        s_head[threadIdx.x] = head_of(threadIdx.x);
     }
-    __syncthreads();
     __nv_bfloat16* out = reinterpret_cast<__nv_bfloat16*>(a.out);
     if (L < n) {
         // A query must see at least itself; the caller broke the contract.
         if (s == 0) {
             flag_error(a.err, kDevQueryTooLong);
             for (int i = threadIdx.x; i < rows * D; i += blockDim.x)
-                out[(static_cast<int64_t>(q0 + s_tok[i / D]) * a.num_q_heads + s_head[i / D]) * D + i % D] =
+                out[(static_cast<int64_t>(q0 + tok_of(i / D)) * a.num_q_heads + head_of(i / D)) * D + i % D] =
                     __float2bfloat16(0.f);
         }
         return;
     }
-    const int start = s * a.kv_chunk;
-    if (start >= L) return;
-    const int end = min(L, start + a.kv_chunk);
-    const int npages = (end - start + kPage - 1) / kPage;
-    const int nsplits = (L + a.kv_chunk - 1) / a.kv_chunk;
+    // This CTA's keys [start, end); start is a page boundary.
+    int start, end, nsplits;
+    if (clustered) {
+        const int pages_b = (L + kPage - 1) / kPage;
+        const int per = (pages_b + a.splits - 1) / a.splits;
+        start = min(L, s * per * kPage);
+        end = min(L, (s + 1) * per * kPage);
+        nsplits = a.splits;
+    } else {
+        start = s * a.kv_chunk;
+        if (start >= L) return;
+        end = min(L, start + a.kv_chunk);
+        nsplits = (L + a.kv_chunk - 1) / a.kv_chunk;
+    }
+    const int npages = (end - start + kPage - 1) / kPage;  // 0 for an empty split of a cluster
     const int my_pages = warp < npages ? (npages - warp + kWarps - 1) / kWarps : 0;
+
+    // Block-table entries of this warp's pages, 32 at a time in registers (lane l
+    // holds the entry of the warp's page 32 * round + l), the next round loaded
+    // ahead, so that the copies do not wait on them.  (Static splits loaded the
+    // first two rounds above; a cluster's split needs the length first.)
+    auto bt_entry = [&](int i) { return i < my_pages ? bt[start / kPage + warp + kWarps * i] : 0; };
+    if (clustered) {
+        bt_cur = bt_entry(lane);
+        bt_nxt = bt_entry(32 + lane);
+    }
 
     // Q fragments for all D/16 k-steps; rows >= `rows` are zero.  Each of this
     // thread's two rows (g, g + 8) has its own causal limit.
     const __nv_bfloat16* q = reinterpret_cast<const __nv_bfloat16*>(a.q);
     const bool row_lo = g < rows, row_hi = g + 8 < rows;
     const __nv_bfloat16* qg =
-        q + (static_cast<int64_t>(q0 + (row_lo ? s_tok[g] : 0)) * a.num_q_heads + (row_lo ? s_head[g] : 0)) * D;
+        q + (static_cast<int64_t>(q0 + (row_lo ? tok_of(g) : 0)) * a.num_q_heads + (row_lo ? head_of(g) : 0)) * D;
     const __nv_bfloat16* qg8 =
-        q + (static_cast<int64_t>(q0 + (row_hi ? s_tok[g + 8] : 0)) * a.num_q_heads + (row_hi ? s_head[g + 8] : 0)) *
+        q + (static_cast<int64_t>(q0 + (row_hi ? tok_of(g + 8) : 0)) * a.num_q_heads + (row_hi ? head_of(g + 8) : 0)) *
                 D;
-    const int lim_lo = L - n + (row_lo ? s_tok[g] : 0);      // last key row g may see
-    const int lim_hi = L - n + (row_hi ? s_tok[g + 8] : 0);
+    const int lim_lo = L - n + (row_lo ? tok_of(g) : 0);      // last key row g may see
+    const int lim_hi = L - n + (row_hi ? tok_of(g + 8) : 0);
     uint32_t qa[D / 16][4];
 #pragma unroll
     for (int ks = 0; ks < D / 16; ++ks) {
@@ -229,17 +284,9 @@ __global__ void __launch_bounds__(kWarps * 32) decode_splitkv_kernel(const Args 
 
     const __nv_bfloat16* kc = reinterpret_cast<const __nv_bfloat16*>(a.k_cache);
     const __nv_bfloat16* vc = reinterpret_cast<const __nv_bfloat16*>(a.v_cache);
-    const int32_t* bt = a.block_table + static_cast<int64_t>(b) * a.max_pages;
     const uint32_t wbase = smem_u32(smem) + warp * Tile::kWarpBytes;
     const uint64_t policy = policy_evict_first();
 
-    // Issue the copies of this warp's it-th page into stage it % kStages; always
-    // commit a group so that the wait count below stays uniform.
-    // Block-table entries of this warp's pages, 32 at a time in registers (lane l
-    // holds the entry of the warp's page 32 * round + l), the next round loaded
-    // ahead, so that the copies do not wait on them.
-    auto bt_entry = [&](int i) { return i < my_pages ? bt[start / kPage + warp + kWarps * i] : 0; };
-    int bt_cur = bt_entry(lane), bt_nxt = bt_entry(32 + lane);
     auto page_of = [&](int it) {  // every lane calls it with the same it
         if (it > 0 && (it & 31) == 0) {
             bt_cur = bt_nxt;
@@ -247,6 +294,8 @@ __global__ void __launch_bounds__(kWarps * 32) decode_splitkv_kernel(const Args 
         }
         return __shfl_sync(0xffffffffu, bt_cur, it & 31);
     };
+    // Issue the copies of this warp's it-th page into stage it % kStages; always
+    // commit a group so that the wait count below stays uniform.
     auto issue = [&](int it) {
         if (it < my_pages) {
             const int lp = start / kPage + warp + kWarps * it;
@@ -285,7 +334,6 @@ __global__ void __launch_bounds__(kWarps * 32) decode_splitkv_kernel(const Args 
         __syncwarp();
         const uint32_t sk = wbase + (it % kStages) * Tile::kStageBytes;
         const uint32_t sv = sk + Tile::kPageBytes;
-
         // S = Q K^T for the page's 16 tokens: two n-tiles of 8 tokens.
         float sc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
         {
@@ -359,45 +407,55 @@ __global__ void __launch_bounds__(kWarps * 32) decode_splitkv_kernel(const Args 
     cp_async_wait<0>();
     __syncthreads();
 
-    // Merge the 4 warps' partial softmax states in shared memory.
+    // Merge the warps' partial softmax states in shared memory.
+    constexpr int kMS = Tile::kMS;
+    constexpr int kM0 = kRows * kMS;  // m[16], then l[16], after the O rows
     float* mw = reinterpret_cast<float*>(smem) + warp * Tile::kMergeWarpFloats;
 #pragma unroll
     for (int i = 0; i < D / 8; ++i) {
         const int c = i * 8 + 2 * tq;
-        mw[g * D + c] = o[i][0];
-        mw[g * D + c + 1] = o[i][1];
-        mw[(g + 8) * D + c] = o[i][2];
-        mw[(g + 8) * D + c + 1] = o[i][3];
+        *reinterpret_cast<float2*>(mw + g * kMS + c) = make_float2(o[i][0], o[i][1]);
+        *reinterpret_cast<float2*>(mw + (g + 8) * kMS + c) = make_float2(o[i][2], o[i][3]);
     }
     l_lo = quad_sum(l_lo);
     l_hi = quad_sum(l_hi);
     if (tq == 0) {
-        mw[kRows * D + g] = m_lo;
-        mw[kRows * D + g + 8] = m_hi;
-        mw[kRows * D + kRows + g] = l_lo;
-        mw[kRows * D + kRows + g + 8] = l_hi;
+        mw[kM0 + g] = m_lo;
+        mw[kM0 + g + 8] = m_hi;
+        mw[kM0 + kRows + g] = l_lo;
+        mw[kM0 + kRows + g + 8] = l_hi;
     }
     __syncthreads();
 
+    // This CTA's (O, m, l) for row r: over the warps, M = max m_w, then
+    // O = sum 2^(m_w - M) O_w and l likewise.
     const float* ms = reinterpret_cast<const float*>(smem);
+    float* cta = reinterpret_cast<float*>(smem) + Tile::kCtaPartialOffFloats;  // [16][D] O, [16] m, [16] l
     for (int i = threadIdx.x; i < rows * D; i += blockDim.x) {
         const int r = i / D, d = i % D;
         float M = -INFINITY;
 #pragma unroll
-        for (int w = 0; w < kWarps; ++w) M = fmaxf(M, ms[w * Tile::kMergeWarpFloats + kRows * D + r]);
+        for (int w = 0; w < kWarps; ++w) M = fmaxf(M, ms[w * Tile::kMergeWarpFloats + kM0 + r]);
         float acc = 0.f, l = 0.f;
 #pragma unroll
         for (int w = 0; w < kWarps; ++w) {
             const float* mwr = ms + w * Tile::kMergeWarpFloats;
-            const float mwv = mwr[kRows * D + r];
+            const float mwv = mwr[kM0 + r];
             const float sc = mwv == -INFINITY ? 0.f : fast_exp2(mwv - M);
-            acc += sc * mwr[r * D + d];
-            l += sc * mwr[kRows * D + kRows + r];
+            acc += sc * mwr[r * kMS + d];
+            l += sc * mwr[kM0 + kRows + r];
         }
-        if (nsplits == 1) {
-            out[(static_cast<int64_t>(q0 + s_tok[r]) * a.num_q_heads + s_head[r]) * D + d] = __float2bfloat16(acc / l);
+        if (clustered) {
+            cta[r * D + d] = acc;
+            if (d == 0) {
+                cta[kRows * D + r] = M;
+                cta[kRows * D + kRows + r] = l;
+            }
+        } else if (nsplits == 1) {
+            out[(static_cast<int64_t>(q0 + tok_of(r)) * a.num_q_heads + head_of(r)) * D + d] =
+                __float2bfloat16(acc / l);
         } else {
-            const int64_t slot = partial_row(a, b, s, s_tok[r], s_head[r]);
+            const int64_t slot = partial_row(a, b, s, tok_of(r), head_of(r));
             a.ws_o[slot * D + d] = acc;
             if (d == 0) {
                 a.ws_ml[slot * 2] = M;
@@ -405,40 +463,96 @@ __global__ void __launch_bounds__(kWarps * 32) decode_splitkv_kernel(const Args 
             }
         }
     }
+
+    if (clustered) {
+        // Every CTA of the cluster merges D / C columns of every row, reading the
+        // C partials from the CTAs' shared memory; a CTA with no keys holds
+        // m = -inf and weight 0.  The second barrier keeps every CTA's shared
+        // memory alive until its peers have read it.
+        cluster_sync();
+        const int C = a.splits;
+        // (m, l) of every row of every CTA, one remote load per thread, then the
+        // per-row weights 2^(m_c - M) / sum_c 2^(m_c - M) l_c.
+        __shared__ float s_w[kMaxCluster][kRows], s_lc[kMaxCluster][kRows];
+        for (int i = threadIdx.x; i < C * kRows; i += blockDim.x) {
+            const int c = i / kRows, r = i % kRows;
+            const float mc = r < rows ? ld_peer(cta + kRows * D + r, c) : -INFINITY;
+            const float lc = r < rows ? ld_peer(cta + kRows * D + kRows + r, c) : 0.f;
+            s_w[c][r] = mc;
+            s_lc[c][r] = lc;
+        }
+        __syncthreads();
+        if (threadIdx.x < rows) {
+            const int r = threadIdx.x;
+            float M = -INFINITY;
+            for (int c = 0; c < C; ++c) M = fmaxf(M, s_w[c][r]);
+            float l = 0.f;
+            for (int c = 0; c < C; ++c) {
+                const float w = s_w[c][r] == -INFINITY ? 0.f : fast_exp2(s_w[c][r] - M);
+                s_w[c][r] = w;
+                l += w * s_lc[c][r];
+            }
+            const float inv = 1.f / l;
+            for (int c = 0; c < C; ++c) s_w[c][r] *= inv;
+        }
+        __syncthreads();
+        const int cols = (D + C - 1) / C;
+        const int d0 = s * cols;
+        const int ncols = max(0, min(cols, D - d0));
+        for (int i = threadIdx.x; i < rows * ncols; i += blockDim.x) {
+            const int r = i / ncols, d = d0 + i % ncols;
+            float v[kMaxCluster];
+#pragma unroll
+            for (int c = 0; c < kMaxCluster; ++c) v[c] = c < C ? ld_peer(cta + r * D + d, c) : 0.f;
+            float acc = 0.f;
+#pragma unroll
+            for (int c = 0; c < kMaxCluster; ++c)
+                if (c < C) acc += s_w[c][r] * v[c];
+            out[(static_cast<int64_t>(q0 + tok_of(r)) * a.num_q_heads + head_of(r)) * D + d] = __float2bfloat16(acc);
+        }
+        cluster_sync();
+        return;
+    }
     if (nsplits == 1) return;
 
-    // Split merge.  Each split CTA publishes its partial, then takes a ticket;
-    // the one that draws the last ticket merges every split of (b, h, rg) and
-    // resets the counter for the next call.  Nobody waits on anybody.
+    // Split merge through the workspace.  Each split CTA publishes its partial,
+    // then takes a ticket; the one that draws the last ticket merges every split
+    // of (b, h, rg) and resets the counter for the next call.  Nobody waits on
+    // anybody.  The ticket is a release-acquire atomic of one thread after a
+    // CTA barrier: release is cumulative, so it publishes the whole CTA's
+    // partial, and the last CTA's acquire makes every partial visible to it
+    // (its barrier passes that on to the other threads).
     __shared__ int s_last;
-    __threadfence();
     __syncthreads();
     int32_t* counter = a.counters + (static_cast<int64_t>(b) * a.num_kv_heads + h) * a.row_groups + rg;
-    if (threadIdx.x == 0) s_last = atomicAdd(counter, 1) == nsplits - 1;
+    if (threadIdx.x == 0) {
+        int prev;
+        asm volatile("atom.acq_rel.gpu.global.add.s32 %0, [%1], 1;\n" : "=r"(prev) : "l"(counter) : "memory");
+        s_last = prev == nsplits - 1;
+    }
     __syncthreads();
     if (!s_last) return;
-    __threadfence();
-    merge_splits<D>(a, b, s_tok, s_head, rows, nsplits, q0, reinterpret_cast<float*>(smem));
+    merge_splits<D, (kWarps == 8 ? 16 : 8)>(a, b, s_tok, s_head, rows, nsplits, q0);
     if (threadIdx.x == 0) *counter = 0;
 }
 
 template <int D, int kWarps, int kStages>
 cudaError_t launch_decode_d(const Args& a, cudaStream_t stream) {
     using Tile = DecodeTile<D, kWarps, kStages>;
-    static bool configured[64] = {};  // the attribute is set once per device
+    auto kernel = decode_splitkv_kernel<D, kWarps, kStages>;
+    static bool configured[64] = {};  // the attributes are set once per device
     int dev = 0;
     cudaGetDevice(&dev);
     if (!configured[dev & 63]) {
-        cudaError_t e = cudaFuncSetAttribute(decode_splitkv_kernel<D, kWarps, kStages>,
-                                             cudaFuncAttributeMaxDynamicSharedMemorySize, Tile::kSmemBytes);
+        cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, Tile::kSmemBytes);
+        if (e == cudaSuccess) e = cudaFuncSetAttribute(kernel, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
         if (e != cudaSuccess) return e;
         configured[dev & 63] = true;
     }
     const int64_t ctas = decode_ctas(a);
     if (ctas == 0) return cudaSuccess;
-    decode_splitkv_kernel<D, kWarps, kStages>
-        <<<static_cast<unsigned>(ctas), kWarps * 32, Tile::kSmemBytes, stream>>>(a);
-    return cudaGetLastError();
+    return launch_kernel(kernel, static_cast<unsigned>(ctas), kWarps * 32, Tile::kSmemBytes, stream,
+                         a.decode_cluster, a);
 }
 
 template <int D>

@@ -125,11 +125,14 @@ extern "C" pa_status pa_forward_noalloc(const void* q, const void* k_cache, cons
     a.decode_max_q = pa::decode_max_q(a.group);
     a.decode_stages = info.decode_stages;
     a.decode_warps = info.decode_warps;
+    a.decode_cluster = info.decode_cluster > 1 ? info.decode_cluster : 1;
     a.scale = scale;
     a.scale_log2 = scale * 1.4426950408889634f;
     const pa::WorkspaceLayout wl =
-        pa::workspace_layout(a.num_seqs, a.num_q_heads, a.splits, a.head_dim, a.decode_max_q,
-                             pa::counter_bytes_needed(a.num_seqs, a.num_kv_heads, a.row_groups, a.splits));
+        pa::workspace_layout(a.num_seqs, a.num_q_heads, pa::ws_splits(a.splits, a.decode_cluster), a.head_dim,
+                             a.decode_max_q,
+                             pa::counter_bytes_needed(a.num_seqs, a.num_kv_heads, a.row_groups,
+                                                      pa::ws_splits(a.splits, a.decode_cluster)));
     unsigned char* const sb = static_cast<unsigned char*>(scratch);
     a.counters = reinterpret_cast<int32_t*>(sb + wl.counters_off);
     a.ws_o = reinterpret_cast<float*>(sb + wl.o_off);

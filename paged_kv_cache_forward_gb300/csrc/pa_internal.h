@@ -5,6 +5,8 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <utility>
+
 namespace pa {
 
 // Device error codes written to the sticky error word (first one wins).
@@ -38,6 +40,9 @@ struct Args {
     int32_t decode_max_q;  // sequences with 1..decode_max_q new tokens take the decode path
     int32_t decode_stages; // cp.async pipeline depth per decode warp (pages)
     int32_t decode_warps;  // warps per decode CTA
+    int32_t decode_cluster;  // > 1: the splits of a (sequence, KV head, row group) are one
+                             // thread-block cluster of this many CTAs (== splits), merged
+                             // through distributed shared memory; 1: merged through ws
     float scale;         // softmax scale
     float scale_log2;    // scale * log2(e)
 };
@@ -52,6 +57,9 @@ cudaError_t launch_cache_write(const void* k_new, const void* v_new, const int64
 // (tokens x the G heads of a KV head) must fit one 16-row MMA tile.  With more
 // than 16 heads per KV head the decode path takes single-token queries only.
 inline int32_t decode_max_q(int32_t group) { return group <= 16 ? 16 / group : 1; }
+
+// Splits whose partials go through the workspace (none in cluster mode).
+inline int32_t ws_splits(int32_t splits, int32_t decode_cluster) { return decode_cluster > 1 ? 1 : splits; }
 
 // Workspace layout shared by pa_forward and pa_forward_noalloc: a 256-byte
 // header (sticky error word), an area of split ticket counters (zero before and
@@ -76,6 +84,31 @@ inline WorkspaceLayout workspace_layout(int64_t num_seqs, int32_t num_q_heads, i
     w.ml_off = w.o_off + rows * head_dim * 4;
     w.bytes = w.ml_off + rows * 2 * 4;
     return w;
+}
+
+// Launches a kernel of this library, as 1-D thread-block clusters of `cluster`
+// CTAs if cluster > 1.  (Programmatic dependent launch was measured and left
+// out: early-resident CTAs of the next step land unevenly on the SMs.)
+template <typename... KArgs, typename... Args>
+cudaError_t launch_kernel(void (*kernel)(KArgs...), unsigned grid, unsigned block, size_t smem,
+                          cudaStream_t stream, int cluster, Args&&... args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(grid, 1, 1);
+    cfg.blockDim = dim3(block, 1, 1);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    int n = 0;
+    if (cluster > 1) {
+        attr[0].id = cudaLaunchAttributeClusterDimension;
+        attr[0].val.clusterDim.x = static_cast<unsigned>(cluster);
+        attr[0].val.clusterDim.y = 1;
+        attr[0].val.clusterDim.z = 1;
+        n = 1;
+    }
+    cfg.attrs = attr;
+    cfg.numAttrs = n;
+    return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
 }
 
 // Sets the calling thread's pa_last_error() text.

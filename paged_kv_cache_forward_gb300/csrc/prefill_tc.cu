@@ -573,9 +573,8 @@ cudaError_t launch_d(const Args& a, cudaStream_t stream) {
         !encode_cache_map(&tk_map, a.k_cache, D, a.num_kv_heads, a.num_blocks) ||
         !encode_cache_map(&tv_map, a.v_cache, D, a.num_kv_heads, a.num_blocks))
         return cudaErrorInvalidValue;
-    prefill_tc_kernel<D><<<static_cast<unsigned>(ctas), kThreads, S::kAlloc, stream>>>(tq_map, tk_map, tv_map, a, tq,
-                                                                                       pairs_bound(a));
-    return cudaGetLastError();
+    return launch_kernel(prefill_tc_kernel<D>, static_cast<unsigned>(ctas), kThreads, S::kAlloc, stream, 1, tq_map,
+                         tk_map, tv_map, a, tq, pairs_bound(a));
 }
 
 }  // namespace

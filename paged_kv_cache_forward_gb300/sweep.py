@@ -61,22 +61,22 @@ def candidates(bound: int, batch: int, sms: int, warps: int, stages: int):
     return sorted(c for c in base if 16 <= c <= bound)
 
 
-def time_shape(bound, batch, chunk, pools, stream, warps=0, stages=0, steps_per_graph=16, reps=30):
+def time_shape(bound, batch, chunk, pools, stream, warps=0, stages=0, cluster=0, steps_per_graph=16, reps=30):
     q, ks, vs, bt, sl, qsl, out = pools
     R = len(ks)
     pa.prepare(q, ks[0], bt, sl, kv_chunk=chunk, stream=stream, decode_stages=stages,
-               decode_warps=warps)
+               decode_warps=warps, decode_cluster=cluster)
     with torch.cuda.stream(stream):
         for i in range(2):
             pa.forward(q, ks[i % R], vs[i % R], bt, sl, qsl, out, kv_chunk=chunk, stream=stream,
-                       decode_stages=stages, decode_warps=warps)
+                       decode_stages=stages, decode_warps=warps, decode_cluster=cluster)
     stream.synchronize()
     M = max(R, (steps_per_graph // R) * R)
     g = torch.cuda.CUDAGraph()
     with torch.cuda.graph(g, stream=stream):
         for i in range(M):
             pa.forward(q, ks[i % R], vs[i % R], bt, sl, qsl, out, kv_chunk=chunk, stream=stream,
-                       decode_stages=stages, decode_warps=warps)
+                       decode_stages=stages, decode_warps=warps, decode_cluster=cluster)
     for _ in range(3):
         g.replay()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
@@ -89,7 +89,7 @@ def time_shape(bound, batch, chunk, pools, stream, warps=0, stages=0, steps_per_
     code = pa.device_error(stream)
     if code:
         raise RuntimeError(f"device error {code} ({pa.DEVICE_ERRORS.get(code)}) at bound {bound}, batch {batch}, "
-                           f"split {chunk}, variant {warps}x{stages}")
+                           f"split {chunk}, variant {warps}x{stages}, cluster {cluster}")
     return e0.elapsed_time(e1) * 1e3 / (reps * M)  # us per step
 
 
@@ -120,10 +120,12 @@ def main(argv=None):
     ap.add_argument("--bounds", default=",".join(map(str, BOUNDS)))
     ap.add_argument("--batches", default=",".join(map(str, BATCHES)))
     ap.add_argument("--variants", default=VARIANTS, help="decode variants to try: warps x stages")
+    ap.add_argument("--clusters", default="2,4,8,16", help="cluster sizes to try (even split, merge in DSMEM)")
     args = ap.parse_args(argv)
     bounds = [int(x) for x in args.bounds.split(",")]
     batches = [int(x) for x in args.batches.split(",")]
     variants = [tuple(int(y) for y in v.split("x")) for v in args.variants.split(",")]
+    clusters = [int(c) for c in args.clusters.split(",") if c]
 
     from paged_kv_cache_forward_gb300 import build
     build.build()
@@ -142,19 +144,23 @@ def main(argv=None):
             pools, kv = make_pools(bound, batch, l2, gen)
             res = []
             for w, st in variants:
-                for chunk in candidates(bound, batch, sms, w, st):
+                # (split size, 1): splits merged through the workspace;
+                # (0, C): an even split over a cluster of C CTAs
+                cands = [(c, 1) for c in candidates(bound, batch, sms, w, st)] + [(0, c) for c in clusters]
+                for chunk, cl in cands:
                     try:
-                        us = time_shape(bound, batch, chunk, pools, stream, warps=w, stages=st)
+                        us = time_shape(bound, batch, chunk, pools, stream, warps=w, stages=st, cluster=cl)
                     except RuntimeError as e:  # reported, and the candidate is not used
                         print(f"skipped: {e}", flush=True)
                         continue
-                    res.append((us, chunk, st, w))
+                    res.append((us, chunk, st, w, cl))
             res.sort()
-            us, chunk, st, w = res[0]
-            best[(bound, batch)] = (chunk, st, w)
-            row = " ".join(f"{c}/{ww}x{t}:{kv / u / 1e3:.0f}"
-                           for u, c, t, ww in sorted(res, key=lambda x: (x[3], x[2], x[1])))
-            lines.append(f"| {batch} | {bound} | {chunk} | {w}x{st} | {us:.1f} | {kv / us / 1e3:.0f} | {row} |")
+            us, chunk, st, w, cl = res[0]
+            best[(bound, batch)] = (chunk, st, w, cl)
+            name = lambda c, cl: f"c{cl}" if cl > 1 else f"{c}"
+            row = " ".join(f"{name(c, k)}/{ww}x{t}:{kv / u / 1e3:.0f}"
+                           for u, c, t, ww, k in sorted(res, key=lambda x: (x[3], x[2], x[4], x[1])))
+            lines.append(f"| {batch} | {bound} | {name(chunk, cl)} | {w}x{st} | {us:.1f} | {kv / us / 1e3:.0f} | {row} |")
             print(lines[-1], flush=True)
             del pools
             torch.cuda.empty_cache()
@@ -177,6 +183,7 @@ def main(argv=None):
                 "Llama-3.1-8B-shaped decode (Hq 32, Hkv 8, D 128), every sequence at the bound,\n"
                 "graph-replayed pa_forward steps rotating over KV pool copies larger than 3 x L2.\n"
                 "GB/s = KV bytes per step / step time.\n\n"
+                "Split `cN`: the keys split evenly over a thread-block cluster of N CTAs.\n\n"
                 "| batch | bound | best split | warps x stages | us/step | GB/s | split/variant:GB/s for every candidate |\n"
                 "|---|---|---|---|---|---|---|\n")
         f.write("\n".join(lines) + "\n")
@@ -187,14 +194,15 @@ def write_table(path, entries, last_batch, fallback, gpu_name, stamp):
     with open(path, "w") as f:
         f.write("// Keys per split and decode kernel variant, keyed on the context bound\n"
                 "// (max_pages * page_size) and the number of sequences:\n"
-                "// {max_bound, max_seqs, kv_chunk, decode_stages, decode_warps}.  The first\n"
+                "// {max_bound, max_seqs, kv_chunk, decode_stages, decode_warps, decode_cluster}\n"
+                "// (cluster > 1: an even split over a cluster of that many CTAs).  The first\n"
                 "// entry that matches wins; the last entry is the fallback.  Written by\n"
                 f"// paged_kv_cache_forward_gb300/sweep.py on {gpu_name} ({stamp}).\n"
                 "static const LutEntry kSplitTable[] = {\n")
-        for bound, batch, chunk, st, w in entries:
+        for bound, batch, chunk, st, w, cl in entries:
             mb = (1 << 30) if batch == last_batch else batch
-            f.write(f"    {{{bound}, {mb}, {chunk}, {st}, {w}}},\n")
-        f.write(f"    {{1 << 30, 1 << 30, {fallback[0]}, {fallback[1]}, {fallback[2]}}},\n}};\n")
+            f.write(f"    {{{bound}, {mb}, {chunk or 16}, {st}, {w}, {cl}}},\n")
+        f.write(f"    {{1 << 30, 1 << 30, {fallback[0] or 16}, {fallback[1]}, {fallback[2]}, {fallback[3]}}},\n}};\n")
 
 
 if __name__ == "__main__":

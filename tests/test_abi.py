@@ -106,6 +106,22 @@ def test_decode_variant_option(lib):
         assert e.value.status == B.PA_ERR_INVALID_ARG
 
 
+def test_decode_cluster_option(lib):
+    for c in (2, 4, 8, 16, 3):
+        p = B.plan(llama_dims(), decode_cluster=c)
+        assert p["decode_cluster"] == c and p["splits"] == c
+        assert p["decode_ctas"] == 8 * c
+        assert p["kv_chunk"] * c >= 2048 * 16 and p["kv_chunk"] % 16 == 0
+        # partials merge in distributed shared memory: only the error word
+        assert p["workspace_bytes"] == 256
+    assert B.plan(llama_dims(), kv_chunk=1024)["decode_cluster"] == 1
+    assert B.plan(llama_dims(), decode_cluster=1, decode_warps=8)["decode_cluster"] == 1
+    for kw in (dict(decode_cluster=17), dict(decode_cluster=-1), dict(decode_cluster=4, kv_chunk=1024)):
+        with pytest.raises(B.PagedAttnError) as e:
+            B.plan(llama_dims(), **kw)
+        assert e.value.status == B.PA_ERR_INVALID_ARG
+
+
 def test_bad_chunk_rejected(lib):
     with pytest.raises(B.PagedAttnError) as e:
         B.plan(llama_dims(), kv_chunk=24)

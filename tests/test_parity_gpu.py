@@ -124,6 +124,36 @@ def test_decode_variants(warps, stages, D):
         assert torch.equal(got.view(torch.int16), base.view(torch.int16)), (warps, stages, chunk)
 
 
+@pytest.mark.parametrize("cluster", [2, 3, 4, 8, 16])
+@pytest.mark.parametrize("warps,stages", [(4, 2), (8, 3), (12, 2)])
+def test_decode_cluster_mode(cluster, warps, stages):
+    """Splits merged in distributed shared memory: the keys of each (sequence,
+    KV head) split evenly over a cluster of CTAs.  Sequences shorter than the
+    cluster's page count leave some CTAs without keys; multi-token rows included."""
+    b = W.make_batch([1, 1, 3, 1, 2, 1], [4000, 1, 777, 65, 2500, 16], 32, 8, 128, seed=41 + cluster,
+                     max_pages=256)
+    ref = oracle.batch_attention(b)
+    got = run(b, decode_cluster=cluster, decode_warps=warps, decode_stages=stages)
+    assert_close(got, ref, f"cluster {cluster} {warps}x{stages}")
+
+
+@pytest.mark.parametrize("Hq,Hkv,D", [(32, 1, 128), (16, 2, 64), (8, 8, 128)])
+def test_decode_cluster_mode_head_shapes(Hq, Hkv, D):
+    b = W.make_batch([1, 1, 1], [3000, 129, 40], Hq, Hkv, D, seed=Hq * Hkv + D, max_pages=200)
+    ref = oracle.batch_attention(b)
+    for cluster in (4, 16):
+        assert_close(run(b, decode_cluster=cluster), ref, f"heads {Hq}/{Hkv} D {D} cluster {cluster}")
+
+
+def test_decode_cluster_spikes_bit_exact():
+    b, exp = W.spike_batch([1, 2, 1, 4], [40, 1000, 5000, 17], 32, 8, 128, seed=27, max_pages=320)
+    want = _codes(exp, 128)
+    for cluster in (2, 7, 16):
+        got = run(b, decode_cluster=cluster)
+        bad = (got.view(torch.int16) != want.view(torch.int16)).any(-1)
+        assert not bad.any(), (cluster, torch.nonzero(bad)[:5].tolist())
+
+
 # ------------------------------------------------------------------- edge cases
 
 def test_edge_lengths():
