@@ -35,7 +35,7 @@ pa_status cuda_fail(cudaError_t e, const char* what) {
 // number of sequences, as measured by the offline sweep (lut_gb300.inc).
 struct LutEntry {
     int32_t max_bound;  // applies when context bound <= max_bound
-    int32_t max_seqs;   // ... and num_seqs <= max_seqs
+    int32_t max_units;  // ... and (sequences x KV heads x row groups) <= max_units
     int32_t kv_chunk;
     int32_t decode_stages;  // 0: the default depth
     int32_t decode_warps;   // 0: the default warps per CTA
@@ -46,9 +46,13 @@ struct LutEntry {
 constexpr int32_t kDefaultDecodeStages = 2, kDefaultDecodeWarps = 4;
 constexpr int32_t kMaxDecodeCluster = 16;  // largest thread-block cluster (non-portable size)
 
-const LutEntry& table_entry(int64_t bound, int32_t num_seqs) {
+// The key is the context bound and the number of independent (sequence, KV
+// head, row group) units: the decode grid is units x splits, so a shape with
+// the same units and bound needs the same split (an MQA batch of 8 behaves like
+// one Llama sequence with 8 KV heads).
+const LutEntry& table_entry(int64_t bound, int64_t units) {
     for (const LutEntry& e : kSplitTable)
-        if (bound <= e.max_bound && num_seqs <= e.max_seqs) return e;
+        if (bound <= e.max_bound && units <= e.max_units) return e;
     return kSplitTable[sizeof(kSplitTable) / sizeof(kSplitTable[0]) - 1];
 }
 
@@ -92,7 +96,9 @@ pa_status make_plan(const pa_dims* d, const pa_options* o, Plan* p) {
     pa_status st = check_dims(d);
     if (st != PA_OK) return st;
     const int64_t bound = static_cast<int64_t>(d->max_pages) * d->page_size;
-    const LutEntry& te = table_entry(bound, d->num_seqs);
+    const int32_t group0 = d->num_q_heads / d->num_kv_heads;
+    const LutEntry& te =
+        table_entry(bound, static_cast<int64_t>(d->num_seqs) * d->num_kv_heads * ((group0 + 15) / 16));
     int64_t chunk = (o && o->kv_chunk) ? o->kv_chunk : te.kv_chunk;
     if (chunk < d->page_size || chunk % d->page_size)
         return fail(PA_ERR_INVALID_ARG, "kv_chunk %lld must be a positive multiple of page_size",

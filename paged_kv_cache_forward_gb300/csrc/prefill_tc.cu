@@ -14,10 +14,11 @@
 // mask bottom-right aligned ("Flash Attention in Triton"), online softmax,
 // O += P V, out = O / l.
 //
-// Warp roles (320 threads):
-//   warp 0      TMA producer: both Q tiles once, then per KV tile the K page
-//               boxes and the V page boxes (64 columns x 16 slots of one page and
-//               head, 128-byte swizzle) into 2-stage K and V rings.  Block-table
+// Warp roles (352 threads):
+//   warps 0, 10 TMA producers: warp 0 both Q tiles once, then per KV tile the K
+//               page boxes (64 columns x 16 slots of one page and head, 128-byte
+//               swizzle) into a 3-stage K ring; warp 10 the V page boxes into a
+//               2-stage V ring, each running ahead on its own.  Block-table
 //               entries are fetched one group of 4 tiles ahead.  The one page of
 //               V that holds the sequence end is copied by plain loads with zero
 //               fill, so no slot past seq_len reaches the MMA.
@@ -53,7 +54,8 @@
 namespace pa {
 namespace {
 
-constexpr int kThreads = 320;
+constexpr int kThreads = 352;
+constexpr int kWarpV = 10;  // the V producer
 constexpr int kM = 128;            // rows per tile
 constexpr int kKeys = 128;         // keys per KV tile
 constexpr int kPage = 16;
@@ -64,8 +66,13 @@ constexpr uint32_t kTmemCols = 512;
 // TMEM columns of tile x: S at 128 x (P over its last 64 columns), O at 256 + 128 x.
 __device__ __forceinline__ uint32_t tmem_s(int x) { return x ? 128u : 0u; }
 __device__ __forceinline__ uint32_t tmem_o(int x) { return x ? 384u : 256u; }
-constexpr int kKStages = 2, kVStages = 2;
+constexpr int kKStages = 3, kVStages = 2;
 constexpr int kTilesPerGroup = 4;  // block-table prefetch: 4 tiles x 8 pages = one entry per lane
+#ifndef PA_PREFILL_L2_PREFETCH
+#define PA_PREFILL_L2_PREFETCH 2
+#endif
+constexpr int kPrefetchTiles = PA_PREFILL_L2_PREFETCH;  // K/V tiles ahead brought into L2 (0: none)
+static_assert(kPrefetchTiles < kTilesPerGroup, "prefetched tiles must be in the current or next group");
 
 template <int D>
 struct Smem {
@@ -75,23 +82,24 @@ struct Smem {
     static constexpr int kK0 = kQ0 + 2 * kTile;
     static constexpr int kV0 = kK0 + kKStages * kTile;
     static constexpr int kBar = kV0 + kVStages * kTile;
-    static constexpr int kNumBars = 16;
+    static constexpr int kNumBars = 18;
     static constexpr int kMisc = kBar + kNumBars * 8;  // tmem address, abort flag, tile info
     static constexpr int kBytes = kMisc + 64;
     static constexpr int kAlloc = kBytes + 1024;  // slack to align the base to 1024
+    static_assert(kAlloc <= 227 * 1024, "shared memory above the per-CTA limit");
 };
 
 // barrier indices
 enum Bar {
     kQFull = 0,
-    kKFull0 = 1,    // [2]
-    kKEmpty0 = 3,   // [2]
-    kVFull0 = 5,    // [2]
-    kVEmpty0 = 7,   // [2]
-    kSFull0 = 9,    // [2] per tile: S(j) in TMEM
-    kPFull0 = 11,   // [2] per tile: P(j) in TMEM (4 softmax warps arrive)
-    kODone0 = 13,   // [2] per tile: O += P(j) V(j) done
-    kDrain = 15,
+    kKFull0 = 1,    // [kKStages = 3]
+    kKEmpty0 = 4,   // [3]
+    kVFull0 = 7,    // [kVStages = 2]
+    kVEmpty0 = 9,   // [2]
+    kSFull0 = 11,   // [2] per tile: S(j) in TMEM
+    kPFull0 = 13,   // [2] per tile: P(j) in TMEM (4 softmax warps arrive)
+    kODone0 = 15,   // [2] per tile: O += P(j) V(j) done
+    kDrain = 17,
 };
 
 // Tiles of a sequence with n new tokens (the decode path takes n <= qmax), and
@@ -114,6 +122,24 @@ __device__ __forceinline__ float max3(float a, float b, float c) {
     asm("max.f32 %0, %1, %2, %3;\n" : "=f"(d) : "f"(a), "f"(b), "f"(c));
     return d;
 }
+
+// acc += (x0, x1) on the packed f32x2 adder (acc holds two partial sums).
+__device__ __forceinline__ void add2(uint64_t& acc, float x0, float x1) {
+    uint64_t x;
+    asm("mov.b64 %0, {%1, %2};\n" : "=l"(x) : "f"(x0), "f"(x1));
+    asm("add.rn.f32x2 %0, %0, %1;\n" : "+l"(acc) : "l"(x));
+}
+__device__ __forceinline__ float2 unpack2(uint64_t v) {
+    float2 r;
+    asm("mov.b64 {%0, %1}, %2;\n" : "=f"(r.x), "=f"(r.y) : "l"(v));
+    return r;
+}
+
+// One pair in PA_PREFILL_POLY_EVERY of the softmax exponentials is computed on
+// the FMA pipe (poly_exp2) instead of the special-function unit; 0: none.
+#ifndef PA_PREFILL_POLY_EVERY
+#define PA_PREFILL_POLY_EVERY 0
+#endif
 
 // (a0, a1) * (b, b) + (c, c) on the packed f32x2 FMA.
 __device__ __forceinline__ void fma2(float& y0, float& y1, float a0, float a1, float b, float c) {
@@ -246,19 +272,23 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t tmem = *s_tmem;
     bool ok = true;
 
-    if (warp == 0) {
-        // ================================================= TMA producer
+    if (warp == 0 || warp == kWarpV) {
+        // ========================================== TMA producers (K: warp 0, V: warp 10)
+        const bool is_v = warp == kWarpV;
         if (lane == 0) {
-            tc::prefetch_tmap(&tm_q);
-            tc::prefetch_tmap(&tm_k);
-            tc::prefetch_tmap(&tm_v);
-            const int nq = ntok[1] > 0 ? 2 : 1;
-            tc::mbar_arrive_expect_tx(bar(kQFull), nq * S::kHalves * 64 * 2 * G * tq_tokens);
-            for (int x = 0; x < nq; ++x)
+            if (!is_v) {
+                tc::prefetch_tmap(&tm_q);
+                tc::prefetch_tmap(&tm_k);
+                const int nq = ntok[1] > 0 ? 2 : 1;
+                tc::mbar_arrive_expect_tx(bar(kQFull), nq * S::kHalves * 64 * 2 * G * tq_tokens);
+                for (int x = 0; x < nq; ++x)
 #pragma unroll
-                for (int hf = 0; hf < S::kHalves; ++hf)
-                    tc::tma_load_3d(base + S::kQ0 + x * S::kTile + hf * kHalfBytes, &tm_q, bar(kQFull), hf * 64,
-                                    h * G, q0 + i0 + x * tq_tokens);
+                    for (int hf = 0; hf < S::kHalves; ++hf)
+                        tc::tma_load_3d(base + S::kQ0 + x * S::kTile + hf * kHalfBytes, &tm_q, bar(kQFull), hf * 64,
+                                        h * G, q0 + i0 + x * tq_tokens);
+            } else {
+                tc::prefetch_tmap(&tm_v);
+            }
         }
         const int32_t* bt = a.block_table + static_cast<int64_t>(b) * a.max_pages;
         // lane l holds the block-table entry of page (group * 32 + l); the next
@@ -270,6 +300,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         int cur_grp = load_group(0);
         int next_grp = load_group(1);
         const __nv_bfloat16* vc = reinterpret_cast<const __nv_bfloat16*>(a.v_cache);
+        const int stages = is_v ? kVStages : kKStages;
+        const int full0 = is_v ? kVFull0 : kKFull0, empty0 = is_v ? kVEmpty0 : kKEmpty0;
+        const uint32_t ring = base + (is_v ? S::kV0 : S::kK0);
+        const CUtensorMap* tm = is_v ? &tm_v : &tm_k;
         for (int kt = 0; kt < ntiles; ++kt) {
             const int slot = kt % kTilesPerGroup;
             if (slot == 0 && kt > 0) {
@@ -278,36 +312,21 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             const int p0 = kt * kPagesPerTile;
             const int np = min(kPagesPerTile, last_page - p0);
-            const int nv = max(0, min(np, full_pages - p0));  // V pages by TMA
+            // pages by TMA: all of K; V up to the one holding the sequence end
+            const int nt = is_v ? max(0, min(np, full_pages - p0)) : np;
             int page = __shfl_sync(0xffffffffu, cur_grp, (slot * kPagesPerTile + lane) & 31);
             if (lane < np && static_cast<uint32_t>(page) >= static_cast<uint64_t>(a.num_blocks)) {
                 flag_error(a.err, kDevBadBlock);
                 page = 0;
             }
-            // ---- K(kt)
-            const int kst = kt % kKStages;
-            if (kt >= kKStages && !warp_wait(bar(kKEmpty0 + kst), (kt / kKStages - 1) & 1, s_abort)) {
+            const int st = kt % stages;
+            if (kt >= stages && !warp_wait(bar(empty0 + st), (kt / stages - 1) & 1, s_abort)) {
                 ok = false;
                 break;
             }
-            const uint32_t sk = base + S::kK0 + kst * S::kTile;
-            if (lane == 0) tc::mbar_arrive_expect_tx(bar(kKFull0 + kst), np * S::kHalves * 2048);
-            __syncwarp();
-            if (lane < np) {
-#pragma unroll
-                for (int hf = 0; hf < S::kHalves; ++hf)
-                    tc::tma_load_4d(sk + hf * kHalfBytes + lane * 2048, &tm_k, bar(kKFull0 + kst), hf * 64, h, 0,
-                                    page);
-            }
-            // ---- V(kt)
-            const int vst = kt % kVStages;
-            if (kt >= kVStages && !warp_wait(bar(kVEmpty0 + vst), (kt / kVStages - 1) & 1, s_abort)) {
-                ok = false;
-                break;
-            }
-            const uint32_t sv = base + S::kV0 + vst * S::kTile;
-            if (nv < np) {
-                // The page holding the sequence end: plain loads, slots >= L as zeros.
+            const uint32_t sd = ring + st * S::kTile;
+            if (is_v && nt < np) {
+                // The V page holding the sequence end: plain loads, slots >= L as zeros.
                 const int pi = np - 1;
                 const int pg = __shfl_sync(0xffffffffu, page, pi);
                 for (int c = lane; c < kPage * (D / 8); c += 32) {
@@ -317,7 +336,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     if ((p0 + pi) * kPage + t < L)
                         val = *reinterpret_cast<const uint4*>(
                             vc + ((static_cast<int64_t>(pg) * kPage + t) * a.num_kv_heads + h) * D + ch * 8);
-                    const uint32_t dst = sv + (ch >> 3) * kHalfBytes + sw128(row, ch & 7);
+                    const uint32_t dst = sd + (ch >> 3) * kHalfBytes + sw128(row, ch & 7);
                     asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};\n" ::"r"(dst), "r"(val.x), "r"(val.y),
                                  "r"(val.z), "r"(val.w)
                                  : "memory");
@@ -325,13 +344,27 @@ __global__ void __launch_bounds__(kThreads, 1)
                 tc::fence_proxy_async_smem();
             }
             __syncwarp();
-            if (lane == 0) tc::mbar_arrive_expect_tx(bar(kVFull0 + vst), nv * S::kHalves * 2048);
+            if (lane == 0) tc::mbar_arrive_expect_tx(bar(full0 + st), nt * S::kHalves * 2048);
             __syncwarp();
-            if (lane < nv) {
+            if (lane < nt) {
 #pragma unroll
                 for (int hf = 0; hf < S::kHalves; ++hf)
-                    tc::tma_load_4d(sv + hf * kHalfBytes + lane * 2048, &tm_v, bar(kVFull0 + vst), hf * 64, h, 0,
-                                    page);
+                    tc::tma_load_4d(sd + hf * kHalfBytes + lane * 2048, tm, bar(full0 + st), hf * 64, h, 0, page);
+            }
+            // L2 prefetch of the pages kPrefetchTiles tiles ahead, so that their
+            // ring loads find them in L2 rather than in HBM.
+            if (kPrefetchTiles > 0 && kt + kPrefetchTiles < ntiles) {
+                const int kp = kt + kPrefetchTiles;
+                const int pp0 = kp * kPagesPerTile;
+                const int npp = min(kPagesPerTile, last_page - pp0);
+                const int sp = kp % kTilesPerGroup;
+                // tile kp's entries: in this group, or (kp / 4 > kt / 4) in the next
+                const int src = (kp / kTilesPerGroup == kt / kTilesPerGroup) ? cur_grp : next_grp;
+                const int ppage = __shfl_sync(0xffffffffu, src, (sp * kPagesPerTile + lane) & 31);
+                if (lane < npp && static_cast<uint32_t>(ppage) < static_cast<uint64_t>(a.num_blocks)) {
+#pragma unroll
+                    for (int hf = 0; hf < S::kHalves; ++hf) tc::tma_prefetch_4d(tm, hf * 64, h, 0, ppage);
+                }
             }
         }
         if (!ok && lane == 0) {
@@ -402,7 +435,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             tc::mbar_wait(bar(kDrain), 0, nullptr, kTimeoutNs);
         }
         __syncwarp();
-    } else {
+    } else if (warp >= 2 && warp < 10) {
         // ======================================================== softmax
         const int x = (warp - 2) >> 2;        // tile: warps 2-5 -> A, 6-9 -> B
         const int quarter = warp & 3;         // TMEM lanes 32 * (warp % 4) ..
@@ -415,7 +448,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int pos = valid ? prefix + i0 + x * tq_tokens + r / G : -1;  // causal limit of this row
         const float c = a.scale_log2;
         float m_used = -INFINITY;  // running max, log2 units
-        float lsum[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};  // independent partial sums
+        uint64_t lsum[4] = {0, 0, 0, 0};  // 8 independent partial sums, in f32x2 pairs (0 = +0.0f, +0.0f)
         for (int kt = 0; kt < nt; ++kt) {
             if (!warp_wait(bar(kSFull0 + x), kt & 1, s_abort)) {
                 ok = false;
@@ -468,7 +501,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                         tc::tmem_st32(o_addr + q * 32, o);
                     }
 #pragma unroll
-                    for (int e = 0; e < 8; ++e) lsum[e] *= alpha;
+                    for (int e = 0; e < 4; ++e) {
+                        const float2 v = unpack2(lsum[e]);
+                        asm("mov.b64 %0, {%1, %2};\n" : "=l"(lsum[e]) : "f"(v.x * alpha), "f"(v.y * alpha));
+                    }
                     if (need) m_used = mnew;
                 }
             }
@@ -484,9 +520,17 @@ __global__ void __launch_bounds__(kThreads, 1)
                 for (int e = 0; e < 32; ++e) {
                     float y0, y1;
                     fma2(y0, y1, __uint_as_float(sh[2 * e]), __uint_as_float(sh[2 * e + 1]), c, nmu);
-                    const float x0 = fast_exp2(y0), x1 = fast_exp2(y1);
+                    float x0, x1;
+                    if (PA_PREFILL_POLY_EVERY > 0 && e % (PA_PREFILL_POLY_EVERY > 0 ? PA_PREFILL_POLY_EVERY : 1) ==
+                                                         (PA_PREFILL_POLY_EVERY > 0 ? PA_PREFILL_POLY_EVERY : 1) - 1) {
+                        x0 = poly_exp2(y0);
+                        x1 = poly_exp2(y1);
+                    } else {
+                        x0 = fast_exp2(y0);
+                        x1 = fast_exp2(y1);
+                    }
                     pk[e] = pack_bf16(x0, x1);
-                    lsum[e & 7] += x0 + x1;
+                    add2(lsum[e & 3], x0, x1);
                 }
                 tc::tmem_st32(s_addr + col, pk);
             };
@@ -505,7 +549,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (ok && nt > 0) ok = warp_wait(bar(kODone0 + x), (nt - 1) & 1, s_abort);
         if (ok && nt > 0) {
             tc::tc_fence_after();
-            const float l = ((lsum[0] + lsum[1]) + (lsum[2] + lsum[3])) + ((lsum[4] + lsum[5]) + (lsum[6] + lsum[7]));
+            const float2 l0 = unpack2(lsum[0]), l1 = unpack2(lsum[1]), l2 = unpack2(lsum[2]), l3 = unpack2(lsum[3]);
+            const float l = ((l0.x + l0.y) + (l1.x + l1.y)) + ((l2.x + l2.y) + (l3.x + l3.y));
             const float inv = valid ? 1.f / l : 0.f;
             __nv_bfloat16* orow = out + (static_cast<int64_t>(q0 + i0 + x * tq_tokens + (valid ? r / G : 0)) *
                                              a.num_q_heads +

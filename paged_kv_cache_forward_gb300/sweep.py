@@ -165,8 +165,10 @@ def main(argv=None):
             del pools
             torch.cuda.empty_cache()
 
-    # table: (max_bound, max_seqs) cells, batch-major, so the first match is the
-    # smallest swept batch >= B and, within it, the smallest swept bound >= bound
+    # table: (max_bound, max_units) cells, batch-major, so the first match is the
+    # smallest swept batch >= B and, within it, the smallest swept bound >= bound;
+    # units = sequences x KV heads (x row groups), so other head counts map onto
+    # the Llama-shaped sweep by their parallelism
     entries = []
     for batch in batches:
         for bound in bounds:
@@ -193,14 +195,15 @@ def main(argv=None):
 def write_table(path, entries, last_batch, fallback, gpu_name, stamp):
     with open(path, "w") as f:
         f.write("// Keys per split and decode kernel variant, keyed on the context bound\n"
-                "// (max_pages * page_size) and the number of sequences:\n"
-                "// {max_bound, max_seqs, kv_chunk, decode_stages, decode_warps, decode_cluster}\n"
+                "// (max_pages * page_size) and the number of decode units:\n"
+                "// {max_bound, max_units, kv_chunk, decode_stages, decode_warps, decode_cluster}\n"
+                "// (units = sequences x KV heads x row groups)\n"
                 "// (cluster > 1: an even split over a cluster of that many CTAs).  The first\n"
                 "// entry that matches wins; the last entry is the fallback.  Written by\n"
                 f"// paged_kv_cache_forward_gb300/sweep.py on {gpu_name} ({stamp}).\n"
                 "static const LutEntry kSplitTable[] = {\n")
         for bound, batch, chunk, st, w, cl in entries:
-            mb = (1 << 30) if batch == last_batch else batch
+            mb = (1 << 30) if batch == last_batch else batch * HKV
             f.write(f"    {{{bound}, {mb}, {chunk or 16}, {st}, {w}, {cl}}},\n")
         f.write(f"    {{1 << 30, 1 << 30, {fallback[0] or 16}, {fallback[1]}, {fallback[2]}, {fallback[3]}}},\n}};\n")
 
