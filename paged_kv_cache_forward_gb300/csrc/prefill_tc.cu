@@ -98,7 +98,7 @@ enum Bar {
     kVEmpty0 = 9,   // [2]
     kSFull0 = 11,   // [2] per tile: S(j) in TMEM
     kPFull0 = 13,   // [2] per tile: P(j) in TMEM (4 softmax warps arrive)
-    kODone0 = 15,   // [2] per tile: O += P(j) V(j) done
+    kODone0 = 15,   // [2] per tile: the tile's last O += P V done (completes once)
     kDrain = 17,
 };
 
@@ -109,6 +109,8 @@ __device__ __forceinline__ int pairs_of(int n, int tq, int qmax) { return (tiles
 
 // Bounded wait by every lane of a warp; the result is made warp-uniform so that a
 // timeout can never leave some lanes at a warp-collective instruction alone.
+// (Polling from lane 0 alone and broadcasting was measured slower: 1096 -> 993
+// TFLOP/s on the varlen prefill.)
 __device__ __forceinline__ bool warp_wait(uint32_t addr, uint32_t parity, const volatile int* abort) {
     const bool ok = tc::mbar_wait(addr, parity, abort, kTimeoutNs);
     return __all_sync(0xffffffffu, ok);
@@ -149,6 +151,25 @@ __device__ __forceinline__ void fma2(float& y0, float& y1, float a0, float a1, f
     asm("mov.b64 %0, {%1, %1};\n" : "=l"(cc) : "f"(c));
     asm("fma.rn.f32x2 %0, %1, %2, %3;\n" : "=l"(y) : "l"(a), "l"(bb), "l"(cc));
     asm("mov.b64 {%0, %1}, %2;\n" : "=f"(y0), "=f"(y1) : "l"(y));
+}
+
+// One S tile: D / 16 MMAs of K = 16 (the K steps walk the two 64-column halves
+// of Q and K), accumulating from the second on.
+template <int D>
+__device__ __forceinline__ void issue_s_group(uint32_t d, uint64_t da, uint64_t db, uint32_t idesc) {
+#pragma unroll
+    for (int ks = 0; ks < D / 16; ++ks) {
+        const uint64_t off = static_cast<uint64_t>((ks >> 2) * kHalfBytes + (ks & 3) * 32) >> 4;
+        tc::mma_bf16(d, da + off, db + off, idesc, ks > 0 ? 1u : 0u);
+    }
+}
+// One P V step over the npj pages of a KV tile: A = P from TMEM (8 columns per
+// 16 keys), B = V (one page of 16 keys per MMA, 2 KiB apart).
+__device__ __forceinline__ void issue_pv_group(uint32_t d, uint32_t pa, uint64_t db, uint32_t idesc, int npj,
+                                               bool first) {
+#pragma unroll
+    for (int ks = 0; ks < kPagesPerTile; ++ks)
+        if (ks < npj) tc::mma_bf16_tmem_a(d, pa + ks * 8, db + ks * (2048 >> 4), idesc, (!first || ks > 0) ? 1u : 0u);
 }
 
 template <int D>
@@ -376,56 +397,66 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (lane == 0) {
             constexpr uint32_t kIdQK = tc::idesc_bf16_f32(kM, kKeys, false, false);
             constexpr uint32_t kIdPV = tc::idesc_bf16_f32(kM, D, false, true);
-            auto issue_s = [&](int x, int j) {  // S_x(j) = Q_x K(j)^T, K(j) already resident
-                const uint32_t sk = base + S::kK0 + (j % kKStages) * S::kTile;
-                const uint32_t sq = base + S::kQ0 + x * S::kTile;
-#pragma unroll
-                for (int ks = 0; ks < D / 16; ++ks) {
-                    const uint32_t off = (ks >> 2) * kHalfBytes + (ks & 3) * 32;
-                    tc::mma_bf16(tmem + tmem_s(x), tc::desc_sw128(sq + off, 16, 1024),
-                                 tc::desc_sw128(sk + off, 16, 1024), kIdQK, ks > 0 ? 1u : 0u);
-                }
-                tc::mma_commit(bar(kSFull0 + x));
-            };
-            auto issue_pv = [&](int x, int j) -> bool {  // O_x += P_x(j) V(j), V(j) already resident
-                if (!tc::mbar_wait(bar(kPFull0 + x), j & 1, s_abort, kTimeoutNs)) return false;
-                tc::tc_fence_after();
-                const int npj = min(kPagesPerTile, last_page - j * kPagesPerTile);
-                const uint32_t sv = base + S::kV0 + (j % kVStages) * S::kTile;
-                for (int ks = 0; ks < npj; ++ks) {  // one 16-key step per page; P: 8 columns per step
-                    const uint64_t bd = tc::desc_sw128(sv + ks * 2048, kHalfBytes, 1024);
-                    tc::mma_bf16_tmem_a(tmem + tmem_o(x), tmem + tmem_s(x) + 64 + ks * 8, bd, kIdPV,
-                                        (j > 0 || ks > 0) ? 1u : 0u);
-                }
-                tc::mma_commit(bar(kODone0 + x));
-                return true;
-            };
+            // Shared-memory descriptors, computed once: an MMA only adds a
+            // constant to the start-address field (16-byte units; every operand
+            // lies below 256 KiB, so the 14-bit field never carries).  Issuing
+            // is the bottleneck of this thread (a tcgen05.mma costs tens of
+            // cycles to issue), so nothing else is computed per MMA and the
+            // groups are plain inline functions of register values.
+            const uint64_t dq0 = tc::desc_sw128(base + S::kQ0, 16, 1024);
+            const uint64_t dk0 = tc::desc_sw128(base + S::kK0, 16, 1024);
+            const uint64_t dv0 = tc::desc_sw128(base + S::kV0, kHalfBytes, 1024);
+            constexpr uint64_t kTileU = S::kTile >> 4;
+            const uint32_t d_s0 = tmem + tmem_s(0), d_s1 = tmem + tmem_s(1);
+            const uint32_t d_o0 = tmem + tmem_o(0), d_o1 = tmem + tmem_o(1);
+#define PA_ISSUE_S(x, jj)                                                                                     \
+    do {                                                                                                      \
+        issue_s_group<D>((x) ? d_s1 : d_s0, dq0 + ((x) ? kTileU : 0), dk0 + ((jj) % kKStages) * kTileU, kIdQK); \
+        tc::mma_commit(bar(kSFull0 + (x)));                                                                   \
+    } while (0)
+// (the caller has waited for P_x(jj))
+#define PA_ISSUE_PV(x, jj)                                                                                  \
+    do {                                                                                                    \
+        tc::tc_fence_after();                                                                               \
+        issue_pv_group((x) ? d_o1 : d_o0, ((x) ? d_s1 : d_s0) + 64, dv0 + ((jj) % kVStages) * kTileU, kIdPV, \
+                       min(kPagesPerTile, last_page - (jj) * kPagesPerTile), (jj) == 0);                    \
+        if ((jj) == ((x) ? nkv1 : nkv0) - 1) tc::mma_commit(bar(kODone0 + (x)));                            \
+    } while (0)
             ok = tc::mbar_wait(bar(kQFull), 0, s_abort, kTimeoutNs);
             if (ok && ntiles > 0) ok = tc::mbar_wait(bar(kKFull0), 0, s_abort, kTimeoutNs);
+            const int nkv0 = nkv[0], nkv1 = nkv[1];
             if (ok && ntiles > 0) {
                 tc::tc_fence_after();
-                if (nkv[0] > 0) issue_s(0, 0);
-                if (nkv[1] > 0) issue_s(1, 0);
+                if (nkv0 > 0) PA_ISSUE_S(0, 0);
+                if (nkv1 > 0) PA_ISSUE_S(1, 0);
                 tc::mma_commit(bar(kKEmpty0));
             }
             for (int j = 0; j < ntiles && ok; ++j) {
-                const bool nxt0 = j + 1 < nkv[0], nxt1 = j + 1 < nkv[1];
+                const bool nxt0 = j + 1 < nkv0, nxt1 = j + 1 < nkv1;
                 ok = tc::mbar_wait(bar(kVFull0 + j % kVStages), (j / kVStages) & 1, s_abort, kTimeoutNs);
                 if (!ok) break;
                 tc::tc_fence_after();
-                if (j < nkv[0] && !(ok = issue_pv(0, j))) break;
+                if (j < nkv0) {
+                    if (!(ok = tc::mbar_wait(bar(kPFull0), j & 1, s_abort, kTimeoutNs))) break;
+                    PA_ISSUE_PV(0, j);
+                }
                 if (nxt0 || nxt1) {
                     const int js = j + 1;
                     ok = tc::mbar_wait(bar(kKFull0 + js % kKStages), (js / kKStages) & 1, s_abort, kTimeoutNs);
                     if (!ok) break;
                     tc::tc_fence_after();
                 }
-                if (nxt0) issue_s(0, j + 1);
-                if (j < nkv[1] && !(ok = issue_pv(1, j))) break;
+                if (nxt0) PA_ISSUE_S(0, j + 1);
+                if (j < nkv1) {
+                    if (!(ok = tc::mbar_wait(bar(kPFull0 + 1), j & 1, s_abort, kTimeoutNs))) break;
+                    PA_ISSUE_PV(1, j);
+                }
                 tc::mma_commit(bar(kVEmpty0 + j % kVStages));
-                if (nxt1) issue_s(1, j + 1);
+                if (nxt1) PA_ISSUE_S(1, j + 1);
                 if (nxt0 || nxt1) tc::mma_commit(bar(kKEmpty0 + (j + 1) % kKStages));
             }
+#undef PA_ISSUE_S
+#undef PA_ISSUE_PV
             if (!ok) {
                 *s_abort = 1;
                 flag_error(a.err, kDevWaitTimeout);
@@ -485,12 +516,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             } else {
                 const bool need = mnew > m_used + 8.f;
                 if (__any_sync(0xffffffffu, need)) {
-                    // O holds tiles < kt once P V(kt-1) is done
-                    if (!warp_wait(bar(kODone0 + x), (kt - 1) & 1, s_abort)) {
-                        ok = false;
-                        break;
-                    }
-                    tc::tc_fence_after();
+                    // O holds tiles < kt: P V(kt-1) was issued before S(kt), and
+                    // the commit this warp waited for to read S(kt) completes only
+                    // after every earlier MMA of the issuing thread.
                     const float alpha = need ? fast_exp2(m_used - mnew) : 1.f;
 #pragma unroll
                     for (int q = 0; q < D / 32; ++q) {
@@ -546,7 +574,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             __syncwarp();
             if (lane == 0) tc::mbar_arrive(bar(kPFull0 + x));
         }
-        if (ok && nt > 0) ok = warp_wait(bar(kODone0 + x), (nt - 1) & 1, s_abort);
+        if (ok && nt > 0) ok = warp_wait(bar(kODone0 + x), 0, s_abort);
         if (ok && nt > 0) {
             tc::tc_fence_after();
             const float2 l0 = unpack2(lsum[0]), l1 = unpack2(lsum[1]), l2 = unpack2(lsum[2]), l3 = unpack2(lsum[3]);

@@ -122,7 +122,10 @@ __host__ __device__ constexpr uint32_t idesc_bf16_f32(int M, int N, bool a_mn, b
            (static_cast<uint32_t>(N >> 3) << 17) | (static_cast<uint32_t>(M >> 4) << 24);
 }
 
-// D(tmem) (+)= A(smem) * B(smem), issued by one thread.
+// D(tmem) (+)= A(smem) * B(smem), issued by one thread.  (No memory clobber:
+// the MMA reads shared memory asynchronously, ordered by the mbarrier waits and
+// the tcgen05 fences around it, not by this statement; asm volatile keeps the
+// order among the tcgen05 statements.)
 __device__ __forceinline__ void mma_bf16(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
                                          uint32_t accumulate) {
     asm volatile(
@@ -131,8 +134,7 @@ __device__ __forceinline__ void mma_bf16(uint32_t d_tmem, uint64_t a_desc, uint6
         "setp.ne.b32 p, %4, 0;\n"
         "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n"
         "}\n" ::"r"(d_tmem),
-        "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
-        : "memory");
+        "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate));
 }
 // D(tmem) (+)= A(tmem) * B(smem): A is read from TMEM (row i in lane i, two
 // 16-bit elements per 32-bit column, K along the columns), issued by one thread.
@@ -144,8 +146,7 @@ __device__ __forceinline__ void mma_bf16_tmem_a(uint32_t d_tmem, uint32_t a_tmem
         "setp.ne.b32 p, %4, 0;\n"
         "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n"
         "}\n" ::"r"(d_tmem),
-        "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
-        : "memory");
+        "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate));
 }
 // Arrives once on mbar when every tcgen05 operation this thread issued so far is done.
 __device__ __forceinline__ void mma_commit(uint32_t mbar) {
