@@ -5,7 +5,8 @@ right", third item) replaces run-time autotuning by offline micro-benchmarks
 distilled into a small decision tree keyed on GPU, sequence length and batch.
 This is that step for GB300: for every (context bound, batch size) cell of a
 grid it times pa_forward on Llama-3.1-8B-shaped decode batches (32 query heads,
-8 KV heads, head_dim 128, every sequence at the context bound) for a set of
+8 KV heads, head_dim 128; one sequence at the context bound, or a batch with
+lengths uniform in [bound/16, bound]) for a set of
 (split size, decode kernel variant) pairs -- a variant is the warps per CTA
 and the pipeline depth per warp -- and keeps the fastest.  The result is written as a table that the
 library compiles in; nothing is tuned at run time.
@@ -93,9 +94,21 @@ def time_shape(bound, batch, chunk, pools, stream, warps=0, stages=0, cluster=0,
     return e0.elapsed_time(e1) * 1e3 / (reps * M)  # us per step
 
 
+def seq_lengths(bound, batch):
+    """One sequence at the bound; a batch has lengths uniform in [bound/16, bound]
+    (as a serving batch mixes lengths; with every sequence at the bound the
+    table would favour unsplit CTAs, whose longest sequences then set the time)."""
+    if batch == 1:
+        return [bound]
+    g = torch.Generator().manual_seed(bound * 1000 + batch)
+    lo = max(1, bound // 16)
+    return torch.randint(lo, bound + 1, (batch,), generator=g).tolist()
+
+
 def make_pools(bound, batch, l2_bytes, gen):
     pages = bound // PAGE
-    kv = batch * bound * HKV * D * 2 * 2
+    lens = seq_lengths(bound, batch)
+    kv = sum(lens) * HKV * D * 2 * 2
     R = 1 if kv > 3 * l2_bytes else int(math.ceil(3 * l2_bytes / kv)) + 1
     nb = batch * pages + 1
     dev = "cuda"
@@ -106,7 +119,7 @@ def make_pools(bound, batch, l2_bytes, gen):
         vs.append(torch.randn(nb, PAGE, HKV, D, device=dev, generator=gen).to(torch.bfloat16))
     perm = torch.randperm(nb, device=dev, generator=gen).to(torch.int32)
     bt = perm[: batch * pages].reshape(batch, pages).contiguous()
-    sl = torch.full((batch,), bound, dtype=torch.int32, device=dev)
+    sl = torch.tensor(lens, dtype=torch.int32, device=dev)
     qsl = torch.arange(batch + 1, dtype=torch.int32, device=dev)
     out = torch.empty_like(q)
     return (q, ks, vs, bt, sl, qsl, out), kv
@@ -182,7 +195,8 @@ def main(argv=None):
     with open(args.log, "w") as f:
         f.write(f"# Split-size sweep on {props.name} ({stamp})\n\n"
                 f"Command: `python -m paged_kv_cache_forward_gb300.sweep {' '.join(argv or sys.argv[1:])}`\n\n"
-                "Llama-3.1-8B-shaped decode (Hq 32, Hkv 8, D 128), every sequence at the bound,\n"
+                "Llama-3.1-8B-shaped decode (Hq 32, Hkv 8, D 128); batch 1 at the bound, larger batches\n"
+                "with lengths uniform in [bound/16, bound] (seeded per cell),\n"
                 "graph-replayed pa_forward steps rotating over KV pool copies larger than 3 x L2.\n"
                 "GB/s = KV bytes per step / step time.\n\n"
                 "Split `cN`: the keys split evenly over a thread-block cluster of N CTAs.\n\n"
