@@ -349,6 +349,7 @@ def run_ours(args):
     vs = [d.v_cache] + [d.v_cache.clone() for _ in range(R - 1)]
     out = torch.empty_like(d.q)
     stream = torch.cuda.Stream(device=dev)
+    torch.cuda.synchronize(dev)  # inputs and pool copies were made on the default stream
     plan = pa.plan_for(d.q, d.k_cache, d.block_table, d.seq_lens, kv_chunk=args.kv_chunk)
     pa.prepare(d.q, d.k_cache, d.block_table, d.seq_lens, kv_chunk=args.kv_chunk, stream=stream)
     G = batch.num_q_heads // batch.num_kv_heads
@@ -615,6 +616,7 @@ def run_layers(args):
     qs = [d.q] + [torch.randn(d.q.shape, generator=gen, device=dev).to(torch.bfloat16) for _ in range(L - 1)]
     outs = [torch.empty_like(d.q) for _ in range(L)]
     stream = torch.cuda.Stream(device=dev)
+    torch.cuda.synchronize(dev)  # inputs and caches were made on the default stream
     plan = pa.plan_for(d.q, d.k_cache, d.block_table, d.seq_lens, kv_chunk=args.kv_chunk)
     pa.prepare(d.q, d.k_cache, d.block_table, d.seq_lens, kv_chunk=args.kv_chunk, stream=stream)
 

@@ -155,6 +155,9 @@ def main(argv=None):
             if batch * bound * HKV * D * 4 > MAX_KV_BYTES:
                 continue
             pools, kv = make_pools(bound, batch, l2, gen)
+            # the pools were filled on the default stream; the timing runs on
+            # `stream`, which does not order itself after it
+            torch.cuda.synchronize()
             res = []
             for w, st in variants:
                 # (split size, 1): splits merged through the workspace;

@@ -365,6 +365,7 @@ def test_workspace_reuse_across_growing_batches():
         b = W.make_batch([1] * B, lens, 32, 8, 128, seed=200 + B, max_pages=200)
         d = b.to("cuda")
         out = torch.full_like(d.q, float("nan"))
+        torch.cuda.synchronize()  # the inputs were made on the default stream
         with torch.cuda.stream(s):
             pa.forward(d.q, d.k_cache, d.v_cache, d.block_table, d.seq_lens, d.query_start_loc, out,
                        scale=b.scale, kv_chunk=256)
