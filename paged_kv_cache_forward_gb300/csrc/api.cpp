@@ -69,8 +69,8 @@ pa_status check_dims(const pa_dims* d) {
     if (d->num_q_heads % d->num_kv_heads != 0)
         return fail(PA_ERR_INVALID_ARG, "num_q_heads (%d) is not a multiple of num_kv_heads (%d)", d->num_q_heads,
                     d->num_kv_heads);
-    if (d->head_dim != 64 && d->head_dim != 128)
-        return fail(PA_ERR_UNSUPPORTED, "head_dim %d not built (64, 128)", d->head_dim);
+    if (d->head_dim != 64 && d->head_dim != 128 && d->head_dim != 256)
+        return fail(PA_ERR_UNSUPPORTED, "head_dim %d not built (64, 128, 256)", d->head_dim);
     if (d->page_size != 16) return fail(PA_ERR_UNSUPPORTED, "page_size %d not built (16)", d->page_size);
     if (d->num_q_heads / d->num_kv_heads > 64)
         return fail(PA_ERR_UNSUPPORTED, "more than 64 query heads per KV head");
@@ -106,14 +106,20 @@ pa_status make_plan(const pa_dims* d, const pa_options* o, Plan* p) {
     // the table's variant, unless the caller forces one (fully or in part)
     int32_t stages = te.decode_stages ? te.decode_stages : kDefaultDecodeStages;
     int32_t warps = te.decode_warps ? te.decode_warps : kDefaultDecodeWarps;
+    if (d->head_dim == 256 && !pa::decode_variant_supported(256, warps, stages)) {
+        // the table was swept at head_dim 128; the nearest variant built for 256
+        warps = 4;
+        stages = stages >= 3 ? 3 : 2;
+    }
     if (o && (o->decode_stages || o->decode_warps)) {
         stages = o->decode_stages ? o->decode_stages : kDefaultDecodeStages;
         warps = o->decode_warps ? o->decode_warps : kDefaultDecodeWarps;
     }
-    if (!pa::decode_variant_supported(warps, stages))
+    if (!pa::decode_variant_supported(d->head_dim, warps, stages))
         return fail(PA_ERR_INVALID_ARG,
-                    "decode variant (%d warps, %d stages) is not one of (4, 2..4), (8, 2..3), (12, 2)", warps,
-                    stages);
+                    "decode variant (%d warps, %d stages) is not built for head_dim %d (128 and 64: (4, 2..4), "
+                    "(8, 2..3), (12, 2); 256: (4, 2..3))",
+                    warps, stages, d->head_dim);
     // cluster mode: the table's, unless the caller forces a split size or a cluster
     int32_t cluster = te.decode_cluster > 1 ? te.decode_cluster : 1;
     if (o && (o->kv_chunk || o->decode_cluster)) cluster = o->decode_cluster > 1 ? o->decode_cluster : 1;

@@ -163,9 +163,11 @@ __device__ __forceinline__ float ld_peer(const float* local, uint32_t peer) {
     return v;
 }
 
-// 4-warp CTAs are sized to share an SM three at a time (at most 170 registers).
+// 4-warp CTAs are sized to share an SM three at a time (at most 170 registers),
+// except at D = 256, whose O fragments alone take 128 registers a thread.
 template <int D, int kWarps, int kStages>
-__global__ void __launch_bounds__(kWarps * 32, kWarps == 4 ? 3 : 1) decode_splitkv_kernel(const Args a) {
+__global__ void __launch_bounds__(kWarps * 32, (kWarps == 4 && D <= 128) ? 3 : 1)
+    decode_splitkv_kernel(const Args a) {
     using Tile = DecodeTile<D, kWarps, kStages>;
     extern __shared__ __align__(128) uint8_t smem[];
     const int warp = threadIdx.x >> 5;
@@ -557,6 +559,13 @@ cudaError_t launch_decode_d(const Args& a, cudaStream_t stream) {
 
 template <int D>
 cudaError_t launch_decode_variant(const Args& a, cudaStream_t stream) {
+    if (D == 256) {  // a 4-warp CTA holds 64 (2 stages) or 96 KiB (3) of pages per warp pair
+        switch (a.decode_warps * 16 + a.decode_stages) {
+            case 4 * 16 + 2: return launch_decode_d<256, 4, 2>(a, stream);
+            case 4 * 16 + 3: return launch_decode_d<256, 4, 3>(a, stream);
+            default: return cudaErrorInvalidValue;
+        }
+    }
     switch (a.decode_warps * 16 + a.decode_stages) {
         case 4 * 16 + 2: return launch_decode_d<D, 4, 2>(a, stream);
         case 4 * 16 + 3: return launch_decode_d<D, 4, 3>(a, stream);
@@ -570,7 +579,8 @@ cudaError_t launch_decode_variant(const Args& a, cudaStream_t stream) {
 
 }  // namespace
 
-bool decode_variant_supported(int warps, int stages) {
+bool decode_variant_supported(int head_dim, int warps, int stages) {
+    if (head_dim == 256) return warps == 4 && (stages == 2 || stages == 3);
     return (warps == 4 && stages >= 2 && stages <= 4) || (warps == 8 && (stages == 2 || stages == 3)) ||
            (warps == 12 && stages == 2);
 }
@@ -583,6 +593,7 @@ cudaError_t launch_decode(const Args& a, cudaStream_t stream) {
     switch (a.head_dim) {
         case 64: return launch_decode_variant<64>(a, stream);
         case 128: return launch_decode_variant<128>(a, stream);
+        case 256: return launch_decode_variant<256>(a, stream);
         default: return cudaErrorInvalidValue;
     }
 }

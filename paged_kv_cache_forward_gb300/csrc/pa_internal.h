@@ -115,8 +115,8 @@ cudaError_t launch_kernel(void (*kernel)(KArgs...), unsigned grid, unsigned bloc
 void set_last_error(const char* msg);
 
 // (warps per CTA, pipeline depth) pairs the decode kernel is built for:
-// (4, 2..4), (8, 2..3), (12, 2).
-bool decode_variant_supported(int warps, int stages);
+// (4, 2..4), (8, 2..3), (12, 2); at head_dim 256 only (4, 2..3).
+bool decode_variant_supported(int head_dim, int warps, int stages);
 
 // Static grid sizes (functions of shapes only), shared with the planner.
 int64_t decode_ctas(const Args& a);

@@ -66,7 +66,18 @@ constexpr uint32_t kTmemCols = 512;
 // TMEM columns of tile x: S at 128 x (P over its last 64 columns), O at 256 + 128 x.
 __device__ __forceinline__ uint32_t tmem_s(int x) { return x ? 128u : 0u; }
 __device__ __forceinline__ uint32_t tmem_o(int x) { return x ? 384u : 256u; }
-constexpr int kKStages = 3, kVStages = 2;
+// Query tiles per CTA and ring depths.  At D <= 128 a CTA holds a pair of tiles
+// (S and O of both in the 512 TMEM columns) with a 3-stage K and a 2-stage V
+// ring; at D = 256 one tile's O alone takes 256 columns, so a CTA holds one tile,
+// and a 64 KiB K or V tile leaves room for single-stage rings (K(j+1) loads
+// during the softmax and P V of tile j, V(j+1) during S(j+1) and its softmax).
+template <int D>
+struct Cfg {
+    static constexpr int kTiles = D <= 128 ? 2 : 1;
+    static constexpr int kKStages = D <= 128 ? 3 : 1;
+    static constexpr int kVStages = D <= 128 ? 2 : 1;
+};
+constexpr int kMaxKStages = 3, kMaxVStages = 2;  // barrier slots
 constexpr int kTilesPerGroup = 4;  // block-table prefetch: 4 tiles x 8 pages = one entry per lane
 #ifndef PA_PREFILL_L2_PREFETCH
 #define PA_PREFILL_L2_PREFETCH 2
@@ -79,9 +90,9 @@ struct Smem {
     static constexpr int kHalves = D / 64;
     static constexpr int kTile = kHalves * kHalfBytes;  // one Q, K or V tile (128 rows x D)
     static constexpr int kQ0 = 0;                       // Q_A, then Q_B
-    static constexpr int kK0 = kQ0 + 2 * kTile;
-    static constexpr int kV0 = kK0 + kKStages * kTile;
-    static constexpr int kBar = kV0 + kVStages * kTile;
+    static constexpr int kK0 = kQ0 + Cfg<D>::kTiles * kTile;
+    static constexpr int kV0 = kK0 + Cfg<D>::kKStages * kTile;
+    static constexpr int kBar = kV0 + Cfg<D>::kVStages * kTile;
     static constexpr int kNumBars = 18;
     static constexpr int kMisc = kBar + kNumBars * 8;  // tmem address, abort flag, tile info
     static constexpr int kBytes = kMisc + 64;
@@ -92,9 +103,9 @@ struct Smem {
 // barrier indices
 enum Bar {
     kQFull = 0,
-    kKFull0 = 1,    // [kKStages = 3]
+    kKFull0 = 1,    // [kMaxKStages = 3]
     kKEmpty0 = 4,   // [3]
-    kVFull0 = 7,    // [kVStages = 2]
+    kVFull0 = 7,    // [kMaxVStages = 2]
     kVEmpty0 = 9,   // [2]
     kSFull0 = 11,   // [2] per tile: S(j) in TMEM
     kPFull0 = 13,   // [2] per tile: P(j) in TMEM (4 softmax warps arrive)
@@ -105,7 +116,9 @@ enum Bar {
 // Tiles of a sequence with n new tokens (the decode path takes n <= qmax), and
 // the CTAs (pairs of tiles) they need.
 __device__ __forceinline__ int tiles_of(int n, int tq, int qmax) { return n > qmax ? (n + tq - 1) / tq : 0; }
-__device__ __forceinline__ int pairs_of(int n, int tq, int qmax) { return (tiles_of(n, tq, qmax) + 1) >> 1; }
+__device__ __forceinline__ int ctas_of(int n, int tq, int qmax, int tiles_per_cta) {
+    return (tiles_of(n, tq, qmax) + tiles_per_cta - 1) / tiles_per_cta;
+}
 
 // Bounded wait by every lane of a warp; the result is made warp-uniform so that a
 // timeout can never leave some lanes at a warp-collective instruction alone.
@@ -177,6 +190,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                       const __grid_constant__ CUtensorMap tm_v, const Args a, int tq_tokens, int pairs_bound) {
     using S = Smem<D>;
+    constexpr int kTiles = Cfg<D>::kTiles, kKStages = Cfg<D>::kKStages, kVStages = Cfg<D>::kVStages;
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = smem_u32(smem_raw);
     const uint32_t base = (raw + 1023u) & ~1023u;
@@ -197,7 +211,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int b0 = 0; b0 < a.num_seqs && found_b < 0; b0 += 32) {
             const int b = b0 + lane;
             const int cnt =
-                b < a.num_seqs ? pairs_of(a.query_start_loc[b + 1] - a.query_start_loc[b], tq_tokens, a.decode_max_q)
+                b < a.num_seqs ? ctas_of(a.query_start_loc[b + 1] - a.query_start_loc[b], tq_tokens, a.decode_max_q,
+                                         kTiles)
                                : 0;
             int inc = cnt;
 #pragma unroll
@@ -239,8 +254,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         L = cap;
     }
     const int G = a.group;
-    const int i0 = p_in_seq * 2 * tq_tokens;       // first new token of tile A
-    const int ntok_pair = min(2 * tq_tokens, n - i0);
+    const int i0 = p_in_seq * kTiles * tq_tokens;  // first new token of tile A
+    const int ntok_pair = min(kTiles * tq_tokens, n - i0);
     const int prefix = L - n;
     __nv_bfloat16* const out = reinterpret_cast<__nv_bfloat16*>(a.out);
     if (prefix < 0) {
@@ -256,7 +271,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     int ntok[2], nkv[2];
 #pragma unroll
     for (int x = 0; x < 2; ++x) {
-        ntok[x] = max(0, min(tq_tokens, n - (i0 + x * tq_tokens)));
+        ntok[x] = x < kTiles ? max(0, min(tq_tokens, n - (i0 + x * tq_tokens))) : 0;
         nkv[x] = ntok[x] > 0 ? (prefix + i0 + x * tq_tokens + ntok[x] + kKeys - 1) / kKeys : 0;
     }
     const int ntiles = max(nkv[0], nkv[1]);
@@ -267,11 +282,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ---- barriers and TMEM
     if (threadIdx.x == 0) {
         tc::mbar_init(bar(kQFull), 1);
-        for (int i = 0; i < kKStages; ++i) {
+        for (int i = 0; i < kMaxKStages; ++i) {
             tc::mbar_init(bar(kKFull0 + i), 1);
             tc::mbar_init(bar(kKEmpty0 + i), 1);
         }
-        for (int i = 0; i < kVStages; ++i) {
+        for (int i = 0; i < kMaxVStages; ++i) {
             tc::mbar_init(bar(kVFull0 + i), 1);
             tc::mbar_init(bar(kVEmpty0 + i), 1);
         }
@@ -618,12 +633,14 @@ __global__ void __launch_bounds__(kThreads, 1)
 // --------------------------------------------------------------- host side
 int tokens_per_tile(int group) { return group <= kM ? kM / group : 0; }
 
-// Upper bound on the pairs of tiles of any batch with these shapes: sum over
-// sequences of ceil(ceil(n_b / TQ) / 2) <= T / (2 TQ) + B.
+// Upper bound on the CTAs (tile pairs, or single tiles at D = 256) of any batch
+// with these shapes: sum over sequences of ceil(ceil(n_b / TQ) / k) =
+// sum of ceil(n_b / (k TQ)) <= T / (k TQ) + B, with k tiles per CTA.
 int pairs_bound(const Args& a) {
     const int tq = tokens_per_tile(a.group);
     if (tq == 0) return 0;
-    return static_cast<int>(a.num_tokens / (2 * tq) + a.num_seqs);
+    const int per_cta = a.head_dim <= 128 ? 2 : 1;  // Cfg<D>::kTiles
+    return static_cast<int>(a.num_tokens / (per_cta * tq) + a.num_seqs);
 }
 
 template <int D>
@@ -661,6 +678,7 @@ cudaError_t launch_prefill(const Args& a, cudaStream_t stream) {
     switch (a.head_dim) {
         case 64: return launch_d<64>(a, stream);
         case 128: return launch_d<128>(a, stream);
+        case 256: return launch_d<256>(a, stream);
         default: return cudaErrorInvalidValue;
     }
 }

@@ -73,6 +73,7 @@ def test_plan_row_groups(lib):
 
 @pytest.mark.parametrize("kw,status", [
     (dict(head_dim=96), B.PA_ERR_UNSUPPORTED),
+    (dict(head_dim=512), B.PA_ERR_UNSUPPORTED),
     (dict(page_size=32), B.PA_ERR_UNSUPPORTED),
     (dict(num_q_heads=30), B.PA_ERR_INVALID_ARG),
     (dict(num_kv_heads=0), B.PA_ERR_INVALID_ARG),
@@ -104,6 +105,17 @@ def test_decode_variant_option(lib):
         with pytest.raises(B.PagedAttnError) as e:
             B.plan(llama_dims(), decode_stages=st, decode_warps=w)
         assert e.value.status == B.PA_ERR_INVALID_ARG
+
+
+def test_head_dim_256_plan(lib):
+    p = B.plan(llama_dims(head_dim=256))
+    assert (p["decode_warps"], p["decode_stages"]) in [(4, 2), (4, 3)]  # table variant mapped to a D=256 one
+    # static prefill grid: T / (tiles per CTA x 32 tokens) + B CTAs per KV head
+    assert B.plan(llama_dims(head_dim=256, num_tokens=64))["prefill_ctas"] == (64 // 32 + 1) * 8  # one tile
+    assert B.plan(llama_dims(head_dim=128, num_tokens=64))["prefill_ctas"] == (64 // 64 + 1) * 8  # a pair
+    with pytest.raises(B.PagedAttnError) as e:
+        B.plan(llama_dims(head_dim=256), decode_warps=8, decode_stages=3)
+    assert e.value.status == B.PA_ERR_INVALID_ARG
 
 
 def test_decode_cluster_option(lib):

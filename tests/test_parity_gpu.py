@@ -90,7 +90,7 @@ def test_mixed_small_full():
 
 
 @pytest.mark.parametrize("Hq,Hkv,D", [(4, 1, 64), (8, 8, 128), (16, 2, 64), (32, 1, 128), (12, 4, 128),
-                                      (64, 2, 64)])
+                                      (64, 2, 64), (32, 8, 256), (16, 2, 256), (8, 8, 256)])
 def test_head_shapes(Hq, Hkv, D):
     q_lens = [1, 9, 1, 33]
     seq_lens = [333, 9, 17, 50]
@@ -152,6 +152,27 @@ def test_decode_cluster_spikes_bit_exact():
         got = run(b, decode_cluster=cluster)
         bad = (got.view(torch.int16) != want.view(torch.int16)).any(-1)
         assert not bad.any(), (cluster, torch.nonzero(bad)[:5].tolist())
+
+
+def test_head_dim_256():
+    """D = 256: one query tile per prefill CTA (its O takes 256 TMEM columns),
+    single-stage K/V rings, P V with N = 256; the 4-warp decode variants.  Several
+    KV tiles, a ragged tail, a sequence end mid-page, multi-token decode rows."""
+    b = W.make_batch([200, 1, 130, 2, 1], [700, 1500, 130, 333, 17], 32, 8, 256, seed=256, max_pages=100)
+    ref = oracle.batch_attention(b)
+    assert_close(run(b), ref, "D 256")
+    for st in (2, 3):
+        assert_close(run(b, decode_stages=st, decode_warps=4), ref, f"D 256 4x{st}")
+    assert_close(run(b, decode_cluster=4), ref, "D 256 cluster 4")
+    assert_close(run(b, kv_chunk=64), ref, "D 256 64-key splits")
+
+
+def test_head_dim_256_spikes_bit_exact():
+    b, exp = W.spike_batch([1, 37, 2, 130], [5000, 300, 90, 130], 16, 4, 256, seed=28, max_pages=320)
+    want = _codes(exp, 256)
+    got = run(b)
+    bad = (got.view(torch.int16) != want.view(torch.int16)).any(-1)
+    assert not bad.any(), torch.nonzero(bad)[:5].tolist()
 
 
 # ------------------------------------------------------------------- edge cases
