@@ -263,8 +263,7 @@ __global__ void __launch_bounds__(kWarps * 32, (kWarps == 4 && D <= 128) ? 3 : 1
         bt_nxt = bt_entry(32 + lane);
     }
 
-    // Q fragments for all D/16 k-steps; rows >= `rows` are zero.  Each of this
-    // thread's two rows (g, g + 8) has its own causal limit.
+    // Each of this thread's two rows (g, g + 8) has its own causal limit.
     const __nv_bfloat16* q = reinterpret_cast<const __nv_bfloat16*>(a.q);
     const bool row_lo = g < rows, row_hi = g + 8 < rows;
     const __nv_bfloat16* qg =
@@ -274,15 +273,6 @@ __global__ void __launch_bounds__(kWarps * 32, (kWarps == 4 && D <= 128) ? 3 : 1
                 D;
     const int lim_lo = L - n + (row_lo ? tok_of(g) : 0);      // last key row g may see
     const int lim_hi = L - n + (row_hi ? tok_of(g + 8) : 0);
-    uint32_t qa[D / 16][4];
-#pragma unroll
-    for (int ks = 0; ks < D / 16; ++ks) {
-        const int c = ks * 16 + 2 * tq;
-        qa[ks][0] = row_lo ? *reinterpret_cast<const uint32_t*>(qg + c) : 0u;
-        qa[ks][1] = row_hi ? *reinterpret_cast<const uint32_t*>(qg8 + c) : 0u;
-        qa[ks][2] = row_lo ? *reinterpret_cast<const uint32_t*>(qg + c + 8) : 0u;
-        qa[ks][3] = row_hi ? *reinterpret_cast<const uint32_t*>(qg8 + c + 8) : 0u;
-    }
 
     const __nv_bfloat16* kc = reinterpret_cast<const __nv_bfloat16*>(a.k_cache);
     const __nv_bfloat16* vc = reinterpret_cast<const __nv_bfloat16*>(a.v_cache);
@@ -329,6 +319,18 @@ __global__ void __launch_bounds__(kWarps * 32, (kWarps == 4 && D <= 128) ? 3 : 1
 
 #pragma unroll
     for (int i = 0; i < kStages - 1; ++i) issue(i);
+    // Q fragments for all D/16 k-steps (rows >= `rows` zero), loaded after the
+    // first pages' copies are issued: the copies wait for nothing else, and
+    // the loads then overlap their latency.
+    uint32_t qa[D / 16][4];
+#pragma unroll
+    for (int ks = 0; ks < D / 16; ++ks) {
+        const int c = ks * 16 + 2 * tq;
+        qa[ks][0] = row_lo ? *reinterpret_cast<const uint32_t*>(qg + c) : 0u;
+        qa[ks][1] = row_hi ? *reinterpret_cast<const uint32_t*>(qg8 + c) : 0u;
+        qa[ks][2] = row_lo ? *reinterpret_cast<const uint32_t*>(qg + c + 8) : 0u;
+        qa[ks][3] = row_hi ? *reinterpret_cast<const uint32_t*>(qg8 + c + 8) : 0u;
+    }
 
     for (int it = 0; it < my_pages; ++it) {
         issue(it + kStages - 1);
@@ -559,21 +561,22 @@ cudaError_t launch_decode_d(const Args& a, cudaStream_t stream) {
 
 template <int D>
 cudaError_t launch_decode_variant(const Args& a, cudaStream_t stream) {
-    if (D == 256) {  // a 4-warp CTA holds 64 (2 stages) or 96 KiB (3) of pages per warp pair
+    if constexpr (D == 256) {  // 4-warp CTAs only: 128 KiB (2 stages) or 192 KiB (3) of pages
         switch (a.decode_warps * 16 + a.decode_stages) {
             case 4 * 16 + 2: return launch_decode_d<256, 4, 2>(a, stream);
             case 4 * 16 + 3: return launch_decode_d<256, 4, 3>(a, stream);
             default: return cudaErrorInvalidValue;
         }
-    }
-    switch (a.decode_warps * 16 + a.decode_stages) {
-        case 4 * 16 + 2: return launch_decode_d<D, 4, 2>(a, stream);
-        case 4 * 16 + 3: return launch_decode_d<D, 4, 3>(a, stream);
-        case 4 * 16 + 4: return launch_decode_d<D, 4, 4>(a, stream);
-        case 8 * 16 + 2: return launch_decode_d<D, 8, 2>(a, stream);
-        case 8 * 16 + 3: return launch_decode_d<D, 8, 3>(a, stream);
-        case 12 * 16 + 2: return launch_decode_d<D, 12, 2>(a, stream);
-        default: return cudaErrorInvalidValue;
+    } else {
+        switch (a.decode_warps * 16 + a.decode_stages) {
+            case 4 * 16 + 2: return launch_decode_d<D, 4, 2>(a, stream);
+            case 4 * 16 + 3: return launch_decode_d<D, 4, 3>(a, stream);
+            case 4 * 16 + 4: return launch_decode_d<D, 4, 4>(a, stream);
+            case 8 * 16 + 2: return launch_decode_d<D, 8, 2>(a, stream);
+            case 8 * 16 + 3: return launch_decode_d<D, 8, 3>(a, stream);
+            case 12 * 16 + 2: return launch_decode_d<D, 12, 2>(a, stream);
+            default: return cudaErrorInvalidValue;
+        }
     }
 }
 
