@@ -379,18 +379,25 @@ def run_ours(args):
     est_ms = e0.elapsed_time(e1) / 10
     steps = args.steps if args.steps else int(min(200000, max(200, 2000.0 / max(est_ms, 1e-3))))
 
-    # graphs of M consecutive steps each, rotating over the R pool copies.  One
-    # step in EVERY has its dominant kernel bracketed by a pair of external
-    # events (event nodes between kernels cost the graph a few microseconds, so
-    # not every step carries them); their durations give roofline.achieved.
+    # graphs of M consecutive steps each, rotating over the R pool copies.  The
+    # dominant kernel's launches are timed by pairs of external events: when a
+    # step is that one kernel, each pair brackets a run of RUN consecutive
+    # launches (one run in every EVERY steps; the mean launch duration is the
+    # run's time / RUN); when a step launches more kernels, each pair brackets
+    # the dominant kernel of one step in EVERY.  (An event node between two
+    # kernels costs the graph a few microseconds, which a lone bracket charges
+    # to the kernel it surrounds.)  Their durations give roofline.achieved.
     EVERY = 8
     M = min(steps, max(R, 256))
     M = max(R, (M // R) * R) if M >= R else M
     key = "prefill" if dominant == "prefill" else "decode"
+    RUN = 16 if plan["launches"] == 1 and M >= 16 else 1
+    if RUN > 1:
+        EVERY = 64
 
     def make_graph(n):
-        evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-               for _ in range(0, n, EVERY)]
+        starts = [i for i in range(0, n, EVERY) if i + RUN <= n]
+        evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in starts]
         # torch creates the CUDA event on its first record(); do that outside the
         # capture so that the library receives real handles to re-record.
         for e_a, e_b in evs:
@@ -400,11 +407,14 @@ def run_ours(args):
         g = torch.cuda.CUDAGraph()
         with torch.cuda.graph(g, stream=stream):
             for i in range(n):
-                ev = None
-                if i % EVERY == 0:
-                    e_a, e_b = evs[i // EVERY]
-                    ev = {f"{key}_start_event": e_a, f"{key}_stop_event": e_b}
-                call(i, events=ev)
+                ev = {}
+                k, r = divmod(i, EVERY)
+                if k < len(evs):
+                    if r == 0:
+                        ev[f"{key}_start_event"] = evs[k][0]
+                    if r == RUN - 1:
+                        ev[f"{key}_stop_event"] = evs[k][1]
+                call(i, events=ev or None)
         return g, evs
 
     full, rem = divmod(steps, M)
@@ -436,7 +446,7 @@ def run_ours(args):
     sampler.stop()
     region_ms = start.elapsed_time(stop)
     # the last replay of each graph left its events' times
-    kernel_ms = [a.elapsed_time(b) for a, b in ev_main + ev_rem]
+    kernel_ms = [a.elapsed_time(b) / RUN for a, b in ev_main + ev_rem]
     assert pa.device_error(stream) == 0
 
     region_ms_max = reduce_max(region_ms, world, dev)
@@ -613,8 +623,11 @@ def run_ours(args):
                       f"> 3 x L2 {l2 / 2**20:.0f} MiB)" if R > 1 else "KV bytes per step > 3 x L2",
                 "graph": f"CUDA graphs of {M} steps", "kv_chunk": plan["kv_chunk"], "splits": plan["splits"],
                 "decode_stages": plan["decode_stages"],
-                "kernel_timing": f"CUDA events around the dominant kernel of one step in {EVERY} of the "
-                                 f"timed graphs ({len(kernel_ms)} launches of the last replays)",
+                "kernel_timing": (f"CUDA events around runs of {RUN} consecutive launches of the dominant "
+                                  f"kernel (the whole step), one run in {EVERY} steps of the timed graphs "
+                                  f"({len(kernel_ms)} runs of the last replays)" if RUN > 1 else
+                                  f"CUDA events around the dominant kernel of one step in {EVERY} of the "
+                                  f"timed graphs ({len(kernel_ms)} launches of the last replays)"),
                 "parallelism": f"dp{world}" if world > 1 else "single GPU",
             },
             "tok_s": total_tokens * steps / (region_ms_max / 1e3),
