@@ -326,6 +326,7 @@ pa_status pa_forward_ex(const void* q, const void* k_cache, const void* v_cache,
     a.query_start_loc = query_start_loc;
     a.out = out;
     a.err = static_cast<int32_t*>(ws);
+    a.sched = reinterpret_cast<int32_t*>(static_cast<char*>(ws) + pa::kSchedOffset);
     const pa::WorkspaceLayout wl =
         pa::workspace_layout(a.num_seqs, a.num_q_heads, pa::ws_splits(a.splits, a.decode_cluster), a.head_dim,
                              a.decode_max_q, counter_area);

@@ -137,20 +137,17 @@ extern "C" pa_status pa_forward_noalloc(const void* q, const void* k_cache, cons
     a.counters = reinterpret_cast<int32_t*>(sb + wl.counters_off);
     a.ws_o = reinterpret_cast<float*>(sb + wl.o_off);
     a.ws_ml = reinterpret_cast<float*>(sb + wl.ml_off);
-    if (device_error) {
-        a.err = device_error;
-    } else {
-        a.err = static_cast<int32_t*>(scratch);
-        cudaError_t e = cudaMemsetAsync(scratch, 0, sizeof(int32_t), s);
-        if (e != cudaSuccess) return report(PA_ERR_CUDA, "cudaMemsetAsync(error word) failed");
-    }
-    // The split ticket counters must start at zero: clear them (a completed call
-    // leaves them zero, but the array is shared and the last call may not have
-    // completed normally).  The partials are written before they are read within
-    // one call, so they need no clearing.
-    if (wl.o_off > wl.counters_off) {
-        cudaError_t e = cudaMemsetAsync(sb + wl.counters_off, 0, static_cast<size_t>(wl.o_off - wl.counters_off), s);
-        if (e != cudaSuccess) return report(PA_ERR_CUDA, "cudaMemsetAsync(split counters) failed");
+    a.err = device_error ? device_error : static_cast<int32_t*>(scratch);
+    a.sched = reinterpret_cast<int32_t*>(sb + pa::kSchedOffset);
+    // The error word (unless the caller's), the prefill item counters and the
+    // split ticket counters must start at zero: clear them in one memset (a
+    // completed call leaves the counters zero, but the array is shared and the
+    // last call may not have completed normally).  The partials are written
+    // before they are read within one call, so they need no clearing.
+    {
+        const int64_t lo = device_error ? pa::kSchedOffset : 0;
+        cudaError_t e = cudaMemsetAsync(sb + lo, 0, static_cast<size_t>(wl.o_off - lo), s);
+        if (e != cudaSuccess) return report(PA_ERR_CUDA, "cudaMemsetAsync(error word and counters) failed");
     }
     cudaError_t e = pa::launch_decode(a, s);
     if (e == cudaSuccess) e = pa::launch_prefill(a, s);

@@ -31,6 +31,7 @@ struct Args {
     float* ws_ml;   // [B, splits, Hq, 2] fp32: running max (log2 domain) and sum
     int32_t* counters;  // split tickets [B, Hkv, row_groups]; zero between calls
     int32_t* err;   // sticky device error word
+    int32_t* sched; // prefill item counters [2] (next item, finished CTAs); zero between calls
     int64_t num_tokens;
     int64_t num_blocks;
     int32_t num_seqs, num_q_heads, num_kv_heads, group, head_dim, page_size, max_pages;
@@ -61,8 +62,13 @@ inline int32_t decode_max_q(int32_t group) { return group <= 16 ? 16 / group : 1
 // Splits whose partials go through the workspace (none in cluster mode).
 inline int32_t ws_splits(int32_t splits, int32_t decode_cluster) { return decode_cluster > 1 ? 1 : splits; }
 
+// Byte offset, in the workspace header, of the prefill kernel's two item
+// counters (zero before and after every call: the last CTA resets them).
+constexpr int64_t kSchedOffset = 128;
+
 // Workspace layout shared by pa_forward and pa_forward_noalloc: a 256-byte
-// header (sticky error word), an area of split ticket counters (zero before and
+// header (sticky error word at 0, prefill item counters at kSchedOffset), an
+// area of split ticket counters (zero before and
 // after every call: the last CTA of each ticket resets it), then the partials O
 // and (m, l) of [B, splits, decode_max_q, Hq] rows.  The counter area never
 // overlaps bytes that held partials: its size is a property of the buffer

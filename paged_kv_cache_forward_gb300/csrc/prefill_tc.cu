@@ -1,7 +1,8 @@
 // prefill_tc.cu -- causal varlen chunked prefill on the 5th-generation tensor
 // cores (tcgen05 + TMEM + TMA), sm_103a.
 //
-// One CTA owns (a pair of query tiles, KV head h).  A tile packs TQ =
+// A work item is (a pair of query tiles, KV head h); one persistent CTA per SM
+// takes items one after another (see prefill_tc_kernel).  A tile packs TQ =
 // floor(128 / G) consecutive new tokens of one sequence times the G query heads
 // sharing h into the M = 128 rows of one MMA tile, row r = (token r / G, head
 // h*G + r % G): the "Q-Block" item of the five-step list on the Triton
@@ -14,10 +15,11 @@
 // mask bottom-right aligned ("Flash Attention in Triton"), online softmax,
 // O += P V, out = O / l.
 //
-// Warp roles (352 threads):
-//   warps 0, 10 TMA producers: warp 0 both Q tiles once, then per KV tile the K
-//               page boxes (64 columns x 16 slots of one page and head, 128-byte
-//               swizzle) into a 3-stage K ring; warp 10 the V page boxes into a
+// Warp roles (352 threads), each looping over the CTA's items:
+//   warps 0, 10 TMA producers: warp 0 resolves the items and per item loads
+//               both Q tiles and the K page boxes (64 columns x 16 slots of one
+//               page and head, 128-byte swizzle) into a 3-stage K ring; warp 10
+//               the V page boxes into a
 //               2-stage V ring, each running ahead on its own.  Block-table
 //               entries are fetched one group of 4 tiles ahead.  The one page of
 //               V that holds the sequence end is copied by plain loads with zero
@@ -93,9 +95,10 @@ struct Smem {
     static constexpr int kK0 = kQ0 + Cfg<D>::kTiles * kTile;
     static constexpr int kV0 = kK0 + Cfg<D>::kKStages * kTile;
     static constexpr int kBar = kV0 + Cfg<D>::kVStages * kTile;
-    static constexpr int kNumBars = 18;
-    static constexpr int kMisc = kBar + kNumBars * 8;  // tmem address, abort flag, tile info
-    static constexpr int kBytes = kMisc + 64;
+    static constexpr int kNumBars = 23;
+    static constexpr int kMisc = kBar + kNumBars * 8;  // tmem address, abort flag
+    static constexpr int kItems = kMisc + 32;          // 2-slot item ring, 32 bytes a slot
+    static constexpr int kBytes = kItems + 64;
     static constexpr int kAlloc = kBytes + 1024;  // slack to align the base to 1024
     static_assert(kAlloc <= 227 * 1024, "shared memory above the per-CTA limit");
 };
@@ -109,8 +112,11 @@ enum Bar {
     kVEmpty0 = 9,   // [2]
     kSFull0 = 11,   // [2] per tile: S(j) in TMEM
     kPFull0 = 13,   // [2] per tile: P(j) in TMEM (4 softmax warps arrive)
-    kODone0 = 15,   // [2] per tile: the tile's last O += P V done (completes once)
+    kODone0 = 15,   // [2] per tile: the tile's last O += P V of an item done
     kDrain = 17,
+    kQEmpty = 18,      // the item's last S MMA has read Q
+    kItemFull0 = 19,   // [2] item ring slot written
+    kItemEmpty0 = 21,  // [2] item ring slot read by every role
 };
 
 // Tiles of a sequence with n new tokens (the decode path takes n <= qmax), and
@@ -185,10 +191,119 @@ __device__ __forceinline__ void issue_pv_group(uint32_t d, uint32_t pa, uint64_t
         if (ks < npj) tc::mma_bf16_tmem_a(d, pa + ks * 8, db + ks * (2048 >> 4), idesc, (!first || ks > 0) ? 1u : 0u);
 }
 
+// A work item is (pair of query tiles, KV head).  Items are numbered pair-major:
+// item w is pair w / Hkv of KV head w % Hkv, pairs counted over the sequences in
+// order and, within a sequence, last pair first (it sees the most keys), so the
+// items handed out last are the shortest of the last sequence.
+struct Item {
+    int b;   // sequence; -1: no item left
+    int h;   // KV head
+    int i0;  // first new token (within the sequence) of tile A
+    int q0;  // first query row of the sequence
+    int n;   // new tokens of the sequence
+    int L;   // keys of the sequence (clamped to the block table's capacity)
+    int pad[2];
+};
+enum ItemStatus { kItemEnd = 0, kItemOk = 1, kItemSkip = 2 };
+
+// Resolves item w (warp-collective; every lane gets the same result).  An item
+// whose metadata are inconsistent is settled here (error code; rows of a query
+// longer than its sequence written as zeros) and reported as skipped.
+template <int D, int kTiles>
+__device__ ItemStatus resolve_item(const Args& a, int w, int tq_tokens, Item& it, int lane) {
+    const int pidx = w / a.num_kv_heads;
+    int found_b = -1, found_p = 0, base_t = 0, q0 = 0, n = 0;
+    for (int b0 = 0; b0 < a.num_seqs && found_b < 0; b0 += 32) {
+        const int b = b0 + lane;
+        int s0 = 0, s1 = 0;
+        if (b < a.num_seqs) {
+            s0 = a.query_start_loc[b];
+            s1 = a.query_start_loc[b + 1];
+        }
+        const int cnt = b < a.num_seqs ? ctas_of(s1 - s0, tq_tokens, a.decode_max_q, kTiles) : 0;
+        int inc = cnt;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int v = __shfl_up_sync(0xffffffffu, inc, o);
+            if (lane >= o) inc += v;
+        }
+        const int excl = base_t + inc - cnt;
+        const unsigned m = __ballot_sync(0xffffffffu, cnt > 0 && pidx >= excl && pidx < excl + cnt);
+        if (m) {
+            const int src = __ffs(m) - 1;
+            found_b = b0 + src;
+            found_p = __shfl_sync(0xffffffffu, excl + cnt - 1, src) - pidx;  // last pair first
+            q0 = __shfl_sync(0xffffffffu, s0, src);
+            n = __shfl_sync(0xffffffffu, s1 - s0, src);
+        }
+        base_t += __shfl_sync(0xffffffffu, inc, 31);
+    }
+    if (found_b < 0) return kItemEnd;  // w is past the last item
+    it.b = found_b;
+    it.h = w - pidx * a.num_kv_heads;
+    it.i0 = found_p * kTiles * tq_tokens;
+    it.q0 = q0;
+    it.n = n;
+    if (q0 < 0 || static_cast<int64_t>(q0) + n > a.num_tokens) {
+        if (lane == 0) flag_error(a.err, kDevBadQueryStart);
+        return kItemSkip;
+    }
+    const int cap = a.max_pages * kPage;
+    int L = a.seq_lens[found_b];
+    if (L > cap) {
+        if (lane == 0) flag_error(a.err, kDevSeqTooLong);
+        L = cap;
+    }
+    it.L = L;
+    if (L < n) {
+        if (lane == 0) flag_error(a.err, kDevQueryTooLong);
+        const int G = a.group;
+        const int rows = min(kTiles * tq_tokens, n - it.i0) * G;
+        __nv_bfloat16* const out = reinterpret_cast<__nv_bfloat16*>(a.out);
+        for (int i = lane; i < rows * D; i += 32) {
+            const int r = i / D;
+            out[(static_cast<int64_t>(q0 + it.i0 + r / G) * a.num_q_heads + it.h * G + r % G) * D + i % D] =
+                __float2bfloat16(0.f);
+        }
+        return kItemSkip;
+    }
+    return kItemOk;
+}
+
+// What every role derives from an item.
+struct ItemShape {
+    int ntok[2];     // new tokens of tile x
+    int nkv[2];      // KV tiles up to tile x's last causal position
+    int ntiles;      // KV tiles of the item
+    int last_page;   // pages [0, last_page) are read
+    int full_pages;  // pages with no slot past L
+    int prefix;      // cached keys before the first new token
+};
+__device__ __forceinline__ ItemShape shape_of(const Item& it, int tq_tokens, int kTiles) {
+    ItemShape s;
+    s.prefix = it.L - it.n;
+#pragma unroll
+    for (int x = 0; x < 2; ++x) {
+        s.ntok[x] = x < kTiles ? max(0, min(tq_tokens, it.n - (it.i0 + x * tq_tokens))) : 0;
+        s.nkv[x] = s.ntok[x] > 0 ? (s.prefix + it.i0 + x * tq_tokens + s.ntok[x] + kKeys - 1) / kKeys : 0;
+    }
+    s.ntiles = max(s.nkv[0], s.nkv[1]);
+    const int kv_end = s.prefix + it.i0 + s.ntok[0] + s.ntok[1];  // keys [0, kv_end) are visible to some row
+    s.last_page = (kv_end + kPage - 1) / kPage;
+    s.full_pages = it.L / kPage;
+    return s;
+}
+
+// Persistent: one CTA per SM walks the items.  Warp 0 resolves the CTA's next
+// item (its first is blockIdx.x, later ones come from an atomic counter in the
+// workspace, so CTAs that finish early take more) and publishes it in a 2-slot
+// ring of shared memory that every other role reads in the same order.  All ring
+// and barrier positions run on across items, so the next item's Q, K and first
+// S MMAs proceed while the softmax warps still finish the previous one.
 template <int D>
 __global__ void __launch_bounds__(kThreads, 1)
     prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
-                      const __grid_constant__ CUtensorMap tm_v, const Args a, int tq_tokens, int pairs_bound) {
+                      const __grid_constant__ CUtensorMap tm_v, const Args a, int tq_tokens) {
     using S = Smem<D>;
     constexpr int kTiles = Cfg<D>::kTiles, kKStages = Cfg<D>::kKStages, kVStages = Cfg<D>::kVStages;
     extern __shared__ uint8_t smem_raw[];
@@ -198,90 +313,16 @@ __global__ void __launch_bounds__(kThreads, 1)
     auto bar = [&](int i) { return base + S::kBar + 8 * i; };
     uint32_t* const s_tmem = reinterpret_cast<uint32_t*>(sp + S::kMisc);
     volatile int* const s_abort = reinterpret_cast<volatile int*>(sp + S::kMisc + 4);
-    int* const s_info = reinterpret_cast<int*>(sp + S::kMisc + 8);
+    Item* const s_items = reinterpret_cast<Item*>(sp + S::kItems);
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
-    const int pair = blockIdx.x % pairs_bound;
-    const int h = blockIdx.x / pairs_bound;
-
-    // ---- which sequence owns this pair (prefix sum of per-sequence pair counts)
-    if (warp == 0) {
-        int found_b = -1, found_t = 0, base_t = 0;
-        for (int b0 = 0; b0 < a.num_seqs && found_b < 0; b0 += 32) {
-            const int b = b0 + lane;
-            const int cnt =
-                b < a.num_seqs ? ctas_of(a.query_start_loc[b + 1] - a.query_start_loc[b], tq_tokens, a.decode_max_q,
-                                         kTiles)
-                               : 0;
-            int inc = cnt;
-#pragma unroll
-            for (int o = 1; o < 32; o <<= 1) {
-                const int v = __shfl_up_sync(0xffffffffu, inc, o);
-                if (lane >= o) inc += v;
-            }
-            const int excl = base_t + inc - cnt;
-            const unsigned m = __ballot_sync(0xffffffffu, cnt > 0 && pair >= excl && pair < excl + cnt);
-            if (m) {
-                const int src = __ffs(m) - 1;
-                found_b = b0 + src;
-                // the sequence's last pair first: its tiles see the most keys
-                found_t = __shfl_sync(0xffffffffu, excl + cnt - 1, src) - pair;
-            }
-            base_t += __shfl_sync(0xffffffffu, inc, 31);
-        }
-        if (lane == 0) {
-            s_info[0] = found_b;
-            s_info[1] = found_t;
-            *s_abort = 0;
-        }
-    }
-    __syncthreads();
-    const int b = s_info[0];
-    if (b < 0) return;  // surplus CTA of the static grid (uniform for the block)
-    const int p_in_seq = s_info[1];
-
-    const int q0 = a.query_start_loc[b];
-    const int n = a.query_start_loc[b + 1] - q0;
-    if (q0 < 0 || static_cast<int64_t>(q0) + n > a.num_tokens) {
-        if (threadIdx.x == 0) flag_error(a.err, kDevBadQueryStart);
-        return;
-    }
-    const int cap = a.max_pages * kPage;
-    int L = a.seq_lens[b];
-    if (L > cap) {
-        if (threadIdx.x == 0) flag_error(a.err, kDevSeqTooLong);
-        L = cap;
-    }
     const int G = a.group;
-    const int i0 = p_in_seq * kTiles * tq_tokens;  // first new token of tile A
-    const int ntok_pair = min(kTiles * tq_tokens, n - i0);
-    const int prefix = L - n;
-    __nv_bfloat16* const out = reinterpret_cast<__nv_bfloat16*>(a.out);
-    if (prefix < 0) {
-        if (threadIdx.x == 0) flag_error(a.err, kDevQueryTooLong);
-        for (int i = threadIdx.x; i < ntok_pair * G * D; i += blockDim.x) {
-            const int r = i / D;
-            out[(static_cast<int64_t>(q0 + i0 + r / G) * a.num_q_heads + h * G + r % G) * D + i % D] =
-                __float2bfloat16(0.f);
-        }
-        return;
-    }
-    // per tile x: new tokens, and KV tiles up to its last causal position
-    int ntok[2], nkv[2];
-#pragma unroll
-    for (int x = 0; x < 2; ++x) {
-        ntok[x] = x < kTiles ? max(0, min(tq_tokens, n - (i0 + x * tq_tokens))) : 0;
-        nkv[x] = ntok[x] > 0 ? (prefix + i0 + x * tq_tokens + ntok[x] + kKeys - 1) / kKeys : 0;
-    }
-    const int ntiles = max(nkv[0], nkv[1]);
-    const int kv_end = prefix + i0 + ntok_pair;          // keys [0, kv_end) are visible to some row
-    const int last_page = (kv_end + kPage - 1) / kPage;  // pages [0, last_page) are read
-    const int full_pages = L / kPage;                    // pages with no slot past L
 
-    // ---- barriers and TMEM
+    // ---- barriers and TMEM, once per CTA
     if (threadIdx.x == 0) {
         tc::mbar_init(bar(kQFull), 1);
+        tc::mbar_init(bar(kQEmpty), 1);
         for (int i = 0; i < kMaxKStages; ++i) {
             tc::mbar_init(bar(kKFull0 + i), 1);
             tc::mbar_init(bar(kKEmpty0 + i), 1);
@@ -294,8 +335,12 @@ __global__ void __launch_bounds__(kThreads, 1)
             tc::mbar_init(bar(kSFull0 + x), 1);
             tc::mbar_init(bar(kPFull0 + x), 4);
             tc::mbar_init(bar(kODone0 + x), 1);
+            tc::mbar_init(bar(kItemFull0 + x), 1);
+            // readers of an item: the MMA thread, the V producer, the softmax warps
+            tc::mbar_init(bar(kItemEmpty0 + x), 2 + 4 * kTiles);
         }
         tc::mbar_init(bar(kDrain), 1);
+        *s_abort = 0;
         tc::fence_mbar_init();
     }
     if (warp == 1) {
@@ -309,99 +354,152 @@ __global__ void __launch_bounds__(kThreads, 1)
     bool ok = true;
 
     if (warp == 0 || warp == kWarpV) {
-        // ========================================== TMA producers (K: warp 0, V: warp 10)
+        // ==================== scheduler + Q and K producer (warp 0), V producer (warp 10)
         const bool is_v = warp == kWarpV;
         if (lane == 0) {
             if (!is_v) {
                 tc::prefetch_tmap(&tm_q);
                 tc::prefetch_tmap(&tm_k);
-                const int nq = ntok[1] > 0 ? 2 : 1;
-                tc::mbar_arrive_expect_tx(bar(kQFull), nq * S::kHalves * 64 * 2 * G * tq_tokens);
-                for (int x = 0; x < nq; ++x)
-#pragma unroll
-                    for (int hf = 0; hf < S::kHalves; ++hf)
-                        tc::tma_load_3d(base + S::kQ0 + x * S::kTile + hf * kHalfBytes, &tm_q, bar(kQFull), hf * 64,
-                                        h * G, q0 + i0 + x * tq_tokens);
             } else {
                 tc::prefetch_tmap(&tm_v);
             }
         }
-        const int32_t* bt = a.block_table + static_cast<int64_t>(b) * a.max_pages;
-        // lane l holds the block-table entry of page (group * 32 + l); the next
-        // group's entries are loaded while the current group is being used.
-        auto load_group = [&](int grp) -> int {
-            const int pg = grp * kTilesPerGroup * kPagesPerTile + lane;
-            return pg < last_page ? bt[pg] : 0;
-        };
-        int cur_grp = load_group(0);
-        int next_grp = load_group(1);
         const __nv_bfloat16* vc = reinterpret_cast<const __nv_bfloat16*>(a.v_cache);
         const int stages = is_v ? kVStages : kKStages;
         const int full0 = is_v ? kVFull0 : kKFull0, empty0 = is_v ? kVEmpty0 : kKEmpty0;
         const uint32_t ring = base + (is_v ? S::kV0 : S::kK0);
         const CUtensorMap* tm = is_v ? &tm_v : &tm_k;
-        for (int kt = 0; kt < ntiles; ++kt) {
-            const int slot = kt % kTilesPerGroup;
-            if (slot == 0 && kt > 0) {
-                cur_grp = next_grp;
-                next_grp = load_group(kt / kTilesPerGroup + 1);
-            }
-            const int p0 = kt * kPagesPerTile;
-            const int np = min(kPagesPerTile, last_page - p0);
-            // pages by TMA: all of K; V up to the one holding the sequence end
-            const int nt = is_v ? max(0, min(np, full_pages - p0)) : np;
-            int page = __shfl_sync(0xffffffffu, cur_grp, (slot * kPagesPerTile + lane) & 31);
-            if (lane < np && static_cast<uint32_t>(page) >= static_cast<uint64_t>(a.num_blocks)) {
-                flag_error(a.err, kDevBadBlock);
-                page = 0;
-            }
-            const int st = kt % stages;
-            if (kt >= stages && !warp_wait(bar(empty0 + st), (kt / stages - 1) & 1, s_abort)) {
-                ok = false;
-                break;
-            }
-            const uint32_t sd = ring + st * S::kTile;
-            if (is_v && nt < np) {
-                // The V page holding the sequence end: plain loads, slots >= L as zeros.
-                const int pi = np - 1;
-                const int pg = __shfl_sync(0xffffffffu, page, pi);
-                for (int c = lane; c < kPage * (D / 8); c += 32) {
-                    const int t = c / (D / 8), ch = c % (D / 8);
-                    const int row = pi * kPage + t;
-                    uint4 val = make_uint4(0u, 0u, 0u, 0u);
-                    if ((p0 + pi) * kPage + t < L)
-                        val = *reinterpret_cast<const uint4*>(
-                            vc + ((static_cast<int64_t>(pg) * kPage + t) * a.num_kv_heads + h) * D + ch * 8);
-                    const uint32_t dst = sd + (ch >> 3) * kHalfBytes + sw128(row, ch & 7);
-                    asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};\n" ::"r"(dst), "r"(val.x), "r"(val.y),
-                                 "r"(val.z), "r"(val.w)
-                                 : "memory");
+        int w = blockIdx.x;  // warp 0: the item to resolve next
+        uint32_t tc_n = 0;   // K or V tiles loaded so far (ring position)
+        for (int it = 0;; ++it) {
+            const int slot = it & 1;
+            Item itm;
+            if (!is_v) {
+                ItemStatus st;
+                while ((st = resolve_item<D, kTiles>(a, w, tq_tokens, itm, lane)) == kItemSkip) {
+                    int wn = 0;
+                    if (lane == 0) wn = static_cast<int>(gridDim.x) + atomicAdd(a.sched, 1);
+                    w = __shfl_sync(0xffffffffu, wn, 0);
                 }
-                tc::fence_proxy_async_smem();
+                if (st == kItemEnd) itm.b = -1;
+                if (it >= 2 && !warp_wait(bar(kItemEmpty0 + slot), ((it >> 1) - 1) & 1, s_abort)) {
+                    ok = false;
+                    break;
+                }
+                if (lane == 0) {
+                    s_items[slot] = itm;
+                    tc::mbar_arrive(bar(kItemFull0 + slot));
+                }
+                __syncwarp();
+            } else {
+                if (!warp_wait(bar(kItemFull0 + slot), (it >> 1) & 1, s_abort)) {
+                    ok = false;
+                    break;
+                }
+                itm = s_items[slot];
+                __syncwarp();
+                if (lane == 0) tc::mbar_arrive(bar(kItemEmpty0 + slot));
             }
-            __syncwarp();
-            if (lane == 0) tc::mbar_arrive_expect_tx(bar(full0 + st), nt * S::kHalves * 2048);
-            __syncwarp();
-            if (lane < nt) {
+            if (itm.b < 0) break;
+            // warp 0: the number of the item after this one, fetched while this one loads
+            int wn = 0;
+            if (!is_v && lane == 0) wn = static_cast<int>(gridDim.x) + atomicAdd(a.sched, 1);
+            const ItemShape sh = shape_of(itm, tq_tokens, kTiles);
+            const int h = itm.h, L = itm.L;
+            const int32_t* bt = a.block_table + static_cast<int64_t>(itm.b) * a.max_pages;
+            // lane l holds the block-table entry of page (group * 32 + l); the next
+            // group's entries are loaded while the current group is being used.
+            auto load_group = [&](int grp) -> int {
+                const int pg = grp * kTilesPerGroup * kPagesPerTile + lane;
+                return pg < sh.last_page ? bt[pg] : 0;
+            };
+            int cur_grp = load_group(0);
+            int next_grp = load_group(1);
+            for (int kt = 0; kt < sh.ntiles; ++kt) {
+                const int gslot = kt % kTilesPerGroup;
+                if (gslot == 0 && kt > 0) {
+                    cur_grp = next_grp;
+                    next_grp = load_group(kt / kTilesPerGroup + 1);
+                }
+                const int p0 = kt * kPagesPerTile;
+                const int np = min(kPagesPerTile, sh.last_page - p0);
+                // pages by TMA: all of K; V up to the one holding the sequence end
+                const int nt = is_v ? max(0, min(np, sh.full_pages - p0)) : np;
+                int page = __shfl_sync(0xffffffffu, cur_grp, (gslot * kPagesPerTile + lane) & 31);
+                if (lane < np && static_cast<uint32_t>(page) >= static_cast<uint64_t>(a.num_blocks)) {
+                    flag_error(a.err, kDevBadBlock);
+                    page = 0;
+                }
+                const int st = tc_n % stages;
+                if (tc_n >= static_cast<uint32_t>(stages) &&
+                    !warp_wait(bar(empty0 + st), (tc_n / stages - 1) & 1, s_abort)) {
+                    ok = false;
+                    break;
+                }
+                const uint32_t sd = ring + st * S::kTile;
+                if (is_v && nt < np) {
+                    // The V page holding the sequence end: plain loads, slots >= L as zeros.
+                    const int pi = np - 1;
+                    const int pg = __shfl_sync(0xffffffffu, page, pi);
+                    for (int c = lane; c < kPage * (D / 8); c += 32) {
+                        const int t = c / (D / 8), ch = c % (D / 8);
+                        const int row = pi * kPage + t;
+                        uint4 val = make_uint4(0u, 0u, 0u, 0u);
+                        if ((p0 + pi) * kPage + t < L)
+                            val = *reinterpret_cast<const uint4*>(
+                                vc + ((static_cast<int64_t>(pg) * kPage + t) * a.num_kv_heads + h) * D + ch * 8);
+                        const uint32_t dst = sd + (ch >> 3) * kHalfBytes + sw128(row, ch & 7);
+                        asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};\n" ::"r"(dst), "r"(val.x), "r"(val.y),
+                                     "r"(val.z), "r"(val.w)
+                                     : "memory");
+                    }
+                    tc::fence_proxy_async_smem();
+                }
+                __syncwarp();
+                if (lane == 0) tc::mbar_arrive_expect_tx(bar(full0 + st), nt * S::kHalves * 2048);
+                __syncwarp();
+                if (lane < nt) {
 #pragma unroll
-                for (int hf = 0; hf < S::kHalves; ++hf)
-                    tc::tma_load_4d(sd + hf * kHalfBytes + lane * 2048, tm, bar(full0 + st), hf * 64, h, 0, page);
-            }
-            // L2 prefetch of the pages kPrefetchTiles tiles ahead, so that their
-            // ring loads find them in L2 rather than in HBM.
-            if (kPrefetchTiles > 0 && kt + kPrefetchTiles < ntiles) {
-                const int kp = kt + kPrefetchTiles;
-                const int pp0 = kp * kPagesPerTile;
-                const int npp = min(kPagesPerTile, last_page - pp0);
-                const int sp = kp % kTilesPerGroup;
-                // tile kp's entries: in this group, or (kp / 4 > kt / 4) in the next
-                const int src = (kp / kTilesPerGroup == kt / kTilesPerGroup) ? cur_grp : next_grp;
-                const int ppage = __shfl_sync(0xffffffffu, src, (sp * kPagesPerTile + lane) & 31);
-                if (lane < npp && static_cast<uint32_t>(ppage) < static_cast<uint64_t>(a.num_blocks)) {
+                    for (int hf = 0; hf < S::kHalves; ++hf)
+                        tc::tma_load_4d(sd + hf * kHalfBytes + lane * 2048, tm, bar(full0 + st), hf * 64, h, 0, page);
+                }
+                ++tc_n;
+                if (!is_v && kt == 0) {
+                    // Q of this item (after its first K tile): once the previous
+                    // item's last S MMA has read the Q buffer.
+                    if (it > 0 && !warp_wait(bar(kQEmpty), (it - 1) & 1, s_abort)) {
+                        ok = false;
+                        break;
+                    }
+                    if (lane == 0) {
+                        const int nq = sh.ntok[1] > 0 ? 2 : 1;
+                        tc::mbar_arrive_expect_tx(bar(kQFull), nq * S::kHalves * 64 * 2 * G * tq_tokens);
+                        for (int x = 0; x < nq; ++x)
 #pragma unroll
-                    for (int hf = 0; hf < S::kHalves; ++hf) tc::tma_prefetch_4d(tm, hf * 64, h, 0, ppage);
+                            for (int hf = 0; hf < S::kHalves; ++hf)
+                                tc::tma_load_3d(base + S::kQ0 + x * S::kTile + hf * kHalfBytes, &tm_q, bar(kQFull),
+                                                hf * 64, h * G, itm.q0 + itm.i0 + x * tq_tokens);
+                    }
+                    __syncwarp();
+                }
+                // L2 prefetch of the pages kPrefetchTiles tiles ahead, so that their
+                // ring loads find them in L2 rather than in HBM.
+                if (kPrefetchTiles > 0 && kt + kPrefetchTiles < sh.ntiles) {
+                    const int kp = kt + kPrefetchTiles;
+                    const int pp0 = kp * kPagesPerTile;
+                    const int npp = min(kPagesPerTile, sh.last_page - pp0);
+                    const int spg = kp % kTilesPerGroup;
+                    // tile kp's entries: in this group, or (kp / 4 > kt / 4) in the next
+                    const int src = (kp / kTilesPerGroup == kt / kTilesPerGroup) ? cur_grp : next_grp;
+                    const int ppage = __shfl_sync(0xffffffffu, src, (spg * kPagesPerTile + lane) & 31);
+                    if (lane < npp && static_cast<uint32_t>(ppage) < static_cast<uint64_t>(a.num_blocks)) {
+#pragma unroll
+                        for (int hf = 0; hf < S::kHalves; ++hf) tc::tma_prefetch_4d(tm, hf * 64, h, 0, ppage);
+                    }
                 }
             }
+            if (!ok) break;
+            if (!is_v) w = __shfl_sync(0xffffffffu, wn, 0);
         }
         if (!ok && lane == 0) {
             *s_abort = 1;
@@ -424,51 +522,72 @@ __global__ void __launch_bounds__(kThreads, 1)
             constexpr uint64_t kTileU = S::kTile >> 4;
             const uint32_t d_s0 = tmem + tmem_s(0), d_s1 = tmem + tmem_s(1);
             const uint32_t d_o0 = tmem + tmem_o(0), d_o1 = tmem + tmem_o(1);
-#define PA_ISSUE_S(x, jj)                                                                                     \
+            uint32_t kc = 0, vc = 0, pc0 = 0, pc1 = 0;  // K and V tiles, P tiles consumed so far
+#define PA_ISSUE_S(x)                                                                                         \
     do {                                                                                                      \
-        issue_s_group<D>((x) ? d_s1 : d_s0, dq0 + ((x) ? kTileU : 0), dk0 + ((jj) % kKStages) * kTileU, kIdQK); \
+        issue_s_group<D>((x) ? d_s1 : d_s0, dq0 + ((x) ? kTileU : 0), dk0 + (kc % kKStages) * kTileU, kIdQK); \
         tc::mma_commit(bar(kSFull0 + (x)));                                                                   \
     } while (0)
 // (the caller has waited for P_x(jj))
 #define PA_ISSUE_PV(x, jj)                                                                                  \
     do {                                                                                                    \
         tc::tc_fence_after();                                                                               \
-        issue_pv_group((x) ? d_o1 : d_o0, ((x) ? d_s1 : d_s0) + 64, dv0 + ((jj) % kVStages) * kTileU, kIdPV, \
+        issue_pv_group((x) ? d_o1 : d_o0, ((x) ? d_s1 : d_s0) + 64, dv0 + (vc % kVStages) * kTileU, kIdPV,  \
                        min(kPagesPerTile, last_page - (jj) * kPagesPerTile), (jj) == 0);                    \
         if ((jj) == ((x) ? nkv1 : nkv0) - 1) tc::mma_commit(bar(kODone0 + (x)));                            \
     } while (0)
-            ok = tc::mbar_wait(bar(kQFull), 0, s_abort, kTimeoutNs);
-            if (ok && ntiles > 0) ok = tc::mbar_wait(bar(kKFull0), 0, s_abort, kTimeoutNs);
-            const int nkv0 = nkv[0], nkv1 = nkv[1];
-            if (ok && ntiles > 0) {
+            for (int it = 0; ok; ++it) {
+                const int slot = it & 1;
+                if (!(ok = tc::mbar_wait(bar(kItemFull0 + slot), (it >> 1) & 1, s_abort, kTimeoutNs))) break;
+                const Item itm = s_items[slot];
+                tc::mbar_arrive(bar(kItemEmpty0 + slot));
+                if (itm.b < 0) break;
+                const ItemShape sh = shape_of(itm, tq_tokens, kTiles);
+                const int nkv0 = sh.nkv[0], nkv1 = sh.nkv[1], ntiles = sh.ntiles, last_page = sh.last_page;
+                if (!(ok = tc::mbar_wait(bar(kQFull), it & 1, s_abort, kTimeoutNs))) break;
+                if (!(ok = tc::mbar_wait(bar(kKFull0 + kc % kKStages), (kc / kKStages) & 1, s_abort, kTimeoutNs)))
+                    break;
                 tc::tc_fence_after();
-                if (nkv0 > 0) PA_ISSUE_S(0, 0);
-                if (nkv1 > 0) PA_ISSUE_S(1, 0);
-                tc::mma_commit(bar(kKEmpty0));
-            }
-            for (int j = 0; j < ntiles && ok; ++j) {
-                const bool nxt0 = j + 1 < nkv0, nxt1 = j + 1 < nkv1;
-                ok = tc::mbar_wait(bar(kVFull0 + j % kVStages), (j / kVStages) & 1, s_abort, kTimeoutNs);
-                if (!ok) break;
-                tc::tc_fence_after();
-                if (j < nkv0) {
-                    if (!(ok = tc::mbar_wait(bar(kPFull0), j & 1, s_abort, kTimeoutNs))) break;
-                    PA_ISSUE_PV(0, j);
-                }
-                if (nxt0 || nxt1) {
-                    const int js = j + 1;
-                    ok = tc::mbar_wait(bar(kKFull0 + js % kKStages), (js / kKStages) & 1, s_abort, kTimeoutNs);
+                // S(0) of both tiles.  The P V that read each tile's last P of the
+                // previous item was issued before, and one thread's tcgen05
+                // operations execute in issue order.
+                if (nkv0 > 0) PA_ISSUE_S(0);
+                if (nkv1 > 0) PA_ISSUE_S(1);
+                tc::mma_commit(bar(kKEmpty0 + kc % kKStages));
+                ++kc;
+                if (ntiles == 1) tc::mma_commit(bar(kQEmpty));
+                for (int j = 0; j < ntiles && ok; ++j) {
+                    const bool nxt0 = j + 1 < nkv0, nxt1 = j + 1 < nkv1;
+                    ok = tc::mbar_wait(bar(kVFull0 + vc % kVStages), (vc / kVStages) & 1, s_abort, kTimeoutNs);
                     if (!ok) break;
                     tc::tc_fence_after();
+                    if (j < nkv0) {
+                        // (P_A(0) of an item arrives after its softmax warps have
+                        // read the previous item's O_A, which this P V overwrites)
+                        if (!(ok = tc::mbar_wait(bar(kPFull0), pc0 & 1, s_abort, kTimeoutNs))) break;
+                        ++pc0;
+                        PA_ISSUE_PV(0, j);
+                    }
+                    if (nxt0 || nxt1) {
+                        ok = tc::mbar_wait(bar(kKFull0 + kc % kKStages), (kc / kKStages) & 1, s_abort, kTimeoutNs);
+                        if (!ok) break;
+                        tc::tc_fence_after();
+                    }
+                    if (nxt0) PA_ISSUE_S(0);
+                    if (j < nkv1) {
+                        if (!(ok = tc::mbar_wait(bar(kPFull0 + 1), pc1 & 1, s_abort, kTimeoutNs))) break;
+                        ++pc1;
+                        PA_ISSUE_PV(1, j);
+                    }
+                    tc::mma_commit(bar(kVEmpty0 + vc % kVStages));
+                    ++vc;
+                    if (nxt1) PA_ISSUE_S(1);
+                    if (nxt0 || nxt1) {
+                        tc::mma_commit(bar(kKEmpty0 + kc % kKStages));
+                        ++kc;
+                        if (j + 2 == ntiles) tc::mma_commit(bar(kQEmpty));  // the item's last S MMAs
+                    }
                 }
-                if (nxt0) PA_ISSUE_S(0, j + 1);
-                if (j < nkv1) {
-                    if (!(ok = tc::mbar_wait(bar(kPFull0 + 1), j & 1, s_abort, kTimeoutNs))) break;
-                    PA_ISSUE_PV(1, j);
-                }
-                tc::mma_commit(bar(kVEmpty0 + j % kVStages));
-                if (nxt1) PA_ISSUE_S(1, j + 1);
-                if (nxt0 || nxt1) tc::mma_commit(bar(kKEmpty0 + (j + 1) % kKStages));
             }
 #undef PA_ISSUE_S
 #undef PA_ISSUE_PV
@@ -481,7 +600,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             tc::mbar_wait(bar(kDrain), 0, nullptr, kTimeoutNs);
         }
         __syncwarp();
-    } else if (warp >= 2 && warp < 10) {
+    } else if (warp >= 2 && warp < 2 + 4 * kTiles) {
         // ======================================================== softmax
         const int x = (warp - 2) >> 2;        // tile: warps 2-5 -> A, 6-9 -> B
         const int quarter = warp & 3;         // TMEM lanes 32 * (warp % 4) ..
@@ -489,116 +608,136 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t lane_addr = tmem + (static_cast<uint32_t>(quarter * 32) << 16);
         const uint32_t s_addr = lane_addr + tmem_s(x);
         const uint32_t o_addr = lane_addr + tmem_o(x);
-        const int nt = nkv[x];
-        const bool valid = r < ntok[x] * G;
-        const int pos = valid ? prefix + i0 + x * tq_tokens + r / G : -1;  // causal limit of this row
         const float c = a.scale_log2;
-        float m_used = -INFINITY;  // running max, log2 units
-        uint64_t lsum[4] = {0, 0, 0, 0};  // 8 independent partial sums, in f32x2 pairs (0 = +0.0f, +0.0f)
-        for (int kt = 0; kt < nt; ++kt) {
-            if (!warp_wait(bar(kSFull0 + x), kt & 1, s_abort)) {
+        uint32_t sc = 0, oc = 0;  // S tiles and finished O of this tile so far
+        for (int it = 0; ok; ++it) {
+            const int slot = it & 1;
+            if (!warp_wait(bar(kItemFull0 + slot), (it >> 1) & 1, s_abort)) {
                 ok = false;
                 break;
             }
-            tc::tc_fence_after();
-            const int j0 = kt * kKeys;
-            const bool diag = __any_sync(0xffffffffu, j0 + kKeys - 1 > pos);
-            uint32_t sh[64];
-            // masked running max of 64 keys starting at key k0 of the tile
-            auto half_max = [&](int k0, float (&mx8)[8]) {
+            const Item itm = s_items[slot];
+            __syncwarp();
+            if (lane == 0) tc::mbar_arrive(bar(kItemEmpty0 + slot));
+            if (itm.b < 0) break;
+            const ItemShape shp = shape_of(itm, tq_tokens, kTiles);
+            const int nt = x ? shp.nkv[1] : shp.nkv[0];
+            if (nt == 0) continue;
+            const int t0 = itm.i0 + x * tq_tokens;  // first new token of this tile
+            const bool valid = r < (x ? shp.ntok[1] : shp.ntok[0]) * G;
+            const int pos = valid ? shp.prefix + t0 + r / G : -1;  // causal limit of this row
+            float m_used = -INFINITY;  // running max, log2 units
+            uint64_t lsum[4] = {0, 0, 0, 0};  // 8 independent partial sums, in f32x2 pairs (0 = +0.0f, +0.0f)
+            for (int kt = 0; kt < nt; ++kt) {
+                if (!warp_wait(bar(kSFull0 + x), sc & 1, s_abort)) {
+                    ok = false;
+                    break;
+                }
+                ++sc;
+                tc::tc_fence_after();
+                const int j0 = kt * kKeys;
+                const bool diag = __any_sync(0xffffffffu, j0 + kKeys - 1 > pos);
+                uint32_t sh[64];
+                // masked running max of 64 keys starting at key k0 of the tile
+                auto half_max = [&](int k0, float (&mx8)[8]) {
+                    if (diag) {
+#pragma unroll
+                        for (int j = 0; j < 64; ++j)
+                            if (j0 + k0 + j > pos) sh[j] = __float_as_uint(-INFINITY);
+                    }
+#pragma unroll
+                    for (int j = 0; j < 64; j += 16)
+#pragma unroll
+                        for (int e = 0; e < 8; ++e)
+                            mx8[e] = max3(mx8[e], __uint_as_float(sh[j + e]), __uint_as_float(sh[j + 8 + e]));
+                };
+                float mx8[8];
+#pragma unroll
+                for (int e = 0; e < 8; ++e) mx8[e] = -INFINITY;
+                tc::tmem_ld64(s_addr, sh);
+                half_max(0, mx8);
+                tc::tmem_ld64(s_addr + 64, sh);  // keys 64-127 stay in registers
+                half_max(64, mx8);
+                const float mx =
+                    max3(max3(mx8[0], mx8[1], mx8[2]), max3(mx8[3], mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7]));
+                const float mnew = mx * c;  // scale > 0, so the max commutes with it
+                if (kt == 0) {
+                    m_used = mnew;
+                } else {
+                    const bool need = mnew > m_used + 8.f;
+                    if (__any_sync(0xffffffffu, need)) {
+                        // O holds tiles < kt: P V(kt-1) was issued before S(kt), and
+                        // the commit this warp waited for to read S(kt) completes only
+                        // after every earlier MMA of the issuing thread.
+                        const float alpha = need ? fast_exp2(m_used - mnew) : 1.f;
+#pragma unroll
+                        for (int q = 0; q < D / 32; ++q) {
+                            uint32_t o[32];
+                            tc::tmem_ld32(o_addr + q * 32, o);
+#pragma unroll
+                            for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
+                            tc::tmem_st32(o_addr + q * 32, o);
+                        }
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) {
+                            const float2 v = unpack2(lsum[e]);
+                            asm("mov.b64 %0, {%1, %2};\n" : "=l"(lsum[e]) : "f"(v.x * alpha), "f"(v.y * alpha));
+                        }
+                        if (need) m_used = mnew;
+                    }
+                }
+                const float nmu = m_used == -INFINITY ? 0.f : -m_used;
+                // P = 2^(s*c - m) as bf16 pairs into the last 64 columns of S: keys
+                // 64-127 (in registers) to columns 96-127, then keys 0-63 (loaded
+                // again) to columns 64-95; every column written has been read.  The
+                // P V that read the previous P finished before this S was written.
+                // l sums the fp32 values.
+                auto half_p = [&](uint32_t col) {
+                    uint32_t pk[32];
+#pragma unroll
+                    for (int e = 0; e < 32; ++e) {
+                        float y0, y1;
+                        fma2(y0, y1, __uint_as_float(sh[2 * e]), __uint_as_float(sh[2 * e + 1]), c, nmu);
+                        float x0, x1;
+                        if (PA_PREFILL_POLY_EVERY > 0 &&
+                            e % (PA_PREFILL_POLY_EVERY > 0 ? PA_PREFILL_POLY_EVERY : 1) ==
+                                (PA_PREFILL_POLY_EVERY > 0 ? PA_PREFILL_POLY_EVERY : 1) - 1) {
+                            x0 = poly_exp2(y0);
+                            x1 = poly_exp2(y1);
+                        } else {
+                            x0 = fast_exp2(y0);
+                            x1 = fast_exp2(y1);
+                        }
+                        pk[e] = pack_bf16(x0, x1);
+                        add2(lsum[e & 3], x0, x1);
+                    }
+                    tc::tmem_st32(s_addr + col, pk);
+                };
+                half_p(96);
+                tc::tmem_ld64(s_addr, sh);
                 if (diag) {
 #pragma unroll
                     for (int j = 0; j < 64; ++j)
-                        if (j0 + k0 + j > pos) sh[j] = __float_as_uint(-INFINITY);
+                        if (j0 + j > pos) sh[j] = __float_as_uint(-INFINITY);
                 }
-#pragma unroll
-                for (int j = 0; j < 64; j += 16)
-#pragma unroll
-                    for (int e = 0; e < 8; ++e)
-                        mx8[e] = max3(mx8[e], __uint_as_float(sh[j + e]), __uint_as_float(sh[j + 8 + e]));
-            };
-            float mx8[8];
-#pragma unroll
-            for (int e = 0; e < 8; ++e) mx8[e] = -INFINITY;
-            tc::tmem_ld64(s_addr, sh);
-            half_max(0, mx8);
-            tc::tmem_ld64(s_addr + 64, sh);  // keys 64-127 stay in registers
-            half_max(64, mx8);
-            const float mx = max3(max3(mx8[0], mx8[1], mx8[2]), max3(mx8[3], mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7]));
-            const float mnew = mx * c;  // scale > 0, so the max commutes with it
-            if (kt == 0) {
-                m_used = mnew;
-            } else {
-                const bool need = mnew > m_used + 8.f;
-                if (__any_sync(0xffffffffu, need)) {
-                    // O holds tiles < kt: P V(kt-1) was issued before S(kt), and
-                    // the commit this warp waited for to read S(kt) completes only
-                    // after every earlier MMA of the issuing thread.
-                    const float alpha = need ? fast_exp2(m_used - mnew) : 1.f;
-#pragma unroll
-                    for (int q = 0; q < D / 32; ++q) {
-                        uint32_t o[32];
-                        tc::tmem_ld32(o_addr + q * 32, o);
-#pragma unroll
-                        for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
-                        tc::tmem_st32(o_addr + q * 32, o);
-                    }
-#pragma unroll
-                    for (int e = 0; e < 4; ++e) {
-                        const float2 v = unpack2(lsum[e]);
-                        asm("mov.b64 %0, {%1, %2};\n" : "=l"(lsum[e]) : "f"(v.x * alpha), "f"(v.y * alpha));
-                    }
-                    if (need) m_used = mnew;
-                }
+                half_p(64);
+                tc::tc_fence_before();
+                __syncwarp();
+                if (lane == 0) tc::mbar_arrive(bar(kPFull0 + x));
             }
-            const float nmu = m_used == -INFINITY ? 0.f : -m_used;
-            // P = 2^(s*c - m) as bf16 pairs into the last 64 columns of S: keys
-            // 64-127 (in registers) to columns 96-127, then keys 0-63 (loaded
-            // again) to columns 64-95; every column written has been read.  The
-            // P V that read the previous P finished before this S was written.
-            // l sums the fp32 values.
-            auto half_p = [&](uint32_t col) {
-                uint32_t pk[32];
-#pragma unroll
-                for (int e = 0; e < 32; ++e) {
-                    float y0, y1;
-                    fma2(y0, y1, __uint_as_float(sh[2 * e]), __uint_as_float(sh[2 * e + 1]), c, nmu);
-                    float x0, x1;
-                    if (PA_PREFILL_POLY_EVERY > 0 && e % (PA_PREFILL_POLY_EVERY > 0 ? PA_PREFILL_POLY_EVERY : 1) ==
-                                                         (PA_PREFILL_POLY_EVERY > 0 ? PA_PREFILL_POLY_EVERY : 1) - 1) {
-                        x0 = poly_exp2(y0);
-                        x1 = poly_exp2(y1);
-                    } else {
-                        x0 = fast_exp2(y0);
-                        x1 = fast_exp2(y1);
-                    }
-                    pk[e] = pack_bf16(x0, x1);
-                    add2(lsum[e & 3], x0, x1);
-                }
-                tc::tmem_st32(s_addr + col, pk);
-            };
-            half_p(96);
-            tc::tmem_ld64(s_addr, sh);
-            if (diag) {
-#pragma unroll
-                for (int j = 0; j < 64; ++j)
-                    if (j0 + j > pos) sh[j] = __float_as_uint(-INFINITY);
+            if (!ok) break;
+            if (!warp_wait(bar(kODone0 + x), oc & 1, s_abort)) {
+                ok = false;
+                break;
             }
-            half_p(64);
-            tc::tc_fence_before();
-            __syncwarp();
-            if (lane == 0) tc::mbar_arrive(bar(kPFull0 + x));
-        }
-        if (ok && nt > 0) ok = warp_wait(bar(kODone0 + x), 0, s_abort);
-        if (ok && nt > 0) {
+            ++oc;
             tc::tc_fence_after();
             const float2 l0 = unpack2(lsum[0]), l1 = unpack2(lsum[1]), l2 = unpack2(lsum[2]), l3 = unpack2(lsum[3]);
             const float l = ((l0.x + l0.y) + (l1.x + l1.y)) + ((l2.x + l2.y) + (l3.x + l3.y));
             const float inv = valid ? 1.f / l : 0.f;
-            __nv_bfloat16* orow = out + (static_cast<int64_t>(q0 + i0 + x * tq_tokens + (valid ? r / G : 0)) *
-                                             a.num_q_heads +
-                                         h * G + r % G) *
-                                            D;
+            __nv_bfloat16* orow =
+                reinterpret_cast<__nv_bfloat16*>(a.out) +
+                (static_cast<int64_t>(itm.q0 + t0 + (valid ? r / G : 0)) * a.num_q_heads + itm.h * G + r % G) * D;
 #pragma unroll
             for (int q = 0; q < D / 32; ++q) {
                 uint32_t o[32];
@@ -615,7 +754,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                     }
                 }
             }
-        } else if (!ok && lane == 0) {
+            // (O has been read out: the next item's first P V, which overwrites
+            // O, waits for this warp's next P, arrived after this point.)
+        }
+        if (!ok && lane == 0) {
             *s_abort = 1;
             flag_error(a.err, kDevWaitTimeout);
         }
@@ -628,14 +770,24 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc::tc_fence_after();
         tc::tmem_dealloc(tmem, kTmemCols);
     }
+    // The last CTA to finish returns the item counters to zero for the next
+    // launch (every CTA's last fetch precedes its arrival here).
+    if (threadIdx.x == 0) {
+        __threadfence();
+        if (atomicAdd(a.sched + 1, 1) == static_cast<int>(gridDim.x) - 1) {
+            __threadfence();
+            atomicExch(a.sched, 0);
+            atomicExch(a.sched + 1, 0);
+        }
+    }
 }
 
 // --------------------------------------------------------------- host side
 int tokens_per_tile(int group) { return group <= kM ? kM / group : 0; }
 
-// Upper bound on the CTAs (tile pairs, or single tiles at D = 256) of any batch
-// with these shapes: sum over sequences of ceil(ceil(n_b / TQ) / k) =
-// sum of ceil(n_b / (k TQ)) <= T / (k TQ) + B, with k tiles per CTA.
+// Upper bound on the tile pairs (single tiles at D = 256) of any batch with these
+// shapes: sum over sequences of ceil(ceil(n_b / TQ) / k) = sum of
+// ceil(n_b / (k TQ)) <= T / (k TQ) + B, with k tiles per pair.
 int pairs_bound(const Args& a) {
     const int tq = tokens_per_tile(a.group);
     if (tq == 0) return 0;
@@ -655,8 +807,15 @@ cudaError_t launch_d(const Args& a, cudaStream_t stream) {
         if (e != cudaSuccess) return e;
         configured[dev & 63] = true;
     }
-    const int64_t ctas = prefill_ctas(a);
-    if (ctas == 0) return cudaSuccess;
+    const int64_t items = prefill_ctas(a);
+    if (items == 0) return cudaSuccess;
+    // one persistent CTA per SM (at most one per item)
+    static int sms[64] = {};
+    if (sms[dev & 63] == 0) {
+        cudaError_t e = cudaDeviceGetAttribute(&sms[dev & 63], cudaDevAttrMultiProcessorCount, dev);
+        if (e != cudaSuccess) return e;
+    }
+    const int64_t ctas = items < sms[dev & 63] ? items : sms[dev & 63];
     const int G = a.group, tq = tokens_per_tile(G);
     CUtensorMap tq_map, tk_map, tv_map;
     if (!encode_q_map(&tq_map, a.q, D, a.num_q_heads, a.num_tokens, G, tq) ||
@@ -664,11 +823,12 @@ cudaError_t launch_d(const Args& a, cudaStream_t stream) {
         !encode_cache_map(&tv_map, a.v_cache, D, a.num_kv_heads, a.num_blocks))
         return cudaErrorInvalidValue;
     return launch_kernel(prefill_tc_kernel<D>, static_cast<unsigned>(ctas), kThreads, S::kAlloc, stream, 1, tq_map,
-                         tk_map, tv_map, a, tq, pairs_bound(a));
+                         tk_map, tv_map, a, tq);
 }
 
 }  // namespace
 
+// Work items (tile pairs x KV heads) of the largest batch with these shapes.
 int64_t prefill_ctas(const Args& a) {
     if (a.num_tokens < 2) return 0;
     return static_cast<int64_t>(pairs_bound(a)) * a.num_kv_heads;

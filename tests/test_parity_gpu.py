@@ -339,6 +339,54 @@ def test_query_longer_than_context_flagged():
     assert torch.isfinite(got.float()).all()
 
 
+@pytest.mark.parametrize("D", [64, 128, 256])
+def test_prefill_items_beyond_the_grid(D):
+    """Several times more (tile pair, KV head) items than SMs: each persistent
+    prefill CTA takes items one after another from the item counter.  Sampled
+    rows against the oracle; two eager calls and a graph of three forwards,
+    replayed twice, bit-exact (the counter returns to zero after every launch)."""
+    n = [700, 1500, 300, 1200, 900, 2000]
+    p = [0, 333, 1000, 17, 2500, 64]
+    b = W.make_batch(n, [a + c for a, c in zip(n, p)], 32, 8, D, seed=77)
+    e1 = run(b)
+    e2 = run(b)
+    assert torch.equal(e1.view(torch.int16), e2.view(torch.int16))
+    rows = sample_rows(b, 300, seed=7)
+    ref = oracle.batch_attention(b, rows=rows)
+    assert_close(torch.stack([e1[t, h] for t, h in rows]), ref, f"prefill items beyond the grid, D {D}")
+    d = b.to("cuda")
+    outs = [torch.full_like(d.q, float("nan")) for _ in range(3)]
+    s = torch.cuda.Stream()
+    pa.prepare(d.q, d.k_cache, d.block_table, d.seq_lens, stream=s)
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s):
+        for o in outs:
+            pa.forward(d.q, d.k_cache, d.v_cache, d.block_table, d.seq_lens, d.query_start_loc, o, scale=b.scale)
+    for _ in range(2):
+        for o in outs:
+            o.fill_(float("nan"))
+        g.replay()
+        torch.cuda.synchronize()
+        assert pa.device_error(s) == 0
+        for o in outs:
+            assert torch.equal(o.cpu().view(torch.int16), e1.view(torch.int16))
+
+
+def test_prefill_query_longer_than_context_between_good_sequences():
+    """A prefill-sized query longer than its sequence (a contract violation) is
+    flagged and its rows written as zeros, without disturbing the items of the
+    sequences around it."""
+    b = W.make_batch([200, 150, 300], [400, 150, 300], 32, 8, 128, seed=78)
+    qsl = b.query_start_loc.tolist()
+    rows = [(t, h) for t in list(range(qsl[0], qsl[1], 7)) + list(range(qsl[2], qsl[3], 7)) for h in (0, 13, 31)]
+    ref = oracle.batch_attention(b, rows=rows)  # (the oracle refuses the broken batch below)
+    b.seq_lens[1] = 100  # 150 new tokens but 100 keys
+    got = run(b, check_errors=False)
+    assert pa.device_error() == 3
+    assert torch.equal(got[qsl[1]:qsl[2]].float(), torch.zeros_like(got[qsl[1]:qsl[2]].float()))
+    assert_close(torch.stack([got[t, h] for t, h in rows]), ref, "good sequences around a bad one")
+
+
 def test_many_splits_long_context():
     # 1024 splits of 64 keys for each of two 65536-key sequences: the split merge
     # reads a long run of partials and the ticket counters see many arrivals
