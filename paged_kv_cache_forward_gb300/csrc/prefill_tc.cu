@@ -15,15 +15,15 @@
 // mask bottom-right aligned ("Flash Attention in Triton"), online softmax,
 // O += P V, out = O / l.
 //
-// Warp roles (352 threads), each looping over the CTA's items:
-//   warps 0, 10 TMA producers: warp 0 resolves the items and per item loads
+// Warp roles (384 threads, three warpgroups), each looping over the CTA's items:
+//   warps 0, 2  TMA producers: warp 0 resolves the items and per item loads
 //               both Q tiles and the K page boxes (64 columns x 16 slots of one
-//               page and head, 128-byte swizzle) into a 3-stage K ring; warp 10
-//               the V page boxes into a
-//               2-stage V ring, each running ahead on its own.  Block-table
-//               entries are fetched one group of 4 tiles ahead.  The one page of
-//               V that holds the sequence end is copied by plain loads with zero
-//               fill, so no slot past seq_len reaches the MMA.
+//               page and head, 128-byte swizzle) into a 3-stage K ring; warp 2
+//               the V page boxes into a 2-stage V ring, each running ahead on
+//               its own.  Block-table entries are fetched one group of 4 tiles
+//               ahead.  The one page of V that holds the sequence end is copied
+//               by plain loads with zero fill, so no slot past seq_len reaches
+//               the MMA.
 //   warp 1      allocates all 512 TMEM columns (S and O of each tile); its lane 0
 //               issues the MMAs in the order
 //                   O_A += P_A(j) V(j),  S_A(j+1) = Q_A K(j+1)^T,
@@ -33,13 +33,13 @@
 //               last 64 columns of its tile's S; the MMA that next overwrites S
 //               is issued after the P V that reads it, and tcgen05 operations of
 //               one thread execute in issue order.
-//   warps 2-5   softmax of tile A, warps 6-9 softmax of tile B: one thread per
-//               row (TMEM lane).  Load S from TMEM in two 64-column halves,
-//               mask, running max in log2 units, P = 2^(x - m) stored straight
-//               into TMEM (keys 64-127 from registers, then keys 0-63 loaded
-//               again, so only half of S is in registers).  The running max
-//               is only moved (and O in TMEM rescaled) when the row max grows by
-//               more than 2^8; the final O / l is exact either way.
+//   (warp 3 idle; warpgroup 0 gives registers to the softmax warpgroups)
+//   warps 4-7   softmax of tile A, warps 8-11 softmax of tile B: one thread per
+//               row (TMEM lane).  The whole S row is loaded from TMEM at once,
+//               masked, its max taken in log2 units, and P = 2^(x - m) stored
+//               straight into TMEM in four stores of 32 keys with one wait.  The
+//               running max is only moved (and O in TMEM rescaled) when the row
+//               max grows by more than 2^8; the final O / l is exact either way.
 // Every wait on an mbarrier is bounded (2 s); on timeout the CTA records
 // kDevWaitTimeout, stops all roles, drains the MMAs it issued, frees TMEM and
 // exits.
@@ -56,8 +56,14 @@
 namespace pa {
 namespace {
 
-constexpr int kThreads = 352;
-constexpr int kWarpV = 10;  // the V producer
+constexpr int kThreads = 384;
+constexpr int kWarpV = 2;  // the V producer
+// Registers per thread after the split: warpgroup 0 (producers, MMA issuer)
+// gives registers to the two softmax warpgroups, whose whole S row (128 fp32)
+// stays in registers.  384 threads launch with 168 each (64512);
+// 128 x 104 + 256 x 200 = 64512.  The launcher checks the launch count.
+constexpr uint32_t kRegsLaunch = 168, kRegsIssue = 104, kRegsSoftmax = 200;
+static_assert(128 * kRegsIssue + 256 * kRegsSoftmax <= kThreads * kRegsLaunch, "register split above the launch");
 constexpr int kM = 128;            // rows per tile
 constexpr int kKeys = 128;         // keys per KV tile
 constexpr int kPage = 16;
@@ -125,6 +131,12 @@ __device__ __forceinline__ int tiles_of(int n, int tq, int qmax) { return n > qm
 __device__ __forceinline__ int ctas_of(int n, int tq, int qmax, int tiles_per_cta) {
     return (tiles_of(n, tq, qmax) + tiles_per_cta - 1) / tiles_per_cta;
 }
+
+// Register budget of the calling warpgroup (every warp of it executes the same one).
+template <uint32_t N>
+__device__ __forceinline__ void reg_dec() { asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;\n" ::"n"(N)); }
+template <uint32_t N>
+__device__ __forceinline__ void reg_inc() { asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;\n" ::"n"(N)); }
 
 // Bounded wait by every lane of a warp; the result is made warp-uniform so that a
 // timeout can never leave some lanes at a warp-collective instruction alone.
@@ -354,6 +366,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     bool ok = true;
 
     if (warp == 0 || warp == kWarpV) {
+        reg_dec<kRegsIssue>();
         // ==================== scheduler + Q and K producer (warp 0), V producer (warp 10)
         const bool is_v = warp == kWarpV;
         if (lane == 0) {
@@ -507,6 +520,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
     } else if (warp == 1) {
         // ===================================================== MMA issuer
+        reg_dec<kRegsIssue>();
         if (lane == 0) {
             constexpr uint32_t kIdQK = tc::idesc_bf16_f32(kM, kKeys, false, false);
             constexpr uint32_t kIdPV = tc::idesc_bf16_f32(kM, D, false, true);
@@ -600,9 +614,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             tc::mbar_wait(bar(kDrain), 0, nullptr, kTimeoutNs);
         }
         __syncwarp();
-    } else if (warp >= 2 && warp < 2 + 4 * kTiles) {
+    } else if (warp >= 4 && warp < 4 + 4 * kTiles) {
         // ======================================================== softmax
-        const int x = (warp - 2) >> 2;        // tile: warps 2-5 -> A, 6-9 -> B
+        reg_inc<kRegsSoftmax>();
+        const int x = (warp - 4) >> 2;        // tile: warps 4-7 -> A, 8-11 -> B
         const int quarter = warp & 3;         // TMEM lanes 32 * (warp % 4) ..
         const int r = quarter * 32 + lane;    // row == TMEM lane
         const uint32_t lane_addr = tmem + (static_cast<uint32_t>(quarter * 32) << 16);
@@ -637,47 +652,37 @@ __global__ void __launch_bounds__(kThreads, 1)
                 tc::tc_fence_after();
                 const int j0 = kt * kKeys;
                 const bool diag = __any_sync(0xffffffffu, j0 + kKeys - 1 > pos);
-                uint32_t sh[64];
-                // masked running max of 64 keys starting at key k0 of the tile
-                auto half_max = [&](int k0, float (&mx8)[8]) {
-                    if (diag) {
+                // The whole S row in one load and one wait.
+                uint32_t sh[128];
+                tc::tmem_ld128(s_addr, sh);
+                if (diag) {
 #pragma unroll
-                        for (int j = 0; j < 64; ++j)
-                            if (j0 + k0 + j > pos) sh[j] = __float_as_uint(-INFINITY);
-                    }
-#pragma unroll
-                    for (int j = 0; j < 64; j += 16)
-#pragma unroll
-                        for (int e = 0; e < 8; ++e)
-                            mx8[e] = max3(mx8[e], __uint_as_float(sh[j + e]), __uint_as_float(sh[j + 8 + e]));
-                };
+                    for (int j = 0; j < 128; ++j)
+                        if (j0 + j > pos) sh[j] = __float_as_uint(-INFINITY);
+                }
                 float mx8[8];
 #pragma unroll
-                for (int e = 0; e < 8; ++e) mx8[e] = -INFINITY;
-                tc::tmem_ld64(s_addr, sh);
-                half_max(0, mx8);
-                tc::tmem_ld64(s_addr + 64, sh);  // keys 64-127 stay in registers
-                half_max(64, mx8);
+                for (int e = 0; e < 8; ++e) mx8[e] = max3(__uint_as_float(sh[e]), __uint_as_float(sh[8 + e]),
+                                                          __uint_as_float(sh[16 + e]));
+#pragma unroll
+                for (int j = 24; j < 120; j += 16)
+#pragma unroll
+                    for (int e = 0; e < 8; ++e)
+                        mx8[e] = max3(mx8[e], __uint_as_float(sh[j + e]), __uint_as_float(sh[j + 8 + e]));
+#pragma unroll
+                for (int e = 0; e < 8; ++e) mx8[e] = fmaxf(mx8[e], __uint_as_float(sh[120 + e]));
                 const float mx =
                     max3(max3(mx8[0], mx8[1], mx8[2]), max3(mx8[3], mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7]));
                 const float mnew = mx * c;  // scale > 0, so the max commutes with it
+                float alpha = 1.f;
+                bool rescale = false;
                 if (kt == 0) {
                     m_used = mnew;
                 } else {
                     const bool need = mnew > m_used + 8.f;
                     if (__any_sync(0xffffffffu, need)) {
-                        // O holds tiles < kt: P V(kt-1) was issued before S(kt), and
-                        // the commit this warp waited for to read S(kt) completes only
-                        // after every earlier MMA of the issuing thread.
-                        const float alpha = need ? fast_exp2(m_used - mnew) : 1.f;
-#pragma unroll
-                        for (int q = 0; q < D / 32; ++q) {
-                            uint32_t o[32];
-                            tc::tmem_ld32(o_addr + q * 32, o);
-#pragma unroll
-                            for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
-                            tc::tmem_st32(o_addr + q * 32, o);
-                        }
+                        alpha = need ? fast_exp2(m_used - mnew) : 1.f;
+                        rescale = true;
 #pragma unroll
                         for (int e = 0; e < 4; ++e) {
                             const float2 v = unpack2(lsum[e]);
@@ -687,40 +692,40 @@ __global__ void __launch_bounds__(kThreads, 1)
                     }
                 }
                 const float nmu = m_used == -INFINITY ? 0.f : -m_used;
-                // P = 2^(s*c - m) as bf16 pairs into the last 64 columns of S: keys
-                // 64-127 (in registers) to columns 96-127, then keys 0-63 (loaded
-                // again) to columns 64-95; every column written has been read.  The
-                // P V that read the previous P finished before this S was written.
-                // l sums the fp32 values.
-                auto half_p = [&](uint32_t col) {
-                    uint32_t pk[32];
+                // P = 2^(s*c - m) as bf16 pairs into the last 64 columns of S
+                // (key k to column 64 + k / 2), 32 keys per store; S is all in
+                // registers, so any column may be overwritten.  The P V that read
+                // the previous P finished before this S was written.  l sums the
+                // fp32 values.
 #pragma unroll
-                    for (int e = 0; e < 32; ++e) {
+                for (int ch = 0; ch < 4; ++ch) {
+                    uint32_t pk[16];
+#pragma unroll
+                    for (int e = 0; e < 16; ++e) {
                         float y0, y1;
-                        fma2(y0, y1, __uint_as_float(sh[2 * e]), __uint_as_float(sh[2 * e + 1]), c, nmu);
-                        float x0, x1;
-                        if (PA_PREFILL_POLY_EVERY > 0 &&
-                            e % (PA_PREFILL_POLY_EVERY > 0 ? PA_PREFILL_POLY_EVERY : 1) ==
-                                (PA_PREFILL_POLY_EVERY > 0 ? PA_PREFILL_POLY_EVERY : 1) - 1) {
-                            x0 = poly_exp2(y0);
-                            x1 = poly_exp2(y1);
-                        } else {
-                            x0 = fast_exp2(y0);
-                            x1 = fast_exp2(y1);
-                        }
+                        fma2(y0, y1, __uint_as_float(sh[32 * ch + 2 * e]), __uint_as_float(sh[32 * ch + 2 * e + 1]), c,
+                             nmu);
+                        const float x0 = fast_exp2(y0), x1 = fast_exp2(y1);
                         pk[e] = pack_bf16(x0, x1);
                         add2(lsum[e & 3], x0, x1);
                     }
-                    tc::tmem_st32(s_addr + col, pk);
-                };
-                half_p(96);
-                tc::tmem_ld64(s_addr, sh);
-                if (diag) {
-#pragma unroll
-                    for (int j = 0; j < 64; ++j)
-                        if (j0 + j > pos) sh[j] = __float_as_uint(-INFINITY);
+                    tc::tmem_st16_async(s_addr + 64 + 16 * ch, pk);
                 }
-                half_p(64);
+                tc::tmem_wait_st();
+                if (rescale) {
+                    // O holds tiles < kt: P V(kt-1) was issued before S(kt), and
+                    // the commit this warp waited for to read S(kt) completes only
+                    // after every earlier MMA of the issuing thread; P V(kt) waits
+                    // for this warp's arrival below.
+#pragma unroll
+                    for (int q = 0; q < D / 32; ++q) {
+                        uint32_t o[32];
+                        tc::tmem_ld32(o_addr + q * 32, o);
+#pragma unroll
+                        for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
+                        tc::tmem_st32(o_addr + q * 32, o);
+                    }
+                }
                 tc::tc_fence_before();
                 __syncwarp();
                 if (lane == 0) tc::mbar_arrive(bar(kPFull0 + x));
@@ -761,6 +766,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             *s_abort = 1;
             flag_error(a.err, kDevWaitTimeout);
         }
+    } else if (warp < 4) {
+        reg_dec<kRegsIssue>();  // idle warp of warpgroup 0
+    } else {
+        reg_inc<kRegsSoftmax>();  // idle softmax warps (one query tile per CTA)
     }
 
     // ---- teardown: every role is out of its loop; the MMA thread has drained.
@@ -805,6 +814,12 @@ cudaError_t launch_d(const Args& a, cudaStream_t stream) {
         cudaError_t e = cudaFuncSetAttribute(prefill_tc_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                              S::kAlloc);
         if (e != cudaSuccess) return e;
+        // The warpgroups' register split must fit in what the CTA launches with,
+        // or setmaxnreg.inc would wait for registers that never come.
+        cudaFuncAttributes fa{};
+        e = cudaFuncGetAttributes(&fa, prefill_tc_kernel<D>);
+        if (e != cudaSuccess) return e;
+        if (static_cast<uint32_t>(fa.numRegs) < kRegsLaunch) return cudaErrorInvalidConfiguration;
         configured[dev & 63] = true;
     }
     const int64_t items = prefill_ctas(a);
