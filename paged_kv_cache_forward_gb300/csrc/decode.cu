@@ -55,14 +55,18 @@ struct DecodeTile {
     static constexpr int kStageBytes = 2 * kPageBytes;          // K then V
     static constexpr int kWarpBytes = kStages * kStageBytes;
     static constexpr int kPipeBytes = kWarps * kWarpBytes;
-    // merge area: per warp O[16][D + 8] fp32 (the padding makes the fragment
-    // stores bank-conflict free) + m[16] + l[16]; then the CTA's merged partial
-    // O[16][D] + m[16] + l[16] (read by the other CTAs of a cluster)
+    // merge area (over the pipeline, once it is drained): per warp O[16][D + 8]
+    // fp32 (the padding makes the fragment stores bank-conflict free) + m[16] + l[16]
     static constexpr int kMS = D + 8;  // row stride of a warp's O
     static constexpr int kMergeWarpFloats = kRows * kMS + 2 * kRows;
-    static constexpr int kCtaPartialOffFloats = kWarps * kMergeWarpFloats;
-    static constexpr int kMergeBytes = (kWarps * kMergeWarpFloats + kRows * D + 2 * kRows) * 4;
+    static constexpr int kMergeBytes = kWarps * kMergeWarpFloats * 4;
     static constexpr int kSmemBytes = kPipeBytes > kMergeBytes ? kPipeBytes : kMergeBytes;
+    // Cluster mode only, after that: the partials the cluster's CTAs push to
+    // this one, O[src][16][cols] (cols = ceil(D / C), so C * cols <= D + C - 1)
+    // and (m, l)[src][16].  Separate from the pipeline, which may still be busy
+    // when a faster peer pushes.
+    static constexpr int kRecvOFloats = kRows * (D + kMaxCluster);
+    static constexpr int kRecvBytes = (kRecvOFloats + kMaxCluster * kRows * 2) * 4;
 };
 
 // Byte offset of 16-byte chunk c of row r: chunks are XOR-permuted by r % 8.
@@ -155,12 +159,23 @@ __device__ __forceinline__ int ldg_s32(const int32_t* p) {
 __device__ __forceinline__ void cluster_sync() {
     asm volatile("barrier.cluster.arrive.release.aligned;\nbarrier.cluster.wait.acquire.aligned;\n" ::: "memory");
 }
-__device__ __forceinline__ float ld_peer(const float* local, uint32_t peer) {
+// The two halves of a cluster barrier: arrive (relaxed: nothing to publish yet)
+// early, wait just before the first access to a peer's shared memory, so that
+// every peer has started by then.
+__device__ __forceinline__ void cluster_arrive_relaxed() {
+    asm volatile("barrier.cluster.arrive.relaxed.aligned;\n" ::: "memory");
+}
+__device__ __forceinline__ void cluster_wait() { asm volatile("barrier.cluster.wait.aligned;\n" ::: "memory"); }
+// Stores v into peer CTA `peer`'s shared memory at the offset of `local` here.
+__device__ __forceinline__ void st_peer(float* local, uint32_t peer, float v) {
     uint32_t addr = smem_u32(local), remote;
-    float v;
     asm volatile("mapa.shared::cluster.u32 %0, %1, %2;\n" : "=r"(remote) : "r"(addr), "r"(peer));
-    asm volatile("ld.shared::cluster.f32 %0, [%1];\n" : "=f"(v) : "r"(remote) : "memory");
-    return v;
+    asm volatile("st.shared::cluster.f32 [%0], %1;\n" ::"r"(remote), "f"(v) : "memory");
+}
+__device__ __forceinline__ void st_peer2(float* local, uint32_t peer, float x, float y) {
+    uint32_t addr = smem_u32(local), remote;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;\n" : "=r"(remote) : "r"(addr), "r"(peer));
+    asm volatile("st.shared::cluster.v2.f32 [%0], {%1, %2};\n" ::"r"(remote), "f"(x), "f"(y) : "memory");
 }
 
 // 4-warp CTAs are sized to share an SM three at a time (at most 170 registers),
@@ -252,6 +267,7 @@ __global__ void __launch_bounds__(kWarps * 32, (kWarps == 4 && D <= 128) ? 3 : 1
     }
     const int npages = (end - start + kPage - 1) / kPage;  // 0 for an empty split of a cluster
     const int my_pages = warp < npages ? (npages - warp + kWarps - 1) / kWarps : 0;
+    if (clustered) cluster_arrive_relaxed();  // waited for before the first push to a peer
 
     // Block-table entries of this warp's pages, 32 at a time in registers (lane l
     // holds the entry of the warp's page 32 * round + l), the next round loaded
@@ -434,7 +450,13 @@ __global__ void __launch_bounds__(kWarps * 32, (kWarps == 4 && D <= 128) ? 3 : 1
     // This CTA's (O, m, l) for row r: over the warps, M = max m_w, then
     // O = sum 2^(m_w - M) O_w and l likewise.
     const float* ms = reinterpret_cast<const float*>(smem);
-    float* cta = reinterpret_cast<float*>(smem) + Tile::kCtaPartialOffFloats;  // [16][D] O, [16] m, [16] l
+    // Cluster mode: CTA c of the cluster owns columns [c * cols, (c + 1) * cols)
+    // and receives every CTA's partial of them.
+    const int C = a.splits;
+    const int ccols = clustered ? (D + C - 1) / C : D;
+    float* recv_o = reinterpret_cast<float*>(smem + Tile::kSmemBytes);  // [src][16][ccols]
+    float* recv_ml = recv_o + Tile::kRecvOFloats;                        // [src][16][2]
+    if (clustered) cluster_wait();  // every peer has started: its receive area exists
     for (int i = threadIdx.x; i < rows * D; i += blockDim.x) {
         const int r = i / D, d = i % D;
         float M = -INFINITY;
@@ -450,11 +472,10 @@ __global__ void __launch_bounds__(kWarps * 32, (kWarps == 4 && D <= 128) ? 3 : 1
             l += sc * mwr[kM0 + kRows + r];
         }
         if (clustered) {
-            cta[r * D + d] = acc;
-            if (d == 0) {
-                cta[kRows * D + r] = M;
-                cta[kRows * D + kRows + r] = l;
-            }
+            const int own = d / ccols;
+            st_peer(recv_o + (s * kRows + r) * ccols + (d - own * ccols), own, acc);
+            if (d == 0)
+                for (int c = 0; c < C; ++c) st_peer2(recv_ml + (s * kRows + r) * 2, c, M, l);
         } else if (nsplits == 1) {
             out[(static_cast<int64_t>(q0 + tok_of(r)) * a.num_q_heads + head_of(r)) * D + d] =
                 __float2bfloat16(acc / l);
@@ -469,52 +490,36 @@ __global__ void __launch_bounds__(kWarps * 32, (kWarps == 4 && D <= 128) ? 3 : 1
     }
 
     if (clustered) {
-        // Every CTA of the cluster merges D / C columns of every row, reading the
-        // C partials from the CTAs' shared memory; a CTA with no keys holds
-        // m = -inf and weight 0.  The second barrier keeps every CTA's shared
-        // memory alive until its peers have read it.
+        // Every CTA of the cluster has pushed its partial of each column block to
+        // the block's owner; after the barrier (release / acquire: the pushes are
+        // visible) each CTA merges its own columns from its shared memory.  A CTA
+        // with no keys pushed m = -inf and weight 0.  Nobody touches a peer's
+        // shared memory after the barrier, so a CTA may exit when it is done.
         cluster_sync();
-        const int C = a.splits;
-        // (m, l) of every row of every CTA, one remote load per thread, then the
-        // per-row weights 2^(m_c - M) / sum_c 2^(m_c - M) l_c.
-        __shared__ float s_w[kMaxCluster][kRows], s_lc[kMaxCluster][kRows];
-        for (int i = threadIdx.x; i < C * kRows; i += blockDim.x) {
-            const int c = i / kRows, r = i % kRows;
-            const float mc = r < rows ? ld_peer(cta + kRows * D + r, c) : -INFINITY;
-            const float lc = r < rows ? ld_peer(cta + kRows * D + kRows + r, c) : 0.f;
-            s_w[c][r] = mc;
-            s_lc[c][r] = lc;
-        }
-        __syncthreads();
+        __shared__ float s_w[kMaxCluster][kRows], s_inv[kRows];
         if (threadIdx.x < rows) {
             const int r = threadIdx.x;
             float M = -INFINITY;
-            for (int c = 0; c < C; ++c) M = fmaxf(M, s_w[c][r]);
+            for (int c = 0; c < C; ++c) M = fmaxf(M, recv_ml[(c * kRows + r) * 2]);
             float l = 0.f;
             for (int c = 0; c < C; ++c) {
-                const float w = s_w[c][r] == -INFINITY ? 0.f : fast_exp2(s_w[c][r] - M);
+                const float mc = recv_ml[(c * kRows + r) * 2];
+                const float w = mc == -INFINITY ? 0.f : fast_exp2(mc - M);
                 s_w[c][r] = w;
-                l += w * s_lc[c][r];
+                l += w * recv_ml[(c * kRows + r) * 2 + 1];
             }
-            const float inv = 1.f / l;
-            for (int c = 0; c < C; ++c) s_w[c][r] *= inv;
+            s_inv[r] = 1.f / l;
         }
         __syncthreads();
-        const int cols = (D + C - 1) / C;
-        const int d0 = s * cols;
-        const int ncols = max(0, min(cols, D - d0));
+        const int d0 = s * ccols;
+        const int ncols = max(0, min(ccols, D - d0));
         for (int i = threadIdx.x; i < rows * ncols; i += blockDim.x) {
-            const int r = i / ncols, d = d0 + i % ncols;
-            float v[kMaxCluster];
-#pragma unroll
-            for (int c = 0; c < kMaxCluster; ++c) v[c] = c < C ? ld_peer(cta + r * D + d, c) : 0.f;
+            const int r = i / ncols, j = i % ncols;
             float acc = 0.f;
-#pragma unroll
-            for (int c = 0; c < kMaxCluster; ++c)
-                if (c < C) acc += s_w[c][r] * v[c];
-            out[(static_cast<int64_t>(q0 + tok_of(r)) * a.num_q_heads + head_of(r)) * D + d] = __float2bfloat16(acc);
+            for (int c = 0; c < C; ++c) acc += s_w[c][r] * recv_o[(c * kRows + r) * ccols + j];
+            out[(static_cast<int64_t>(q0 + tok_of(r)) * a.num_q_heads + head_of(r)) * D + d0 + j] =
+                __float2bfloat16(acc * s_inv[r]);
         }
-        cluster_sync();
         return;
     }
     if (nsplits == 1) return;
@@ -548,15 +553,16 @@ cudaError_t launch_decode_d(const Args& a, cudaStream_t stream) {
     int dev = 0;
     cudaGetDevice(&dev);
     if (!configured[dev & 63]) {
-        cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, Tile::kSmemBytes);
+        cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             Tile::kSmemBytes + Tile::kRecvBytes);
         if (e == cudaSuccess) e = cudaFuncSetAttribute(kernel, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
         if (e != cudaSuccess) return e;
         configured[dev & 63] = true;
     }
     const int64_t ctas = decode_ctas(a);
     if (ctas == 0) return cudaSuccess;
-    return launch_kernel(kernel, static_cast<unsigned>(ctas), kWarps * 32, Tile::kSmemBytes, stream,
-                         a.decode_cluster, a);
+    const size_t smem = Tile::kSmemBytes + (a.decode_cluster > 1 ? Tile::kRecvBytes : 0);
+    return launch_kernel(kernel, static_cast<unsigned>(ctas), kWarps * 32, smem, stream, a.decode_cluster, a);
 }
 
 template <int D>
