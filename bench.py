@@ -473,9 +473,14 @@ def run_ours(args):
         roof = {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
                 "peak_source": src}
     traffic = committed_traffic(dominant, args.config)
+    qs = statistics.quantiles(kernel_ms, n=10) if len(kernel_ms) >= 2 else [k_ms] * 9
     roof.update({"traffic": traffic, "kernel": dominant, "kernel_ms_mean": k_ms,
                  "kernel_ms_median": statistics.median(kernel_ms),
+                 "kernel_ms_p10": qs[0], "kernel_ms_p90": qs[-1],
                  "algorithmic_per_launch": work["flops"] if dominant == "prefill" else work["decode_bytes"]})
+
+    hbm_frac = (total_kv / world) / (ms_per_step / 1e3) / 1e9 / peaks["hbm"][0]
+    tensor_frac = (total_flops / world) / (ms_per_step / 1e3) / 1e12 / peaks["bf16"][0]
 
     # end to end through the public API: pinned host inputs -> device, forward, result -> host
     e2e = None
@@ -631,7 +636,14 @@ def run_ours(args):
                 "parallelism": f"dp{world}" if world > 1 else "single GPU",
             },
             "tok_s": total_tokens * steps / (region_ms_max / 1e3),
-            "hbm_frac_step": (total_kv / world) / (ms_per_step / 1e3) / 1e9 / peaks["hbm"][0],
+            # one attention layer per step; a 32-layer model's attention alone
+            # could run at most this many tokens/s
+            "tok_s_32_layer_attention_ceiling": total_tokens * steps / (region_ms_max / 1e3) / 32,
+            # whole step against each roofline: KV bytes / HBM, causal FLOPs /
+            # bf16 tensor peak, and the binding one, max(B / BW, F / peak) / t
+            "hbm_frac_step": hbm_frac,
+            "tensor_frac_step": tensor_frac,
+            "roofline_frac_step": max(hbm_frac, tensor_frac),
             "roofline": roof,
             "cpu_baseline": cpu,
             "e2e": e2e,
