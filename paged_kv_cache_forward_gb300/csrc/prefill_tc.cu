@@ -705,7 +705,16 @@ __global__ void __launch_bounds__(kThreads, 1)
                         float y0, y1;
                         fma2(y0, y1, __uint_as_float(sh[32 * ch + 2 * e]), __uint_as_float(sh[32 * ch + 2 * e + 1]), c,
                              nmu);
-                        const float x0 = fast_exp2(y0), x1 = fast_exp2(y1);
+                        float x0, x1;
+                        if (PA_PREFILL_POLY_EVERY > 0 &&
+                            e % (PA_PREFILL_POLY_EVERY > 0 ? PA_PREFILL_POLY_EVERY : 1) ==
+                                (PA_PREFILL_POLY_EVERY > 0 ? PA_PREFILL_POLY_EVERY : 1) - 1) {
+                            x0 = poly_exp2(y0);
+                            x1 = poly_exp2(y1);
+                        } else {
+                            x0 = fast_exp2(y0);
+                            x1 = fast_exp2(y1);
+                        }
                         pk[e] = pack_bf16(x0, x1);
                         add2(lsum[e & 3], x0, x1);
                     }
