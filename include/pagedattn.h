@@ -47,7 +47,14 @@
  * of pa_forward reads device memory on the host or synchronises, and its launch
  * grids depend only on the pa_dims, so it can be captured in a CUDA graph and
  * replayed with new contents of the same buffers (the "static launch grid" and
- * "CUDA / HIP Graphs" items of the same five-step list).
+ * "CUDA / HIP Graphs" items of the same five-step list).  When the dims allow
+ * both decode and prefill rows, the prefill kernel runs on a second stream the
+ * library keeps per (device, stream), forked from the given stream by an event
+ * and joined back by another before the call returns: work enqueued on the
+ * stream before the call happens before both kernels, work enqueued after it
+ * after both, and a capture records the fork and the join (pa_prepare creates
+ * that stream; a call captured without it launches both kernels on the given
+ * stream, one after the other).
  *
  * Scratch memory.  Splitting a long key range needs a workspace of
  * pa_plan(...).workspace_bytes bytes, which the library allocates and caches per

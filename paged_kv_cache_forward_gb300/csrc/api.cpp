@@ -184,6 +184,40 @@ std::mutex g_ws_mutex;
 std::vector<Workspace> g_ws;       // live, one per (device, stream)
 std::vector<Workspace> g_retired;  // outgrown buffers, kept for captured graphs
 
+// A second stream per (device, stream) on which the prefill kernel of a mixed
+// batch runs beside the decode kernel: forked from and joined back into the
+// caller's stream by two events, so the call stays stream-ordered and a capture
+// records the fork and the join.  The prefill kernel's CTAs then take the SMs
+// that the decode kernel's last wave leaves idle.
+struct SideStream {
+    int device;
+    cudaStream_t stream;  // the caller's
+    cudaStream_t side;
+    cudaEvent_t fork, join;
+};
+std::vector<SideStream> g_side;
+
+// The side stream of (device, stream), created if allowed (never while the
+// stream is capturing); nullptr if there is none.
+SideStream* get_side(cudaStream_t stream, bool may_create) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return nullptr;
+    std::lock_guard<std::mutex> lock(g_ws_mutex);
+    for (SideStream& x : g_side)
+        if (x.device == dev && x.stream == stream) return &x;
+    if (!may_create) return nullptr;
+    SideStream n{dev, stream, nullptr, nullptr, nullptr};
+    if (cudaStreamCreateWithFlags(&n.side, cudaStreamNonBlocking) != cudaSuccess) return nullptr;
+    if (cudaEventCreateWithFlags(&n.fork, cudaEventDisableTiming) != cudaSuccess ||
+        cudaEventCreateWithFlags(&n.join, cudaEventDisableTiming) != cudaSuccess) {
+        if (n.fork) cudaEventDestroy(n.fork);
+        cudaStreamDestroy(n.side);
+        return nullptr;
+    }
+    g_side.push_back(n);
+    return &g_side.back();
+}
+
 // Returns the workspace of (device, stream) able to hold a call that needs a
 // counter area of `counter_bytes` and `bytes` in all (at that counter size),
 // growing it if allowed.  A new buffer is zeroed (error word and split counters
@@ -293,8 +327,10 @@ pa_status pa_prepare(const pa_dims* dims, const pa_options* opts, void* stream) 
     if (e != cudaSuccess) return cuda_fail(e, "cudaStreamIsCapturing");
     if (cs != cudaStreamCaptureStatusNone) return fail(PA_ERR_INVALID_ARG, "pa_prepare called during capture");
     void* ws = nullptr;
-    return get_workspace(s, p.ws_bytes > kErrWordBytes ? p.ws_bytes : kErrWordBytes, p.counter_bytes, true, &ws,
-                         nullptr);
+    st = get_workspace(s, p.ws_bytes > kErrWordBytes ? p.ws_bytes : kErrWordBytes, p.counter_bytes, true, &ws,
+                       nullptr);
+    if (st == PA_OK && p.decode_ctas > 0 && p.prefill_ctas > 0) get_side(s, true);
+    return st;
 }
 
 pa_status pa_forward_ex(const void* q, const void* k_cache, const void* v_cache, const int32_t* block_table,
@@ -337,12 +373,27 @@ pa_status pa_forward_ex(const void* q, const void* k_cache, const void* v_cache,
     a.scale_log2 = scale * 1.4426950408889634f;
 
     const bool capturing = cs != cudaStreamCaptureStatusNone;
+    // Both kernels: the prefill one on the side stream, forked after everything
+    // before this call on s and joined back before anything after it.  The two
+    // kernels touch disjoint rows of out and disjoint workspace words.
+    SideStream* side = (p.decode_ctas > 0 && p.prefill_ctas > 0) ? get_side(s, !capturing) : nullptr;
+    cudaStream_t ps = s;
+    if (side) {
+        if ((e = cudaEventRecord(side->fork, s)) != cudaSuccess) return cuda_fail(e, "cudaEventRecord(fork)");
+        if ((e = cudaStreamWaitEvent(side->side, side->fork, 0)) != cudaSuccess)
+            return cuda_fail(e, "cudaStreamWaitEvent(fork)");
+        ps = side->side;
+    }
     if ((st = record(opts ? opts->decode_start_event : nullptr, s, capturing)) != PA_OK) return st;
     if ((e = pa::launch_decode(a, s)) != cudaSuccess) return cuda_fail(e, "decode launch");
     if ((st = record(opts ? opts->decode_stop_event : nullptr, s, capturing)) != PA_OK) return st;
-    if ((st = record(opts ? opts->prefill_start_event : nullptr, s, capturing)) != PA_OK) return st;
-    if ((e = pa::launch_prefill(a, s)) != cudaSuccess) return cuda_fail(e, "prefill launch");
-    if ((st = record(opts ? opts->prefill_stop_event : nullptr, s, capturing)) != PA_OK) return st;
+    if ((st = record(opts ? opts->prefill_start_event : nullptr, ps, capturing)) != PA_OK) return st;
+    if ((e = pa::launch_prefill(a, ps)) != cudaSuccess) return cuda_fail(e, "prefill launch");
+    if ((st = record(opts ? opts->prefill_stop_event : nullptr, ps, capturing)) != PA_OK) return st;
+    if (side) {
+        if ((e = cudaEventRecord(side->join, ps)) != cudaSuccess) return cuda_fail(e, "cudaEventRecord(join)");
+        if ((e = cudaStreamWaitEvent(s, side->join, 0)) != cudaSuccess) return cuda_fail(e, "cudaStreamWaitEvent(join)");
+    }
     return PA_OK;
 }
 
@@ -415,6 +466,13 @@ pa_status pa_release_workspaces(void) {
     };
     drop(g_ws);
     drop(g_retired);
+    for (SideStream& x : g_side) {
+        cudaSetDevice(x.device);
+        cudaEventDestroy(x.fork);
+        cudaEventDestroy(x.join);
+        cudaStreamDestroy(x.side);
+    }
+    g_side.clear();
     cudaSetDevice(cur);
     return st;
 }
