@@ -132,7 +132,8 @@ typedef struct {
     int64_t decode_ctas;      /* decode kernel grid                            */
     int64_t combine_ctas;     /* 0: the log-sum-exp merge of the splits runs in
                                  the decode kernel (last split CTA to finish) */
-    int64_t prefill_ctas;     /* prefill kernel grid                           */
+    int64_t prefill_ctas;     /* prefill work items (tile pairs x KV heads); its
+                                 persistent kernel runs min(this, SMs) CTAs    */
     int64_t workspace_bytes;  /* scratch this call needs                       */
     int32_t launches;         /* kernels launched per pa_forward               */
     int32_t decode_stages;    /* decode pipeline depth (pages per warp)        */

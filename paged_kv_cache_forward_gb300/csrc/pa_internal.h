@@ -124,7 +124,8 @@ void set_last_error(const char* msg);
 // (4, 2..4), (8, 2..3), (12, 2); at head_dim 256 only (4, 2..3).
 bool decode_variant_supported(int head_dim, int warps, int stages);
 
-// Static grid sizes (functions of shapes only), shared with the planner.
+// Static grid sizes (functions of shapes only), shared with the planner; for
+// the persistent prefill kernel, its work items (the grid is min(items, SMs)).
 int64_t decode_ctas(const Args& a);
 int64_t prefill_ctas(const Args& a);
 

@@ -117,7 +117,7 @@ enum Bar {
     kVFull0 = 7,    // [kMaxVStages = 2]
     kVEmpty0 = 9,   // [2]
     kSFull0 = 11,   // [2] per tile: S(j) in TMEM
-    kPFull0 = 13,   // [2] per tile: P(j) in TMEM (4 softmax warps arrive)
+    kPFull0 = 13,   // [2] per tile: P(j) in TMEM (its 4 softmax warps arrive)
     kODone0 = 15,   // [2] per tile: the tile's last O += P V of an item done
     kDrain = 17,
     kQEmpty = 18,      // the item's last S MMA has read Q
@@ -126,10 +126,10 @@ enum Bar {
 };
 
 // Tiles of a sequence with n new tokens (the decode path takes n <= qmax), and
-// the CTAs (pairs of tiles) they need.
+// the work items (pairs of tiles, or single tiles at D = 256) they make per KV head.
 __device__ __forceinline__ int tiles_of(int n, int tq, int qmax) { return n > qmax ? (n + tq - 1) / tq : 0; }
-__device__ __forceinline__ int ctas_of(int n, int tq, int qmax, int tiles_per_cta) {
-    return (tiles_of(n, tq, qmax) + tiles_per_cta - 1) / tiles_per_cta;
+__device__ __forceinline__ int pairs_of(int n, int tq, int qmax, int tiles_per_item) {
+    return (tiles_of(n, tq, qmax) + tiles_per_item - 1) / tiles_per_item;
 }
 
 // Register budget of the calling warpgroup (every warp of it executes the same one).
@@ -232,7 +232,7 @@ __device__ ItemStatus resolve_item(const Args& a, int w, int tq_tokens, Item& it
             s0 = a.query_start_loc[b];
             s1 = a.query_start_loc[b + 1];
         }
-        const int cnt = b < a.num_seqs ? ctas_of(s1 - s0, tq_tokens, a.decode_max_q, kTiles) : 0;
+        const int cnt = b < a.num_seqs ? pairs_of(s1 - s0, tq_tokens, a.decode_max_q, kTiles) : 0;
         int inc = cnt;
 #pragma unroll
         for (int o = 1; o < 32; o <<= 1) {
@@ -367,7 +367,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     if (warp == 0 || warp == kWarpV) {
         reg_dec<kRegsIssue>();
-        // ==================== scheduler + Q and K producer (warp 0), V producer (warp 10)
+        // ===================== scheduler + Q and K producer (warp 0), V producer (warp 2)
         const bool is_v = warp == kWarpV;
         if (lane == 0) {
             if (!is_v) {
