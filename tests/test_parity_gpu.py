@@ -304,6 +304,31 @@ def test_graph_replay_new_contents_bit_exact():
         assert torch.equal(out.cpu().view(torch.int16), e.view(torch.int16))
 
 
+def test_mixed_batch_is_ordered_on_the_callers_stream():
+    """The prefill kernel of a mixed batch runs on the library's side stream:
+    work enqueued on the caller's stream before the call (new q) must be seen by
+    it, and work enqueued after (a copy of out) must see its rows."""
+    b = W.make_batch([300, 1, 1, 150, 1], [800, 2000, 40, 150, 9000], 32, 8, 128, seed=79)
+    g = torch.Generator().manual_seed(80)
+    q2 = torch.randn(b.q.shape, generator=g).to(torch.bfloat16)
+    d = b.to("cuda")
+    q2d = q2.to("cuda")
+    out = torch.full_like(d.q, float("nan"))
+    s = torch.cuda.Stream()
+    pa.prepare(d.q, d.k_cache, d.block_table, d.seq_lens, stream=s)
+    torch.cuda.synchronize()
+    with torch.cuda.stream(s):
+        torch.cuda._sleep(2_000_000)  # keep the stream busy so that ordering matters
+        d.q.copy_(q2d)
+        pa.forward(d.q, d.k_cache, d.v_cache, d.block_table, d.seq_lens, d.query_start_loc, out, scale=b.scale,
+                   stream=s)
+        res = out.clone()
+    s.synchronize()
+    assert pa.device_error(s) == 0
+    b.q = q2
+    assert_close(res.cpu(), oracle.batch_attention(b), "mixed batch on a user stream")
+
+
 def test_capture_without_prepare_is_refused():
     b = W.make_batch([1], [50000], 32, 8, 128, seed=43, max_pages=4096, pool_pages=3200)
     d = b.to("cuda")
