@@ -197,25 +197,30 @@ struct SideStream {
 };
 std::vector<SideStream> g_side;
 
-// The side stream of (device, stream), created if allowed (never while the
-// stream is capturing); nullptr if there is none.
-SideStream* get_side(cudaStream_t stream, bool may_create) {
+// The side stream of (device, stream) into *out (a copy: the handles stay valid
+// until pa_release_workspaces), created if allowed (never while the stream is
+// capturing).  False if there is none.
+bool get_side(cudaStream_t stream, bool may_create, SideStream* out) {
     int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess) return nullptr;
+    if (cudaGetDevice(&dev) != cudaSuccess) return false;
     std::lock_guard<std::mutex> lock(g_ws_mutex);
-    for (SideStream& x : g_side)
-        if (x.device == dev && x.stream == stream) return &x;
-    if (!may_create) return nullptr;
+    for (const SideStream& x : g_side)
+        if (x.device == dev && x.stream == stream) {
+            *out = x;
+            return true;
+        }
+    if (!may_create) return false;
     SideStream n{dev, stream, nullptr, nullptr, nullptr};
-    if (cudaStreamCreateWithFlags(&n.side, cudaStreamNonBlocking) != cudaSuccess) return nullptr;
+    if (cudaStreamCreateWithFlags(&n.side, cudaStreamNonBlocking) != cudaSuccess) return false;
     if (cudaEventCreateWithFlags(&n.fork, cudaEventDisableTiming) != cudaSuccess ||
         cudaEventCreateWithFlags(&n.join, cudaEventDisableTiming) != cudaSuccess) {
         if (n.fork) cudaEventDestroy(n.fork);
         cudaStreamDestroy(n.side);
-        return nullptr;
+        return false;
     }
     g_side.push_back(n);
-    return &g_side.back();
+    *out = n;
+    return true;
 }
 
 // Returns the workspace of (device, stream) able to hold a call that needs a
@@ -329,7 +334,8 @@ pa_status pa_prepare(const pa_dims* dims, const pa_options* opts, void* stream) 
     void* ws = nullptr;
     st = get_workspace(s, p.ws_bytes > kErrWordBytes ? p.ws_bytes : kErrWordBytes, p.counter_bytes, true, &ws,
                        nullptr);
-    if (st == PA_OK && p.decode_ctas > 0 && p.prefill_ctas > 0) get_side(s, true);
+    SideStream side;
+    if (st == PA_OK && p.decode_ctas > 0 && p.prefill_ctas > 0) get_side(s, true, &side);
     return st;
 }
 
@@ -376,13 +382,14 @@ pa_status pa_forward_ex(const void* q, const void* k_cache, const void* v_cache,
     // Both kernels: the prefill one on the side stream, forked after everything
     // before this call on s and joined back before anything after it.  The two
     // kernels touch disjoint rows of out and disjoint workspace words.
-    SideStream* side = (p.decode_ctas > 0 && p.prefill_ctas > 0) ? get_side(s, !capturing) : nullptr;
+    SideStream side{};
+    const bool forked = p.decode_ctas > 0 && p.prefill_ctas > 0 && get_side(s, !capturing, &side);
     cudaStream_t ps = s;
-    if (side) {
-        if ((e = cudaEventRecord(side->fork, s)) != cudaSuccess) return cuda_fail(e, "cudaEventRecord(fork)");
-        if ((e = cudaStreamWaitEvent(side->side, side->fork, 0)) != cudaSuccess)
+    if (forked) {
+        if ((e = cudaEventRecord(side.fork, s)) != cudaSuccess) return cuda_fail(e, "cudaEventRecord(fork)");
+        if ((e = cudaStreamWaitEvent(side.side, side.fork, 0)) != cudaSuccess)
             return cuda_fail(e, "cudaStreamWaitEvent(fork)");
-        ps = side->side;
+        ps = side.side;
     }
     if ((st = record(opts ? opts->decode_start_event : nullptr, s, capturing)) != PA_OK) return st;
     if ((e = pa::launch_decode(a, s)) != cudaSuccess) return cuda_fail(e, "decode launch");
@@ -390,9 +397,9 @@ pa_status pa_forward_ex(const void* q, const void* k_cache, const void* v_cache,
     if ((st = record(opts ? opts->prefill_start_event : nullptr, ps, capturing)) != PA_OK) return st;
     if ((e = pa::launch_prefill(a, ps)) != cudaSuccess) return cuda_fail(e, "prefill launch");
     if ((st = record(opts ? opts->prefill_stop_event : nullptr, ps, capturing)) != PA_OK) return st;
-    if (side) {
-        if ((e = cudaEventRecord(side->join, ps)) != cudaSuccess) return cuda_fail(e, "cudaEventRecord(join)");
-        if ((e = cudaStreamWaitEvent(s, side->join, 0)) != cudaSuccess) return cuda_fail(e, "cudaStreamWaitEvent(join)");
+    if (forked) {
+        if ((e = cudaEventRecord(side.join, ps)) != cudaSuccess) return cuda_fail(e, "cudaEventRecord(join)");
+        if ((e = cudaStreamWaitEvent(s, side.join, 0)) != cudaSuccess) return cuda_fail(e, "cudaStreamWaitEvent(join)");
     }
     return PA_OK;
 }
