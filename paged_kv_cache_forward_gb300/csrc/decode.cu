@@ -85,9 +85,10 @@ __device__ __forceinline__ int64_t partial_row(const Args& a, int b, int s, int 
 // Softmax"): M = max_s m_s, w_s = 2^(m_s - M), out = sum_s w_s O_s / sum_s w_s l_s.
 // A split that saw no visible key of a row has m_s = -inf and weight 0.  The
 // partials were written by other CTAs, so they are read with L2-coherent loads.
-// One thread per (row, 4 columns) loads the (m, l) and O of kBatch splits at
-// a time (8, or 16 for 8-warp CTAs, which have the registers), so a merge
-// of that many splits takes one round trip to L2.
+// One thread per (row, 4 columns) reads the (m, l) and O of kBatch splits per
+// batch into one of two register buffers, the next batch's loads in flight
+// while the current one is combined: 2 * kBatch splits take one round trip to
+// L2, and a long run of splits streams instead of waiting batch by batch.
 template <int D, int kBatch>
 __device__ __forceinline__ void merge_splits(const Args& a, int b, const int* tok, const int* head, int rows,
                                              int nsplits, int q0) {
@@ -103,9 +104,7 @@ __device__ __forceinline__ void merge_splits(const Args& a, int b, const int* to
         const float* os = a.ws_o + row * D + d4;
         float M = -INFINITY, den = 0.f;
         float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-        for (int s0 = 0; s0 < nsplits; s0 += kBatch) {
-            float2 mlv[kBatch];
-            float4 ov[kBatch];
+        auto load = [&](int s0, float2 (&mlv)[kBatch], float4 (&ov)[kBatch]) {
 #pragma unroll
             for (int k = 0; k < kBatch; ++k) {
                 if (s0 + k < nsplits) {
@@ -116,6 +115,8 @@ __device__ __forceinline__ void merge_splits(const Args& a, int b, const int* to
                     ov[k] = make_float4(0.f, 0.f, 0.f, 0.f);
                 }
             }
+        };
+        auto combine = [&](const float2 (&mlv)[kBatch], const float4 (&ov)[kBatch]) {
             float Mn = M;
 #pragma unroll
             for (int k = 0; k < kBatch; ++k) Mn = fmaxf(Mn, mlv[k].x);
@@ -135,6 +136,16 @@ __device__ __forceinline__ void merge_splits(const Args& a, int b, const int* to
                 acc.w += w * ov[k].w;
             }
             M = Mn;
+        };
+        float2 mla[kBatch], mlb[kBatch];
+        float4 oa[kBatch], ob[kBatch];
+        load(0, mla, oa);
+        for (int s0 = 0; s0 < nsplits; s0 += 2 * kBatch) {
+            const bool second = s0 + kBatch < nsplits;
+            if (second) load(s0 + kBatch, mlb, ob);
+            combine(mla, oa);
+            if (s0 + 2 * kBatch < nsplits) load(s0 + 2 * kBatch, mla, oa);
+            if (second) combine(mlb, ob);
         }
         const float inv = 1.f / den;
         uint2 packed;
@@ -541,7 +552,7 @@ __global__ void __launch_bounds__(kWarps * 32, (kWarps == 4 && D <= 128) ? 3 : 1
     }
     __syncthreads();
     if (!s_last) return;
-    merge_splits<D, (kWarps == 8 ? 16 : 8)>(a, b, s_tok, s_head, rows, nsplits, q0);
+    merge_splits<D, 8>(a, b, s_tok, s_head, rows, nsplits, q0);
     if (threadIdx.x == 0) *counter = 0;
 }
 
