@@ -27,28 +27,37 @@ def test_tiny_decode_all_seeds():
         assert_close(run(b), oracle.batch_attention(b), f"tiny seed {seed}")
 
 
+# Seeds 0-4 of every configuration (the full-size prefill and mixed batches on
+# sampled rows).
+SEEDS = range(5)
+
+
+@pytest.mark.parametrize("seed", SEEDS)
 @pytest.mark.parametrize("ctx", [1024, 8192, 32768])
-def test_llama_decode(ctx):
-    b = W.llama_decode(ctx, seed=0)
-    assert_close(run(b), oracle.batch_attention(b), f"llama decode {ctx}")
+def test_llama_decode(ctx, seed):
+    b = W.llama_decode(ctx, seed=seed)
+    assert_close(run(b), oracle.batch_attention(b), f"llama decode {ctx} seed {seed}")
 
 
-def test_batched_decode():
-    b = W.batched_decode(seed=0)
-    assert_close(run(b), oracle.batch_attention(b), "batched decode")
+@pytest.mark.parametrize("seed", SEEDS)
+def test_batched_decode(seed):
+    b = W.batched_decode(seed=seed)
+    assert_close(run(b), oracle.batch_attention(b), f"batched decode seed {seed}")
 
 
-def test_varlen_prefill_full_size_sampled():
-    b = W.varlen_prefill(seed=0)
+@pytest.mark.parametrize("seed", SEEDS)
+def test_varlen_prefill_full_size_sampled(seed):
+    b = W.varlen_prefill(seed=seed)
     got = run(b)
-    rows = sample_rows(b, 600, seed=1)
+    rows = sample_rows(b, 600, seed=1 + seed)
     ref = oracle.batch_attention(b, rows=rows)
     sel = torch.stack([got[t, h] for t, h in rows])
-    assert_close(sel, ref, "varlen prefill (sampled rows)")
+    assert_close(sel, ref, f"varlen prefill seed {seed} (sampled rows)")
 
 
-def test_mixed_full_size_sampled_in_graph():
-    b = W.mixed_batch(seed=0)
+@pytest.mark.parametrize("seed", SEEDS)
+def test_mixed_full_size_sampled_in_graph(seed):
+    b = W.mixed_batch(seed=seed)
     d = b.to("cuda")
     out = torch.full_like(d.q, float("nan"))
     s = torch.cuda.Stream()
@@ -61,13 +70,13 @@ def test_mixed_full_size_sampled_in_graph():
     assert pa.device_error(s) == 0
     got = out.cpu()
     assert torch.isfinite(got.float()).all()
-    rows = sample_rows(b, 400, seed=2)
+    rows = sample_rows(b, 400, seed=2 + seed)
     T = b.num_tokens
     rows += [(T - 1, h) for h in range(b.num_q_heads)]  # the 131072-context decode row
     rows = sorted(set(rows))
     ref = oracle.batch_attention(b, rows=rows)
     sel = torch.stack([got[t, h] for t, h in rows])
-    assert_close(sel, ref, "mixed (sampled rows)")
+    assert_close(sel, ref, f"mixed seed {seed} (sampled rows)")
 
 
 # --------------------------------------------------- smaller full comparisons
