@@ -113,10 +113,10 @@ typedef struct {
                                but fit fewer CTAs on an SM. */
     int32_t decode_cluster; /* 0: from the tuned table (unless kv_chunk is set);
                                1: splits of kv_chunk keys merged through the
-                               workspace; 2..16: the keys of each (sequence, KV
-                               head) are split evenly over a thread-block cluster
-                               of this many CTAs, merged in distributed shared
-                               memory (kv_chunk must then be 0). */
+                               workspace; 2..16: the pages of each (sequence, KV
+                               head) are dealt round-robin to a thread-block
+                               cluster of this many CTAs, merged in distributed
+                               shared memory (kv_chunk must then be 0). */
     /* cudaEvent_t handles recorded on the stream immediately before and after
        the decode kernel and the prefill kernel (NULL: not recorded). */
     void* decode_start_event;

@@ -124,11 +124,12 @@ pa_status make_plan(const pa_dims* d, const pa_options* o, Plan* p) {
     int32_t cluster = te.decode_cluster > 1 ? te.decode_cluster : 1;
     if (o && (o->kv_chunk || o->decode_cluster)) cluster = o->decode_cluster > 1 ? o->decode_cluster : 1;
     if (o && o->kv_chunk && o->decode_cluster > 1)
-        return fail(PA_ERR_INVALID_ARG, "kv_chunk and decode_cluster > 1 are exclusive (a cluster splits evenly)");
+        return fail(PA_ERR_INVALID_ARG, "kv_chunk and decode_cluster > 1 are exclusive (a cluster deals the pages round-robin)");
     if (o && (o->decode_cluster < 0 || o->decode_cluster > kMaxDecodeCluster))
         return fail(PA_ERR_INVALID_ARG, "decode_cluster %d is not in 0..%d", o->decode_cluster, kMaxDecodeCluster);
     if (cluster > 1) {
-        // even split of the longest possible sequence over `cluster` CTAs
+        // keys per CTA of the longest possible sequence, its pages dealt
+        // round-robin to `cluster` CTAs (reported; the kernel needs only the size)
         const int64_t pages = (bound + d->page_size - 1) / d->page_size;
         chunk = (pages + cluster - 1) / cluster * d->page_size;
     }

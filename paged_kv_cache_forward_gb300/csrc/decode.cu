@@ -25,7 +25,7 @@
 // that draws the last ticket merges all splits by log-sum-exp (no CTA waits
 // for another, so there is no spin and no second launch).
 //
-// HBM-bound: per CTA it streams (end - start) * D * 2 bytes of K and as many of
+// HBM-bound: per CTA it streams its keys' D * 2 bytes each of K and as many of
 // V, which is the whole algorithmic traffic of decode.  The contraction has only
 // G rows (4 for Llama), too few for a tcgen05 tile; the warp MMAs keep the
 // arithmetic well below the memory time.
@@ -209,21 +209,24 @@ __global__ void __launch_bounds__(kWarps * 32, (kWarps == 4 && D <= 128) ? 3 : 1
     const int h = static_cast<int>(idx % a.num_kv_heads);
     const int b = static_cast<int>(idx / a.num_kv_heads);
     // Cluster mode: the a.splits == a.decode_cluster CTAs of (b, h, rg) form one
-    // thread-block cluster, split the sequence's pages evenly and merge through
-    // distributed shared memory.  Otherwise split s covers keys
-    // [s * kv_chunk, (s + 1) * kv_chunk) and the splits merge through the workspace.
+    // thread-block cluster, take the sequence's pages round-robin (CTA s: pages
+    // s, s + C, s + 2C, ...) and merge through distributed shared memory.
+    // Otherwise split s covers keys [s * kv_chunk, (s + 1) * kv_chunk) and the
+    // splits merge through the workspace.  Either way the CTA's k-th page is
+    // p0 + pstep * k, and its warp w takes k = w, w + kWarps, ...
     const bool clustered = a.decode_cluster > 1;
+    const int p0 = clustered ? s : s * (a.kv_chunk / kPage);
+    const int pstep = clustered ? a.splits : 1;
 
     // Every exit before the cluster barriers below depends on b alone, so the
-    // CTAs of a cluster take it together.  The metadata loads and (with static
-    // splits, whose page range does not depend on the sequence length) the first
-    // block-table entries are issued together, before anything waits on them.
+    // CTAs of a cluster take it together.  The metadata loads and the first
+    // block-table entries (the page set does not depend on the sequence length)
+    // are issued together, before anything waits on them.
     const int32_t* bt = a.block_table + static_cast<int64_t>(b) * a.max_pages;
     int bt_cur = 0, bt_nxt = 0;
-    if (!clustered) {
-        const int p0 = s * (a.kv_chunk / kPage);
-        const int pe = min(a.max_pages, p0 + a.kv_chunk / kPage);
-        const int i0 = p0 + warp + kWarps * lane, i1 = i0 + 32 * kWarps;
+    {
+        const int pe = clustered ? a.max_pages : min(a.max_pages, p0 + a.kv_chunk / kPage);
+        const int i0 = p0 + pstep * (warp + kWarps * lane), i1 = i0 + pstep * 32 * kWarps;
         if (i0 < pe) bt_cur = ldg_s32(bt + i0);
         if (i1 < pe) bt_nxt = ldg_s32(bt + i1);
     }
@@ -262,33 +265,29 @@ __global__ void __launch_bounds__(kWarps * 32, (kWarps == 4 && D <= 128) ? 3 : 1
         }
         return;
     }
-    // This CTA's keys [start, end); start is a page boundary.
-    int start, end, nsplits;
+    // This CTA's pages (npages of them, page p0 + pstep * k for k < npages) hold
+    // keys below `end`.
+    int end, nsplits, npages;
     if (clustered) {
         const int pages_b = (L + kPage - 1) / kPage;
-        const int per = (pages_b + a.splits - 1) / a.splits;
-        start = min(L, s * per * kPage);
-        end = min(L, (s + 1) * per * kPage);
+        end = L;
+        npages = pages_b > s ? (pages_b - s + a.splits - 1) / a.splits : 0;  // 0: an empty CTA of the cluster
         nsplits = a.splits;
     } else {
-        start = s * a.kv_chunk;
+        const int start = s * a.kv_chunk;
         if (start >= L) return;
         end = min(L, start + a.kv_chunk);
+        npages = (end - start + kPage - 1) / kPage;
         nsplits = (L + a.kv_chunk - 1) / a.kv_chunk;
     }
-    const int npages = (end - start + kPage - 1) / kPage;  // 0 for an empty split of a cluster
     const int my_pages = warp < npages ? (npages - warp + kWarps - 1) / kWarps : 0;
     if (clustered) cluster_arrive_relaxed();  // waited for before the first push to a peer
 
     // Block-table entries of this warp's pages, 32 at a time in registers (lane l
     // holds the entry of the warp's page 32 * round + l), the next round loaded
-    // ahead, so that the copies do not wait on them.  (Static splits loaded the
-    // first two rounds above; a cluster's split needs the length first.)
-    auto bt_entry = [&](int i) { return i < my_pages ? bt[start / kPage + warp + kWarps * i] : 0; };
-    if (clustered) {
-        bt_cur = bt_entry(lane);
-        bt_nxt = bt_entry(32 + lane);
-    }
+    // ahead, so that the copies do not wait on them (the first two rounds were
+    // loaded above).
+    auto bt_entry = [&](int i) { return i < my_pages ? bt[p0 + pstep * (warp + kWarps * i)] : 0; };
 
     // Each of this thread's two rows (g, g + 8) has its own causal limit.
     const __nv_bfloat16* q = reinterpret_cast<const __nv_bfloat16*>(a.q);
@@ -317,7 +316,7 @@ __global__ void __launch_bounds__(kWarps * 32, (kWarps == 4 && D <= 128) ? 3 : 1
     // commit a group so that the wait count below stays uniform.
     auto issue = [&](int it) {
         if (it < my_pages) {
-            const int lp = start / kPage + warp + kWarps * it;
+            const int lp = p0 + pstep * (warp + kWarps * it);
             const int page = page_of(it);
             const bool ok = static_cast<uint32_t>(page) < static_cast<uint64_t>(a.num_blocks);
             if (!ok) flag_error(a.err, kDevBadBlock);
@@ -380,7 +379,7 @@ __global__ void __launch_bounds__(kWarps * 32, (kWarps == 4 && D <= 128) ? 3 : 1
         }
         // Mask keys past the end of the split (only the sequence's last page is
         // partial) and move to log2 units.
-        const int tok0 = (start / kPage + warp + kWarps * it) * kPage;
+        const int tok0 = (p0 + pstep * (warp + kWarps * it)) * kPage;
 #pragma unroll
         for (int nt = 0; nt < 2; ++nt)
 #pragma unroll

@@ -133,7 +133,7 @@ def main(argv=None):
     ap.add_argument("--bounds", default=",".join(map(str, BOUNDS)))
     ap.add_argument("--batches", default=",".join(map(str, BATCHES)))
     ap.add_argument("--variants", default=VARIANTS, help="decode variants to try: warps x stages")
-    ap.add_argument("--clusters", default="2,4,8,16", help="cluster sizes to try (even split, merge in DSMEM)")
+    ap.add_argument("--clusters", default="2,4,8,16", help="cluster sizes to try (pages dealt round-robin, merge in DSMEM)")
     args = ap.parse_args(argv)
     bounds = [int(x) for x in args.bounds.split(",")]
     batches = [int(x) for x in args.batches.split(",")]
@@ -161,7 +161,7 @@ def main(argv=None):
             res = []
             for w, st in variants:
                 # (split size, 1): splits merged through the workspace;
-                # (0, C): an even split over a cluster of C CTAs
+                # (0, C): the pages dealt round-robin to a cluster of C CTAs
                 cands = [(c, 1) for c in candidates(bound, batch, sms, w, st)] + [(0, c) for c in clusters]
                 for chunk, cl in cands:
                     try:
@@ -202,7 +202,7 @@ def main(argv=None):
                 "with lengths uniform in [bound/16, bound] (seeded per cell),\n"
                 "graph-replayed pa_forward steps rotating over KV pool copies larger than 3 x L2.\n"
                 "GB/s = KV bytes per step / step time.\n\n"
-                "Split `cN`: the keys split evenly over a thread-block cluster of N CTAs.\n\n"
+                "Split `cN`: the pages dealt round-robin to a thread-block cluster of N CTAs.\n\n"
                 "| batch | bound | best split | warps x stages | us/step | GB/s | split/variant:GB/s for every candidate |\n"
                 "|---|---|---|---|---|---|---|\n")
         f.write("\n".join(lines) + "\n")
@@ -215,7 +215,7 @@ def write_table(path, entries, last_batch, fallback, gpu_name, stamp):
                 "// (max_pages * page_size) and the number of decode units:\n"
                 "// {max_bound, max_units, kv_chunk, decode_stages, decode_warps, decode_cluster}\n"
                 "// (units = sequences x KV heads x row groups)\n"
-                "// (cluster > 1: an even split over a cluster of that many CTAs).  The first\n"
+                "// (cluster > 1: the pages dealt round-robin to a cluster of that many CTAs).  The first\n"
                 "// entry that matches wins; the last entry is the fallback.  Written by\n"
                 f"// paged_kv_cache_forward_gb300/sweep.py on {gpu_name} ({stamp}).\n"
                 "static const LutEntry kSplitTable[] = {\n")

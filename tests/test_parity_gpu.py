@@ -136,9 +136,10 @@ def test_decode_variants(warps, stages, D):
 @pytest.mark.parametrize("cluster", [2, 3, 4, 8, 16])
 @pytest.mark.parametrize("warps,stages", [(4, 2), (8, 3), (12, 2)])
 def test_decode_cluster_mode(cluster, warps, stages):
-    """Splits merged in distributed shared memory: the keys of each (sequence,
-    KV head) split evenly over a cluster of CTAs.  Sequences shorter than the
-    cluster's page count leave some CTAs without keys; multi-token rows included."""
+    """Splits merged in distributed shared memory: the pages of each (sequence,
+    KV head) dealt round-robin to a cluster of CTAs.  Sequences with fewer pages
+    than the cluster has CTAs leave some CTAs without keys; multi-token rows
+    included."""
     b = W.make_batch([1, 1, 3, 1, 2, 1], [4000, 1, 777, 65, 2500, 16], 32, 8, 128, seed=41 + cluster,
                      max_pages=256)
     ref = oracle.batch_attention(b)
