@@ -1,9 +1,9 @@
 #!/usr/bin/env python3
 """Benchmark of the paged-attention forward pass (libpagedattn) on GB300.
 
-One "step" is one pa_forward call over one batch (decode split-KV kernel,
-log-sum-exp combine, prefill kernel: whatever the batch needs), replayed from
-CUDA graphs captured with a static launch grid.  The default workload is the
+One "step" is one pa_forward call over one batch (the split-KV decode kernel
+with its log-sum-exp merge, the persistent prefill kernel: whatever the batch
+needs), replayed from CUDA graphs captured with a static launch grid.  The default workload is the
 Llama-3.1-8B-shaped single-stream decode at context 32768 (32 query heads,
 8 KV heads, head_dim 128, page 16, bf16 N(0,1), pages scattered in a pool 1.5x
 the need).  Other workloads: --config (see paged_kv_cache_forward_gb300.workloads).
