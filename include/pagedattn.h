@@ -123,6 +123,14 @@ typedef struct {
     void* decode_stop_event;
     void* prefill_start_event;
     void* prefill_stop_event;
+    /* Tests only: nonzero makes the prefill kernel's first CTA withhold the K
+       tile of its first work item, so that the wait for it runs out (after
+       2 s) and the kernel takes its abort path: device error 4, the other
+       roles stop, issued MMAs drain, TMEM is freed.  No memory is touched that
+       a normal call would not touch; outputs of that CTA's item are left as
+       they were. */
+    int32_t test_stall_prefill;
+    int32_t reserved;
 } pa_options;
 
 /* What a call with these dims launches (host-only; no device work). */

@@ -152,6 +152,7 @@ pa_status make_plan(const pa_dims* d, const pa_options* o, Plan* p) {
     a.decode_max_q = pa::decode_max_q(group);
     a.decode_stages = stages;
     a.decode_warps = warps;
+    a.test_stall_prefill = o ? o->test_stall_prefill : 0;
     p->kv_chunk = a.kv_chunk;
     p->splits = a.splits;
     p->row_groups = a.row_groups;
@@ -498,6 +499,6 @@ const char* pa_status_string(pa_status status) {
 
 const char* pa_last_error(void) { return g_last_error; }
 
-int32_t pa_version(void) { return 101; }
+int32_t pa_version(void) { return 102; }
 
 }  // extern "C"

@@ -44,6 +44,7 @@ struct Args {
     int32_t decode_cluster;  // > 1: the splits of a (sequence, KV head, row group) are one
                              // thread-block cluster of this many CTAs (== splits), merged
                              // through distributed shared memory; 1: merged through ws
+    int32_t test_stall_prefill;  // tests only: see pa_options
     float scale;         // softmax scale
     float scale_log2;    // scale * log2(e)
 };

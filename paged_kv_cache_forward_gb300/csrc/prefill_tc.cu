@@ -469,9 +469,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                     tc::fence_proxy_async_smem();
                 }
                 __syncwarp();
-                if (lane == 0) tc::mbar_arrive_expect_tx(bar(full0 + st), nt * S::kHalves * 2048);
+                // (tests only: CTA 0 withholds the K tile of its first item, so
+                // that the MMA thread's wait for it runs out)
+                const bool withhold = a.test_stall_prefill && !is_v && blockIdx.x == 0 && it == 0 && kt == 0;
+                if (lane == 0 && !withhold) tc::mbar_arrive_expect_tx(bar(full0 + st), nt * S::kHalves * 2048);
                 __syncwarp();
-                if (lane < nt) {
+                if (lane < nt && !withhold) {
 #pragma unroll
                     for (int hf = 0; hf < S::kHalves; ++hf)
                         tc::tma_load_4d(sd + hf * kHalfBytes + lane * 2048, tm, bar(full0 + st), hf * 64, h, 0, page);

@@ -26,7 +26,8 @@ def ensure_built():
 
 
 def run(b: W.Batch, kv_chunk: int = 0, device="cuda", check_errors: bool = True,
-        decode_stages: int = 0, decode_warps: int = 0, decode_cluster: int = 0) -> torch.Tensor:
+        decode_stages: int = 0, decode_warps: int = 0, decode_cluster: int = 0,
+        test_stall_prefill: int = 0) -> torch.Tensor:
     """pa_forward on the batch; returns the output on the CPU (bf16).  The output
     buffer starts as NaN so that an unwritten row cannot pass."""
     ensure_built()
@@ -34,7 +35,7 @@ def run(b: W.Batch, kv_chunk: int = 0, device="cuda", check_errors: bool = True,
     out = torch.full_like(d.q, float("nan"))
     pa.forward(d.q, d.k_cache, d.v_cache, d.block_table, d.seq_lens, d.query_start_loc, out,
                scale=b.scale, kv_chunk=kv_chunk, decode_stages=decode_stages,
-               decode_warps=decode_warps, decode_cluster=decode_cluster)
+               decode_warps=decode_warps, decode_cluster=decode_cluster, test_stall_prefill=test_stall_prefill)
     torch.cuda.synchronize()
     if check_errors:
         assert pa.device_error() == 0

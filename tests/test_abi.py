@@ -38,7 +38,7 @@ def test_every_declared_symbol_is_exported(lib):
 def test_status_strings(lib):
     for st in range(5):
         assert lib.pa_status_string(st)
-    assert lib.pa_version() == 101
+    assert lib.pa_version() == 102
 
 
 def llama_dims(**kw):

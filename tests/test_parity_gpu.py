@@ -366,6 +366,20 @@ def test_bad_block_id_sets_error_word_without_fault():
     assert_close(run(b2), oracle.batch_attention(b2), "after error")
 
 
+def test_prefill_wait_that_runs_out_aborts_cleanly():
+    """A wait of the prefill kernel that runs out (the test option withholds one
+    K tile; no memory is touched that a normal call would not touch): the
+    kernel gives up after its bounded wait, records error 4 and returns; the
+    context stays usable and the next call is exact (its item counters are back
+    at zero)."""
+    b = W.make_batch([300, 200, 1], [300, 400, 900], 32, 8, 128, seed=81)
+    run(b, check_errors=False, test_stall_prefill=1)
+    assert pa.device_error() == 4
+    assert pa.device_error() == 0  # cleared
+    b2 = W.make_batch([100, 64, 1], [500, 64, 300], 32, 8, 128, seed=82)
+    assert_close(run(b2), oracle.batch_attention(b2), "after a prefill abort")
+
+
 def test_query_longer_than_context_flagged():
     b = W.make_batch([3], [3], 8, 2, 128, seed=52)
     b.seq_lens[0] = 2  # 3 new tokens but 2 keys: contract violation
