@@ -166,14 +166,17 @@ pa_status pa_forward_ex(const void* q, const void* k_cache, const void* v_cache,
                         const int32_t* query_start_loc, void* out, float scale,
                         const pa_dims* dims, const pa_options* opts, void* stream);
 
-/* Fills *info with the launch plan for dims (host only).  The split size comes
- * from the table an offline sweep produced, keyed on the context bound
- * (max_pages * page_size) and the batch size: the "offline micro-benchmarks ->
- * decision tree" of the same page's third section, with no tuning at run time. */
+/* Fills *info with the launch plan for dims (host only).  The split size and the
+ * decode kernel variant (warps, pipeline depth, cluster size) come from the
+ * table an offline sweep produced, keyed on the context bound
+ * (max_pages * page_size) and the decode units (sequences x KV heads x row
+ * groups of 16 query heads): the "offline micro-benchmarks -> decision tree" of
+ * the same page's third section, with no tuning at run time. */
 pa_status pa_plan(const pa_dims* dims, const pa_options* opts, pa_plan_info* info);
 
 /* Allocates (outside any capture) the workspace a pa_forward with these dims and
- * options needs on stream, so that the call can then be captured. */
+ * options needs on stream, and the side stream and events of a call with both
+ * kernels, so that the call can then be captured. */
 pa_status pa_prepare(const pa_dims* dims, const pa_options* opts, void* stream);
 
 /* Synchronises stream, then returns the stream's sticky device error code in
@@ -182,8 +185,8 @@ pa_status pa_prepare(const pa_dims* dims, const pa_options* opts, void* stream);
  * outside [0, num_tokens]) and clears it.  Rows the check skipped are not written. */
 pa_status pa_device_error(void* stream, int32_t* code);
 
-/* Frees every cached workspace on every device.  No graph that captured a
- * pa_forward may be replayed afterwards. */
+/* Frees every cached workspace on every device, and the side streams and
+ * events.  No graph that captured a pa_forward may be replayed afterwards. */
 pa_status pa_release_workspaces(void);
 
 /* Static text for a status, and this thread's last error detail. */
