@@ -10,9 +10,23 @@ from paged_kv_cache_forward_gb300 import build as build_mod
 from paged_kv_cache_forward_gb300 import workloads as W
 
 # Tolerance of the GPU bf16 output against the fp64 oracle, over all compared
-# elements: max-abs error 1.5e-2 and mean-abs error 2e-3.
+# elements: max-abs error 1.5e-2 and mean-abs error 2e-3.  The output is bf16,
+# so an element whose exact value has magnitude >= 4 cannot always be written
+# within 1.5e-2 (half a bf16 ulp there is 2^-6 = 0.0156); such an element is
+# held to half an ulp of its exact value plus 1e-3 instead (the larger bound).
 TOL_MAX = 1.5e-2
 TOL_MEAN = 2e-3
+TOL_ARITH = 1e-3  # fp32 arithmetic on top of the output rounding, for |exact| >= 4
+
+
+def bf16_half_ulp(x: np.ndarray) -> np.ndarray:
+    """Half the spacing of bf16 numbers (8 significant bits) at |x|."""
+    _, e = np.frexp(np.abs(x))  # |x| = m * 2^e, m in [0.5, 1)
+    return np.ldexp(1.0, e - 9)
+
+
+def max_abs_bound(ref: np.ndarray) -> np.ndarray:
+    return np.maximum(TOL_MAX, bf16_half_ulp(ref) + TOL_ARITH)
 
 _built = False
 
@@ -52,7 +66,10 @@ def errors(got_bf16: torch.Tensor, ref: np.ndarray):
 
 def assert_close(got_bf16, ref, what=""):
     mx, mean = errors(got_bf16, ref)
-    assert mx <= TOL_MAX and mean <= TOL_MEAN, f"{what}: max_abs {mx:.3e} mean_abs {mean:.3e}"
+    g = got_bf16.double().numpy()
+    worst = float((np.abs(g - ref) / max_abs_bound(ref)).max()) if ref.size else 0.0
+    assert worst <= 1.0 and mean <= TOL_MEAN, (
+        f"{what}: max_abs {mx:.3e} mean_abs {mean:.3e} (worst element at {worst:.3f} of its bound)")
     return mx, mean
 
 
