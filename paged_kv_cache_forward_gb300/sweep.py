@@ -23,6 +23,7 @@ from __future__ import annotations
 import argparse
 import datetime
 import math
+import re
 import os
 import sys
 
@@ -134,6 +135,8 @@ def main(argv=None):
     ap.add_argument("--batches", default=",".join(map(str, BATCHES)))
     ap.add_argument("--variants", default=VARIANTS, help="decode variants to try: warps x stages")
     ap.add_argument("--clusters", default="2,4,8,16", help="cluster sizes to try (pages dealt round-robin, merge in DSMEM)")
+    ap.add_argument("--merge", action="store_true",
+                    help="replace only the swept (bound, batch) cells of the existing table and log")
     args = ap.parse_args(argv)
     bounds = [int(x) for x in args.bounds.split(",")]
     batches = [int(x) for x in args.batches.split(",")]
@@ -185,6 +188,15 @@ def main(argv=None):
     # smallest swept batch >= B and, within it, the smallest swept bound >= bound;
     # units = sequences x KV heads (x row groups), so other head counts map onto
     # the Llama-shaped sweep by their parallelism
+    if args.merge:
+        cells, old_lines = read_table(args.out), read_log(args.log)
+        cells.update(best)
+        for line in lines:
+            old_lines[tuple(int(x) for x in line.split("|")[1:3])] = line
+        best = cells
+        batches = sorted({k[1] for k in best})
+        bounds = sorted({k[0] for k in best})
+        lines = [old_lines[(bt, bd)] for bt in batches for bd in bounds if (bt, bd) in old_lines]
     entries = []
     for batch in batches:
         for bound in bounds:
@@ -207,6 +219,28 @@ def main(argv=None):
                 "|---|---|---|---|---|---|---|\n")
         f.write("\n".join(lines) + "\n")
     print(f"wrote {args.log}" + ("" if args.no_write else f" and {args.out}"))
+
+
+def read_table(path):
+    """The cells of an existing table: {(bound, batch): (chunk, stages, warps, cluster)}
+    (the last batch's cells carry max_units 1 << 30; the fallback row is dropped)."""
+    cells = {}
+    rows = re.findall(r"\{(\d+), (\d+|1 << 30), (\d+), (\d+), (\d+), (\d+)\}", open(path).read())
+    for bound, units, chunk, st, w, cl in rows:
+        batch = max(BATCHES) if units == "1 << 30" or int(units) >= 1 << 30 else int(units) // HKV
+        cells[(int(bound), batch)] = (int(chunk), int(st), int(w), int(cl))
+    return cells
+
+
+def read_log(path):
+    """The rows of an existing sweep log: {(batch, bound): line}."""
+    out = {}
+    if os.path.exists(path):
+        for line in open(path):
+            m = re.match(r"\| (\d+) \| (\d+) \|", line)
+            if m:
+                out[(int(m.group(1)), int(m.group(2)))] = line.rstrip("\n")
+    return out
 
 
 def write_table(path, entries, last_batch, fallback, gpu_name, stamp):
