@@ -7,23 +7,27 @@
 // sequences only, in row groups of 16 heads.  This is the "Q-Block" item of the
 // five-step list on the Triton unified-attention page, section "What three things
 // the IBM paper got right": query heads sharing a KV head are computed together,
-// so each KV page is read once per KV head, not once per query head.  The CTA
+// so each KV page is read once per KV head, not once per query head.  Split s
 // covers keys [s*kv_chunk, min((s+1)*kv_chunk, L_b)) -- one tile of the
-// "Parallel Tiled Softmax" item of the same list -- with each row masked
-// causally at its own position L_b - n_b + token.
+// "Parallel Tiled Softmax" item of the same list -- or, in cluster mode, every
+// C-th page of the sequence starting at page s; each row is masked causally at
+// its own position L_b - n_b + token.
 //
-// Inside the CTA, 4 warps take pages round-robin.  Each warp runs its own
-// 2-stage cp.async pipeline of one 16-token page of K and V (16-byte copies into
-// an XOR-swizzled layout, so the ldmatrix fragment loads are bank-conflict free),
-// computes S = Q K^T and O += P V with bf16 m16n8k16 MMAs (the G <= 16 query
-// rows padded to 16), and keeps an online softmax (running max m, sum l; the
-// recurrence of "The Flash Attention revolution" on the GPU programming guide
-// page) in the log2 domain.  At the end the 4 warps' (m, l, O) are merged in
-// shared memory; a sequence with one split writes bf16 out directly.  With
-// several splits each CTA writes its unnormalised partial (O, m, l) to the
-// workspace and takes a ticket from a per-(sequence, KV head) counter; the CTA
-// that draws the last ticket merges all splits by log-sum-exp (no CTA waits
-// for another, so there is no spin and no second launch).
+// Inside the CTA, kWarps warps (4, 8 or 12) take its pages round-robin.  Each
+// warp runs its own kStages-deep cp.async pipeline of 16-token pages of K and V
+// (16-byte copies into an XOR-swizzled layout, so the ldmatrix fragment loads
+// are bank-conflict free), computes S = Q K^T and O += P V with bf16 m16n8k16
+// MMAs (the query rows padded to 16), and keeps an online softmax (running max
+// m, sum l; the recurrence of "The Flash Attention revolution" on the GPU
+// programming guide page) in the log2 domain.  At the end the warps' (m, l, O)
+// are merged in shared memory; a sequence with one split writes bf16 out
+// directly.  With several splits each CTA writes its unnormalised partial
+// (O, m, l) to the workspace and takes a ticket from a per-(sequence, KV head,
+// row group) counter; the CTA that draws the last ticket merges all splits by
+// log-sum-exp (no CTA waits for another, so there is no spin and no second
+// launch).  In cluster mode the C CTAs of (b, h, rg) form a thread-block
+// cluster and merge in distributed shared memory instead.  The variant (warps,
+// stages), the split size and the cluster size come from the offline table.
 //
 // HBM-bound: per CTA it streams its keys' D * 2 bytes each of K and as many of
 // V, which is the whole algorithmic traffic of decode.  The contraction has only
