@@ -145,6 +145,52 @@ def pin_large_logits(lib):
     assert np.max(np.abs(out[0, 0, :3] - w)) < 1e-14
 
 
+def pin_lse(lib):
+    """The log-sum-exp of a row's scores, lse = log(sum_j exp(s_j)) over the
+    visible keys, in closed form: K = 0 gives log(p + 1) (every visible score is
+    0; the count pins the causal alignment); two keys with scores 0 and s give
+    log(1 + e^s); scores near 1e3 give 1000 + log(1 + e^-8 + e^-24) (no overflow,
+    and the row max is added back)."""
+    q_lens, seq_lens = [4, 1], [9, 6]
+    b = W.make_batch(q_lens, seq_lens, 4, 2, 64, seed=23, pool_factor=2.0, max_pages=1)
+    for s_, L in enumerate(seq_lens):
+        for j in range(L):
+            for hk in range(2):
+                _set_logical(b, s_, j, hk, k=torch.zeros(64))
+    _, lse = oracle.attention(b.q, b.k_cache, b.v_cache, b.block_table, b.seq_lens, b.query_start_loc, b.scale,
+                              return_lse=True, lib=lib)
+    t = 0
+    for n, L in zip(q_lens, seq_lens):
+        for i in range(n):
+            assert np.max(np.abs(lse[t] - math.log(L - n + i + 1))) < 1e-13, (t, lse[t])
+            t += 1
+    D, scale, a = 64, 0.37, 5.0
+    b = W.make_batch([1], [2], 1, 1, D, seed=24, pool_pages=3, max_pages=1, scale=scale)
+    e0 = torch.zeros(D)
+    e0[3] = 1.0
+    b.q[0, 0] = _bf(e0)
+    k1 = torch.zeros(D)
+    k1[3] = a
+    _set_logical(b, 0, 0, 0, k=torch.zeros(D))
+    _set_logical(b, 0, 1, 0, k=k1)
+    _, lse = oracle.attention_rows(b.q, b.k_cache, b.v_cache, b.block_table, b.seq_lens, b.query_start_loc,
+                                   b.scale, rows=[(0, 0)], return_lse=True, lib=lib)
+    s1 = float(np.float32(scale)) * a
+    assert abs(lse[0] - math.log1p(math.exp(s1))) < 1e-14, lse[0]
+    b = W.make_batch([1], [3], 1, 1, D, seed=25, pool_pages=2, max_pages=1, scale=1.0)
+    q = torch.zeros(D)
+    q[0] = 32.0
+    b.q[0, 0] = _bf(q)
+    for j, v in enumerate([1000.0, 992.0, 976.0]):
+        k = torch.zeros(D)
+        k[0] = v / 32.0
+        _set_logical(b, 0, j, 0, k=k)
+    _, lse = oracle.attention_rows(b.q, b.k_cache, b.v_cache, b.block_table, b.seq_lens, b.query_start_loc,
+                                   b.scale, rows=[(0, 0)], return_lse=True, lib=lib)
+    want = 1000.0 + math.log1p(math.exp(-8.0) + math.exp(-24.0))
+    assert abs(lse[0] - want) < 1e-12, (lse[0], want)
+
+
 # ------------------------------------------------------------------ invariants
 
 def pin_row_sums(lib):
@@ -383,6 +429,7 @@ ALL_PINS = [
     pin_zero_keys_mean,
     pin_two_key_logistic,
     pin_large_logits,
+    pin_lse,
     pin_row_sums,
     pin_block_permutation,
     pin_causal_hiding,

@@ -39,6 +39,8 @@ MUTANTS = [
     ("owner_seq_off_by_one", "if (qsl[mid] <= t) lo = mid;", "if (qsl[mid] < t) lo = mid;", False),
     ("wrong_seq_row", "int64_t page = block_table[b * d->max_pages + j / d->page_size];",
      "int64_t page = block_table[j / d->page_size];", False),
+    ("lse_without_max", "if (lse) *lse = m + log(l);", "if (lse) *lse = log(l);", False),
+    ("lse_of_weights_sum", "if (lse) *lse = m + log(l);", "if (lse) *lse = m;", False),
     ("cache_write_page_slot_swapped", "const int64_t page = s / page_size, slot = s % page_size;",
      "const int64_t page = s % page_size, slot = s / page_size;", False),
     ("cache_write_v_from_k", "memcpy(v_cache + (page * page_size + slot) * row, v_new + t * row",
