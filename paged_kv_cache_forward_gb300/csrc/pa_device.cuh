@@ -77,23 +77,6 @@ __device__ __forceinline__ float fast_exp2(float x) {
     return y;
 }
 
-// 2^x on the FMA and integer pipes, for x <= 8: Cody-Waite split x = n + f
-// with n = rint(x) (done by adding 1.5 * 2^23), 2^f for f in [-0.5, 0.5] from a
-// cubic fitted to the minimax relative error (paged_kv_cache_forward_gb300/
-// exp2_fit.py; max relative error 7.6e-5 on [-125, 8]), and 2^n added into the
-// exponent field.  Returns 0 below -125 (and for -inf).  Used for part of the
-// softmax so that the special-function unit is not the only exp2 source.
-__device__ __forceinline__ float poly_exp2(float x) {
-    const float t = x + 12582912.0f;
-    const int n = __float_as_int(t) - 0x4B400000;
-    const float f = x - (t - 12582912.0f);
-    float p = fmaf(0.0551702119410038f, f, 0.24260765314102173f);
-    p = fmaf(p, f, 0.693260908126831f);
-    p = fmaf(p, f, 0.9999282956123352f);
-    const float r = __int_as_float(__float_as_int(p) + (n << 23));
-    return x < -125.0f ? 0.0f : r;
-}
-
 __device__ __forceinline__ float quad_max(float v) {
     v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, 1));
     v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, 2));

@@ -168,12 +168,6 @@ __device__ __forceinline__ float2 unpack2(uint64_t v) {
     return r;
 }
 
-// One pair in PA_PREFILL_POLY_EVERY of the softmax exponentials is computed on
-// the FMA pipe (poly_exp2) instead of the special-function unit; 0: none.
-#ifndef PA_PREFILL_POLY_EVERY
-#define PA_PREFILL_POLY_EVERY 0
-#endif
-
 // (a0, a1) * (b, b) + (c, c) on the packed f32x2 FMA.
 __device__ __forceinline__ void fma2(float& y0, float& y1, float a0, float a1, float b, float c) {
     uint64_t a, bb, cc, y;
@@ -708,16 +702,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                         float y0, y1;
                         fma2(y0, y1, __uint_as_float(sh[32 * ch + 2 * e]), __uint_as_float(sh[32 * ch + 2 * e + 1]), c,
                              nmu);
-                        float x0, x1;
-                        if (PA_PREFILL_POLY_EVERY > 0 &&
-                            e % (PA_PREFILL_POLY_EVERY > 0 ? PA_PREFILL_POLY_EVERY : 1) ==
-                                (PA_PREFILL_POLY_EVERY > 0 ? PA_PREFILL_POLY_EVERY : 1) - 1) {
-                            x0 = poly_exp2(y0);
-                            x1 = poly_exp2(y1);
-                        } else {
-                            x0 = fast_exp2(y0);
-                            x1 = fast_exp2(y1);
-                        }
+                        const float x0 = fast_exp2(y0), x1 = fast_exp2(y1);
                         pk[e] = pack_bf16(x0, x1);
                         add2(lsum[e & 3], x0, x1);
                     }
