@@ -86,8 +86,9 @@ typedef enum {
     PA_ERR_CUDA = 4,          /* a CUDA runtime call failed (see pa_last_error) */
 } pa_status;
 
-/* Shapes of one call.  head_dim must be 64 or 128 and page_size 16; any
- * num_q_heads that is a multiple of num_kv_heads is accepted. */
+/* Shapes of one call.  head_dim must be 64, 128 or 256 and page_size 16; any
+ * num_q_heads that is a multiple of num_kv_heads, at most 64 times it, is
+ * accepted. */
 typedef struct {
     int64_t num_tokens;    /* T: rows of q and out (= query_start_loc[B])        */
     int64_t num_blocks;    /* NB: pages in each of k_cache and v_cache           */
@@ -130,7 +131,10 @@ typedef struct {
        a normal call would not touch; outputs of that CTA's item are left as
        they were. */
     int32_t test_stall_prefill;
-    int32_t reserved;
+    /* Timing and tests: 0 launches every kernel the batch needs; 1 only the
+       decode kernel, 2 only the prefill kernel (rows of the other kind are then
+       not written).  Other values are PA_ERR_INVALID_ARG. */
+    int32_t launch_only;
 } pa_options;
 
 /* What a call with these dims launches (host-only; no device work). */
@@ -195,13 +199,15 @@ const char* pa_last_error(void);
 
 /*
  * pa_forward without any allocation.  The pages this library follows have no
- * counterpart of this call; it exists for callers that cannot let a library
- * allocate device memory: code running while a stream is captured into a CUDA
- * graph (allocation is refused there), hosts whose device memory is owned or
- * budgeted by their own allocator, and latency-critical loops where an
- * allocation's cost or failure at an arbitrary call is not acceptable.
+ * counterpart of this call.  It serves callers that cannot let a library
+ * allocate device memory: hosts whose device memory is owned or budgeted up
+ * front by their own allocator (an inference server that hands all free memory
+ * to its KV-cache pool, a plugin living inside another framework's memory
+ * manager), and latency-critical loops where an allocation's cost, or its
+ * failure at an arbitrary call, is not acceptable.
  *
- * Same arguments and result as pa_forward, plus device_error: a device int32
+ * Same arguments and result as pa_forward (the same kernels with the same
+ * launch plan, so the same output bits), plus device_error: a device int32
  * that receives the first device-side error code (as pa_device_error reports
  * them; the caller zeroes it), or NULL to discard the codes.  The split-KV
  * scratch is a fixed 32 MiB array in the library's device image instead of an
@@ -209,10 +215,15 @@ const char* pa_last_error(void);
  * (at the latest this call's first use) until the process exits.  Shapes whose
  * pa_plan(...).workspace_bytes exceed 32 MiB are rejected with
  * PA_ERR_UNSUPPORTED before any launch.  Every call on a device shares that one
- * array, which keeps the last call's contents: calls that overlap on the GPU
- * (unordered streams) race, so order them on one stream.  The first call on each
- * device looks up the array's address with that device current; make it before
- * any stream capture.  It calls no cudaMalloc, cudaFree or allocating routine.
+ * array, which keeps the last call's contents (each call clears the counters it
+ * needs at zero, with a memset on the stream): calls that overlap on the GPU
+ * (unordered streams) race, so order them on one stream.  Both kernels run on
+ * the given stream, one after the other.  The first call on each device looks
+ * up the array's device address with that device current (cudaGetSymbolAddress)
+ * and keeps it for the life of the process; make that first call before any
+ * stream capture, and do not reset the device (cudaDeviceReset) after it.  It
+ * calls no cudaMalloc, cudaFree or allocating routine, and may be called from
+ * several host threads.
  */
 pa_status pa_forward_noalloc(const void* q, const void* k_cache, const void* v_cache,
                              const int32_t* block_table, const int32_t* seq_lens,

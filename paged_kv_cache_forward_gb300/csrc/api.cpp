@@ -125,6 +125,8 @@ pa_status make_plan(const pa_dims* d, const pa_options* o, Plan* p) {
     if (o && (o->kv_chunk || o->decode_cluster)) cluster = o->decode_cluster > 1 ? o->decode_cluster : 1;
     if (o && o->kv_chunk && o->decode_cluster > 1)
         return fail(PA_ERR_INVALID_ARG, "kv_chunk and decode_cluster > 1 are exclusive (a cluster deals the pages round-robin)");
+    if (o && (o->launch_only < 0 || o->launch_only > 2))
+        return fail(PA_ERR_INVALID_ARG, "launch_only %d is not 0, 1 or 2", o->launch_only);
     if (o && (o->decode_cluster < 0 || o->decode_cluster > kMaxDecodeCluster))
         return fail(PA_ERR_INVALID_ARG, "decode_cluster %d is not in 0..%d", o->decode_cluster, kMaxDecodeCluster);
     if (cluster > 1) {
@@ -393,12 +395,17 @@ pa_status pa_forward_ex(const void* q, const void* k_cache, const void* v_cache,
             return cuda_fail(e, "cudaStreamWaitEvent(fork)");
         ps = side.side;
     }
-    if ((st = record(opts ? opts->decode_start_event : nullptr, s, capturing)) != PA_OK) return st;
-    if ((e = pa::launch_decode(a, s)) != cudaSuccess) return cuda_fail(e, "decode launch");
-    if ((st = record(opts ? opts->decode_stop_event : nullptr, s, capturing)) != PA_OK) return st;
-    if ((st = record(opts ? opts->prefill_start_event : nullptr, ps, capturing)) != PA_OK) return st;
-    if ((e = pa::launch_prefill(a, ps)) != cudaSuccess) return cuda_fail(e, "prefill launch");
-    if ((st = record(opts ? opts->prefill_stop_event : nullptr, ps, capturing)) != PA_OK) return st;
+    const int32_t only = opts ? opts->launch_only : 0;
+    if (only != 2) {
+        if ((st = record(opts ? opts->decode_start_event : nullptr, s, capturing)) != PA_OK) return st;
+        if ((e = pa::launch_decode(a, s)) != cudaSuccess) return cuda_fail(e, "decode launch");
+        if ((st = record(opts ? opts->decode_stop_event : nullptr, s, capturing)) != PA_OK) return st;
+    }
+    if (only != 1) {
+        if ((st = record(opts ? opts->prefill_start_event : nullptr, ps, capturing)) != PA_OK) return st;
+        if ((e = pa::launch_prefill(a, ps)) != cudaSuccess) return cuda_fail(e, "prefill launch");
+        if ((st = record(opts ? opts->prefill_stop_event : nullptr, ps, capturing)) != PA_OK) return st;
+    }
     if (forked) {
         if ((e = cudaEventRecord(side.join, ps)) != cudaSuccess) return cuda_fail(e, "cudaEventRecord(join)");
         if ((e = cudaStreamWaitEvent(s, side.join, 0)) != cudaSuccess) return cuda_fail(e, "cudaStreamWaitEvent(join)");

@@ -36,6 +36,8 @@
 
 #include <cuda_bf16.h>
 
+#include <atomic>
+
 #include "pa_device.cuh"
 #include "pa_internal.h"
 
@@ -563,15 +565,17 @@ template <int D, int kWarps, int kStages>
 cudaError_t launch_decode_d(const Args& a, cudaStream_t stream) {
     using Tile = DecodeTile<D, kWarps, kStages>;
     auto kernel = decode_splitkv_kernel<D, kWarps, kStages>;
-    static bool configured[64] = {};  // the attributes are set once per device
+    // The attributes are set once per device.  Host threads may race here; both
+    // then set the same values, which is harmless, and the flag is atomic.
+    static std::atomic<bool> configured[64];
     int dev = 0;
     cudaGetDevice(&dev);
-    if (!configured[dev & 63]) {
+    if (!configured[dev & 63].load(std::memory_order_acquire)) {
         cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                              Tile::kSmemBytes + Tile::kRecvBytes);
         if (e == cudaSuccess) e = cudaFuncSetAttribute(kernel, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
         if (e != cudaSuccess) return e;
-        configured[dev & 63] = true;
+        configured[dev & 63].store(true, std::memory_order_release);
     }
     const int64_t ctas = decode_ctas(a);
     if (ctas == 0) return cudaSuccess;

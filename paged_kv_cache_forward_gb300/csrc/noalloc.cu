@@ -1,15 +1,15 @@
 // noalloc.cu -- pa_forward_noalloc: the forward pass with no memory allocation.
 //
 // pa_forward keeps its split-KV scratch in a buffer it allocates (cudaMalloc)
-// on first use.  Some callers cannot let a library allocate: code running while
-// a stream is being captured into a CUDA graph (allocation is not a stream
-// operation and is refused there), hosts whose device memory is entirely owned
-// by their own allocator or budgeted up front (inference servers, plugins), and
-// latency-critical loops where an allocation's cost or failure at an arbitrary
-// call is not acceptable.  This entry point uses instead a fixed scratch array
-// that is part of the library's device image: a GPU holds it from the time the
-// library's code is loaded there (at the latest, this entry point's first call
-// on it) until the process exits, and no call allocates or frees anything.
+// on first use.  Some callers cannot let a library allocate: hosts whose device
+// memory is entirely owned by their own allocator or budgeted up front
+// (inference servers that give all free memory to their KV-cache pool, plugins
+// inside another framework's memory manager), and latency-critical loops where
+// an allocation's cost or failure at an arbitrary call is not acceptable.  This
+// entry point uses instead a fixed scratch array that is part of the library's
+// device image: a GPU holds it from the time the library's code is loaded there
+// (at the latest, this entry point's first call on it) until the process exits,
+// and no call allocates or frees anything.
 //
 // Limits and rules:
 //  * The scratch holds kNoAllocScratchBytes (32 MiB).  A call whose split
@@ -19,11 +19,13 @@
 //    contents.  Calls that overlap on the GPU (on different streams without
 //    ordering between them) race on it; order them on one stream.
 //  * The first call on a device looks up the array's device address with that
-//    device current (cudaGetSymbolAddress); make that first call before any
-//    stream capture.
+//    device current (cudaGetSymbolAddress) and caches it for the process; make
+//    that first call before any stream capture, and do not reset the device
+//    afterwards (the cached address would be stale).
 //  * The sticky error word is the caller's device int32 if one is given (the
 //    caller clears it), else a slot in the scratch that each call clears and
 //    nothing reads back.
+//  * Host threads may call it concurrently (the set-up is under a mutex).
 
 #include <cuda_runtime.h>
 

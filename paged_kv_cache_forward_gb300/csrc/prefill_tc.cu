@@ -37,7 +37,8 @@
 //   warps 4-7   softmax of tile A, warps 8-11 softmax of tile B: one thread per
 //               row (TMEM lane).  The whole S row is loaded from TMEM at once,
 //               masked, its max taken in log2 units, and P = 2^(x - m) stored
-//               straight into TMEM in four stores of 32 keys with one wait.  The
+//               straight into TMEM as bf16 in four stores of 32 keys with one
+//               wait; the normaliser l sums those same bf16 values.  The
 //               running max is only moved (and O in TMEM rescaled) when the row
 //               max grows by more than 2^8; the final O / l is exact either way.
 // Every wait on an mbarrier is bounded (2 s); on timeout the CTA records
@@ -47,6 +48,8 @@
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
+
+#include <atomic>
 
 #include "pa_device.cuh"
 #include "pa_internal.h"
@@ -156,16 +159,22 @@ __device__ __forceinline__ float max3(float a, float b, float c) {
     return d;
 }
 
-// acc += (x0, x1) on the packed f32x2 adder (acc holds two partial sums).
-__device__ __forceinline__ void add2(uint64_t& acc, float x0, float x1) {
-    uint64_t x;
-    asm("mov.b64 %0, {%1, %2};\n" : "=l"(x) : "f"(x0), "f"(x1));
-    asm("add.rn.f32x2 %0, %0, %1;\n" : "+l"(acc) : "l"(x));
-}
 __device__ __forceinline__ float2 unpack2(uint64_t v) {
     float2 r;
     asm("mov.b64 {%0, %1}, %2;\n" : "=f"(r.x), "=f"(r.y) : "l"(v));
     return r;
+}
+
+// acc += the two bf16 halves of v, widened (two mixed-precision adds): the
+// normaliser l sums exactly the bf16-rounded P that the P V product consumes.
+__device__ __forceinline__ void add_bf16_pair(uint64_t& acc, uint32_t v) {
+    float a0, a1;
+    unsigned short lo, hi;
+    asm("mov.b64 {%0, %1}, %2;\n" : "=f"(a0), "=f"(a1) : "l"(acc));
+    asm("mov.b32 {%0, %1}, %2;\n" : "=h"(lo), "=h"(hi) : "r"(v));
+    asm("add.rn.f32.bf16 %0, %1, %0;\n" : "+f"(a0) : "h"(lo));
+    asm("add.rn.f32.bf16 %0, %1, %0;\n" : "+f"(a1) : "h"(hi));
+    asm("mov.b64 %0, {%1, %2};\n" : "=l"(acc) : "f"(a0), "f"(a1));
 }
 
 // (a0, a1) * (b, b) + (c, c) on the packed f32x2 FMA.
@@ -693,7 +702,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 // (key k to column 64 + k / 2), 32 keys per store; S is all in
                 // registers, so any column may be overwritten.  The P V that read
                 // the previous P finished before this S was written.  l sums the
-                // fp32 values.
+                // same bf16-rounded values, so V rows all equal to c give c.
 #pragma unroll
                 for (int ch = 0; ch < 4; ++ch) {
                     uint32_t pk[16];
@@ -704,7 +713,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                              nmu);
                         const float x0 = fast_exp2(y0), x1 = fast_exp2(y1);
                         pk[e] = pack_bf16(x0, x1);
-                        add2(lsum[e & 3], x0, x1);
+                        add_bf16_pair(lsum[e & 3], pk[e]);
                     }
                     tc::tmem_st16_async(s_addr + 64 + 16 * ch, pk);
                 }
@@ -804,10 +813,13 @@ int pairs_bound(const Args& a) {
 template <int D>
 cudaError_t launch_d(const Args& a, cudaStream_t stream) {
     using S = Smem<D>;
-    static bool configured[64] = {};
+    // One-time set-up per device.  Host threads may race here; both then set
+    // the same values, which is harmless, and the flags are atomic.
+    static std::atomic<bool> configured[64];
+    static std::atomic<int> sms[64];
     int dev = 0;
     cudaGetDevice(&dev);
-    if (!configured[dev & 63]) {
+    if (!configured[dev & 63].load(std::memory_order_acquire)) {
         cudaError_t e = cudaFuncSetAttribute(prefill_tc_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                              S::kAlloc);
         if (e != cudaSuccess) return e;
@@ -817,17 +829,17 @@ cudaError_t launch_d(const Args& a, cudaStream_t stream) {
         e = cudaFuncGetAttributes(&fa, prefill_tc_kernel<D>);
         if (e != cudaSuccess) return e;
         if (static_cast<uint32_t>(fa.numRegs) < kRegsLaunch) return cudaErrorInvalidConfiguration;
-        configured[dev & 63] = true;
+        int n = 0;
+        e = cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+        if (e != cudaSuccess) return e;
+        sms[dev & 63].store(n, std::memory_order_relaxed);
+        configured[dev & 63].store(true, std::memory_order_release);
     }
     const int64_t items = prefill_ctas(a);
     if (items == 0) return cudaSuccess;
     // one persistent CTA per SM (at most one per item)
-    static int sms[64] = {};
-    if (sms[dev & 63] == 0) {
-        cudaError_t e = cudaDeviceGetAttribute(&sms[dev & 63], cudaDevAttrMultiProcessorCount, dev);
-        if (e != cudaSuccess) return e;
-    }
-    const int64_t ctas = items < sms[dev & 63] ? items : sms[dev & 63];
+    const int nsm = sms[dev & 63].load(std::memory_order_relaxed);
+    const int64_t ctas = items < nsm ? items : nsm;
     const int G = a.group, tq = tokens_per_tile(G);
     CUtensorMap tq_map, tk_map, tv_map;
     if (!encode_q_map(&tq_map, a.q, D, a.num_q_heads, a.num_tokens, G, tq) ||
