@@ -3,16 +3,33 @@
 
 One "step" is one pa_forward call over one batch (the split-KV decode kernel
 with its log-sum-exp merge, the persistent prefill kernel: whatever the batch
-needs), replayed from CUDA graphs captured with a static launch grid.  The default workload is the
-Llama-3.1-8B-shaped single-stream decode at context 32768 (32 query heads,
-8 KV heads, head_dim 128, page 16, bf16 N(0,1), pages scattered in a pool 1.5x
-the need).  Other workloads: --config (see paged_kv_cache_forward_gb300.workloads).
+needs), replayed from CUDA graphs captured with a static launch grid.  The
+headline workload is the Llama-3.1-8B-shaped single-stream decode at context
+32768 (32 query heads, 8 KV heads, head_dim 128, page 16, bf16 N(0,1), pages
+scattered in a pool 1.5x the need); --config picks another.  At N = 1 the same
+process also measures every other workload of the metric (single-stream decode
+at 1024 and 8192, the 64-sequence batched decode, the causal varlen prefill, the
+mixed batch) and a 32-layer full-graph decoder step, each as a record under
+"sub_records" with its own timing, kernel roofline, end-to-end figure and clock
+summary.
 
+Per workload:
+  * timed region: `steps` steps replayed from CUDA graphs, after W untimed
+    warm-up steps and a short clock-settling replay; value = algorithmic work
+    (KV bytes, or causal FLOPs for the prefill) of all steps on all ranks / the
+    max over ranks of the region;
+  * kernel roofline: the dominant kernel alone (the other kernel of a mixed
+    batch is not launched), in runs of consecutive launches bracketed by CUDA
+    events on the launching stream, at least 100 runs; achieved = algorithmic
+    bytes (or FLOPs) per launch / mean launch duration; peak = the measured HBM
+    copy bandwidth, or for the prefill the sustained bf16 rate (its timing runs
+    for a second or more under the power cap);
+  * e2e: the same metric through the public API with the step's q and metadata
+    copied in from pinned host memory and out copied back every step (best of
+    eager calls, captured graphs, and a captured pipeline), each mode timed over
+    at least 0.2 s after one untimed replay.
 L2: each step reads one of R identical copies of the KV pool in rotation, with
 R * (KV bytes per step) > 3 * L2, so no step finds its pages in L2.
-
-Prints one JSON line.  value = algorithmic KV bytes (or causal FLOPs for
-prefill) of all steps on all ranks / the max over ranks of the timed region.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--config NAME] [--impl reference]
 """
@@ -25,6 +42,7 @@ import hashlib
 import json
 import math
 import os
+import platform
 import statistics
 import subprocess
 import sys
@@ -35,8 +53,12 @@ ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
 HEADLINE = "llama_decode_32768"
+SUB_CONFIGS = ["llama_decode_1024", "llama_decode_8192", "llama_decode_32768", "batched_decode", "varlen_prefill",
+               "mixed"]
+LAYERS_SUB = ("llama_decode_32768", 32)  # the full-graph decoder step of the sub-records
 FALLBACK_HBM_GBS = 6800.0      # profiling recipe's fallback, one earlier GB300 measurement
 FALLBACK_BF16_TFLOPS = 1900.0
+FALLBACK_BF16_SUSTAINED = 1700.0
 CSRC = os.path.join(ROOT, "paged_kv_cache_forward_gb300", "csrc")
 KERNEL_SOURCES = {
     "decode_splitkv": ["decode.cu", "pa_device.cuh"],
@@ -52,25 +74,31 @@ DESCRIPTIONS = {
     "mixed": "4 prefill x 512 + 60 decode ctx U[1024, 16384] + 1 decode ctx 131072, Hq 32 / Hkv 8, D 128",
     "spec_decode": "batch 16 x 4 new tokens (speculative decoding), ctx U[2048, 8192], Hq 32 / Hkv 8, D 128",
 }
+KERNEL_RUN = 16            # consecutive launches per timed run of the dominant kernel
+KERNEL_MIN_RUNS = 100
+KERNEL_MIN_S = 0.25
+E2E_MIN_S = 0.2
+SETTLE_MS = 300.0
 
 
 def parse_args(argv=None):
     ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=None, help="timed steps (default: about 2 s of work)")
-    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--config", default=HEADLINE)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--seed", type=int, default=0)
     ap.add_argument("--kv-chunk", type=int, default=0, help="override the tuned split size (sweeps)")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-sub-records", action="store_true", help="headline workload only")
     ap.add_argument("--cpu-seconds", type=float, default=10.0, help="target CPU time of the oracle leg")
     ap.add_argument("--layers", type=int, default=0,
                     help="model-step mode: L layers, each with its own KV cache, one pa_forward per layer; "
                          "times one CUDA graph of all L layers against L one-layer graphs and eager calls")
-    ap.add_argument("--min-warm-ms", type=float, default=500.0,
-                    help="graph warm-up time before the timed region (clocks settle); 0 for profiling runs")
+    ap.add_argument("--settle-ms", type=float, default=SETTLE_MS,
+                    help="graph replays before the timed region so that clocks settle; 0 for profiling runs")
     return ap.parse_args(argv)
 
 
@@ -126,10 +154,13 @@ def work_of(batch):
     flops = 4 * D * Hq * batch.causal_pairs()
     q_lens = batch.q_lens()
     qmax = 16 // (Hq // batch.num_kv_heads) if Hq // batch.num_kv_heads <= 16 else 1  # decode-path tokens
-    dec_kv = sum(L for n, L in zip(q_lens, batch.seq_lens.tolist()) if 1 <= n <= qmax) * 2 * batch.num_kv_heads * D * 2
-    dec_tokens = sum(n for n in q_lens if 1 <= n <= qmax)
+    dec = [(n, L) for n, L in zip(q_lens, batch.seq_lens.tolist()) if 1 <= n <= qmax]
+    dec_kv = sum(L for _, L in dec) * 2 * batch.num_kv_heads * D * 2
+    dec_tokens = sum(n for n, _ in dec)
+    dec_pages = sum((L + batch.page_size - 1) // batch.page_size for _, L in dec)
     return dict(kv_bytes=kv, flops=flops, tokens=batch.num_tokens,
-                decode_bytes=dec_kv + dec_tokens * Hq * D * 2 + pages * 4,
+                # K and V of the decode sequences, their q and out rows, 4 B per block-table entry
+                decode_bytes=dec_kv + 2 * dec_tokens * Hq * D * 2 + dec_pages * 4,
                 algorithmic_bytes=kv + 2 * q_bytes + pages * 4)
 
 
@@ -158,7 +189,7 @@ def measured_peaks():
     return dict(
         hbm=(float(hbm), "measured") if hbm else (FALLBACK_HBM_GBS, "fallback"),
         bf16=(float(bf16), "measured") if bf16 else (FALLBACK_BF16_TFLOPS, "fallback"),
-        bf16_sustained=(float(bf16s), "measured") if bf16s else (1700.0, "fallback"),
+        bf16_sustained=(float(bf16s), "measured") if bf16s else (FALLBACK_BF16_SUSTAINED, "fallback"),
     )
 
 
@@ -191,10 +222,16 @@ def committed_traffic(kernel: str, config: str):
         return None
 
 
+def stats_ms(xs):
+    qs = statistics.quantiles(xs, n=10) if len(xs) >= 2 else [xs[0]] * 9
+    return {"mean": statistics.mean(xs), "median": statistics.median(xs), "p10": qs[0], "p90": qs[-1],
+            "n": len(xs)}
+
+
 # -------------------------------------------------------------------- clocks
 
 class ClockSampler:
-    """nvidia-smi sampling (200 ms) running across the warm-up and timed region."""
+    """nvidia-smi sampling (200 ms) running across the warm-up and timed phases."""
 
     FIELDS = ("timestamp,index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
@@ -224,7 +261,7 @@ class ClockSampler:
             except subprocess.TimeoutExpired:
                 self.proc.kill()
 
-    def summary(self, t0: float, t1: float):
+    def summary(self, t0: float, t1: float, what: str):
         if self.proc is None or not self.path:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0, "note": "nvidia-smi unavailable"}
         rows = []
@@ -239,10 +276,10 @@ class ClockSampler:
                 continue
         os.unlink(self.path)
         inside = [r for r in rows if t0 <= r[0] <= t1]
-        note = "samples inside the timed region"
+        note = f"samples inside {what}"
         if not inside:
             inside = rows[-3:]
-            note = "timed region shorter than the sampling period; last samples of the loaded run"
+            note = f"{what} shorter than the sampling period; last samples of the loaded run"
         if not inside:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0, "note": "no samples"}
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
@@ -253,18 +290,28 @@ class ClockSampler:
 
 # ------------------------------------------------------------- CPU baseline
 
-def cpu_baseline(batch, config, target_s: float):
-    """The fp64 oracle, as it stands, on this host's cores, on a bounded sample."""
+def cpu_model() -> str:
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for line in out.splitlines():
+            if line.startswith("Model name:"):
+                return line.split(":", 1)[1].strip()
+    except (OSError, subprocess.SubprocessError):
+        pass
+    return platform.processor() or platform.machine()
+
+
+def _oracle_rate(batch, config, target_s: float, threads: int):
+    """Seconds per whole step of the oracle on `threads` host threads (0: all),
+    from a bounded sample of (token, head) rows spread over the batch."""
     import oracle
     Hq = batch.num_q_heads
-    work = work_of(batch)
     total_rows = batch.num_tokens * Hq
-    # keys per row decide the cost; pick rows evenly over the batch
     rows = [(t, h) for t in range(batch.num_tokens) for h in range(Hq)]
     n = len(rows)
     probe = rows[:: max(1, n // 64)][:64]
     t = time.perf_counter()
-    oracle.batch_attention(batch, rows=probe)
+    oracle.batch_attention(batch, rows=probe, threads=threads)
     per_row = (time.perf_counter() - t) / len(probe)
     want = max(1, int(target_s / max(per_row, 1e-9)))
     if want >= n:
@@ -275,15 +322,25 @@ def cpu_baseline(batch, config, target_s: float):
         reps = 1
     t = time.perf_counter()
     for _ in range(reps):
-        oracle.batch_attention(batch, rows=sample)
+        oracle.batch_attention(batch, rows=sample, threads=threads)
     elapsed = time.perf_counter() - t
     frac = len(sample) * reps / total_rows
-    step_s = elapsed / frac
-    metric, unit, _ = metric_of(config)
+    return elapsed / frac, f"{len(sample)} of {total_rows} (token, head) rows x {reps} repetition(s), " \
+                           f"{elapsed:.1f} s; step time scaled by the row fraction"
+
+
+def cpu_baseline(batch, config, target_s: float):
+    """The fp64 oracle, as it stands, on this host's cores (all of them, and one),
+    on bounded samples of the workload."""
+    import oracle
+    work = work_of(batch)
+    _, unit, _ = metric_of(config)
+    step_s, sample = _oracle_rate(batch, config, target_s, 0)
+    step1_s, sample1 = _oracle_rate(batch, config, max(1.0, target_s / 3), 1)
     return {"value": value_of(config, work, step_s), "unit": unit, "cores": oracle.max_threads(),
-            "kind": "oracle",
-            "sample": f"{len(sample)} of {total_rows} (token, head) rows x {reps} repetition(s), "
-                      f"{elapsed:.1f} s; step time scaled by the row fraction"}
+            "kind": "oracle", "sample": sample, "cpu_model": cpu_model(), "nproc": os.cpu_count(),
+            "single_thread": {"value": value_of(config, work, step1_s), "unit": unit, "threads": 1,
+                              "sample": sample1}}
 
 
 def run_reference(args):
@@ -292,6 +349,7 @@ def run_reference(args):
     if rank != 0:
         return 0
     import torch
+    import oracle
     from paged_kv_cache_forward_gb300 import workloads as W
     torch.manual_seed(0)
     batch = W.CONFIGS[args.config](seed=args.seed)
@@ -300,18 +358,17 @@ def run_reference(args):
     warm = max(0, min(args.warmup, 1))
     budget = min(120.0 / max(1, steps + warm), args.cpu_seconds)
     for _ in range(warm):
-        cpu_baseline(batch, args.config, min(budget, 5.0))
-    vals = [cpu_baseline(batch, args.config, budget) for _ in range(steps)]
-    v = statistics.median(x["value"] for x in vals)
-    step_s = (work_of(batch)["flops"] / v / 1e12) if args.config == "varlen_prefill" else \
-        (work_of(batch)["kv_bytes"] / v / 1e9)
+        _oracle_rate(batch, args.config, min(budget, 5.0), 0)
+    runs = [_oracle_rate(batch, args.config, budget, 0) for _ in range(steps)]
+    step_s = statistics.median(r[0] for r in runs)
+    v = value_of(args.config, work_of(batch), step_s)
     line = {
         "impl": "reference", "metric": metric, "value": v, "unit": unit, "n_gpus": args.gpus, "steps": steps,
         "warmup": warm, "ms_per_step": step_s * 1e3, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f64", "data": "synthetic",
         "config": {"workload": f"{args.config}: {DESCRIPTIONS.get(args.config, '')}", "seed": args.seed},
-        "cpu_baseline": {"value": v, "unit": unit, "cores": vals[0]["cores"], "kind": "oracle",
-                         "sample": vals[0]["sample"]},
+        "cpu_baseline": {"value": v, "unit": unit, "cores": oracle.max_threads(), "kind": "oracle",
+                         "sample": runs[0][1], "cpu_model": cpu_model(), "nproc": os.cpu_count()},
         "e2e": {"value": v, "unit": unit, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
         "gpu_launches": 0,
     }
@@ -321,117 +378,271 @@ def run_reference(args):
 
 # --------------------------------------------------------------------- ours
 
-def run_ours(args):
-    import torch
-    import paged_kv_cache_forward_gb300 as pa
-    from paged_kv_cache_forward_gb300 import build as build_mod
-    from paged_kv_cache_forward_gb300 import workloads as W
+class Workload:
+    """One workload on the device: the batch, R rotating KV pool copies, the
+    output, a stream, the launch plan and the forward call."""
 
-    rank, world, local = dist_env()
-    if world > 1:
-        import torch.distributed as dist
-        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
-    torch.cuda.set_device(local)
-    dev = torch.device("cuda", local)
-    build_mod.build()
-    pa.load()
+    def __init__(self, config, seed, dev, kv_chunk=0):
+        import torch
+        import paged_kv_cache_forward_gb300 as pa
+        from paged_kv_cache_forward_gb300 import workloads as W
+        self.pa, self.torch, self.config, self.dev, self.kv_chunk = pa, torch, config, dev, kv_chunk
+        self.batch = W.CONFIGS[config](seed=seed)
+        self.work = work_of(self.batch)
+        props = torch.cuda.get_device_properties(dev)
+        self.l2 = getattr(props, "L2_cache_size", 128 << 20) or (128 << 20)
+        per_step = max(self.work["kv_bytes"], 1)
+        self.R = 1 if per_step > 3 * self.l2 else int(math.ceil(3 * self.l2 / per_step)) + 1
+        d = self.batch.to(dev)
+        self.d = d
+        self.ks = [d.k_cache] + [d.k_cache.clone() for _ in range(self.R - 1)]
+        self.vs = [d.v_cache] + [d.v_cache.clone() for _ in range(self.R - 1)]
+        self.out = torch.empty_like(d.q)
+        self.stream = torch.cuda.Stream(device=dev)
+        torch.cuda.synchronize(dev)  # inputs and pool copies were made on the default stream
+        self.plan = pa.plan_for(d.q, d.k_cache, d.block_table, d.seq_lens, kv_chunk=kv_chunk)
+        pa.prepare(d.q, d.k_cache, d.block_table, d.seq_lens, kv_chunk=kv_chunk, stream=self.stream)
+        b = self.batch
+        G = b.num_q_heads // b.num_kv_heads
+        qmax = 16 // G if G <= 16 else 1
+        has_decode = any(1 <= n <= qmax for n in b.q_lens())
+        self.dominant = "prefill" if (config == "varlen_prefill" or not has_decode) else "decode_splitkv"
 
-    batch = W.CONFIGS[args.config](seed=rank_seed(args.seed, rank))
-    work = work_of(batch)
-    metric, unit, bound = metric_of(args.config)
-    props = torch.cuda.get_device_properties(dev)
-    l2 = getattr(props, "L2_cache_size", 128 << 20) or (128 << 20)
-    per_step = max(work["kv_bytes"], 1)
-    R = 1 if per_step > 3 * l2 else int(math.ceil(3 * l2 / per_step)) + 1
+    def call(self, i, events=None, launch_only=0, out=None):
+        d = self.d
+        self.pa.forward(d.q, self.ks[i % self.R], self.vs[i % self.R], d.block_table, d.seq_lens, d.query_start_loc,
+                        self.out if out is None else out, scale=self.batch.scale, kv_chunk=self.kv_chunk,
+                        events=events, stream=self.stream, launch_only=launch_only)
 
-    d = batch.to(dev)
-    ks = [d.k_cache] + [d.k_cache.clone() for _ in range(R - 1)]
-    vs = [d.v_cache] + [d.v_cache.clone() for _ in range(R - 1)]
-    out = torch.empty_like(d.q)
-    stream = torch.cuda.Stream(device=dev)
-    torch.cuda.synchronize(dev)  # inputs and pool copies were made on the default stream
-    plan = pa.plan_for(d.q, d.k_cache, d.block_table, d.seq_lens, kv_chunk=args.kv_chunk)
-    pa.prepare(d.q, d.k_cache, d.block_table, d.seq_lens, kv_chunk=args.kv_chunk, stream=stream)
-    G = batch.num_q_heads // batch.num_kv_heads
-    qmax = 16 // G if G <= 16 else 1
-    has_decode = any(1 <= n <= qmax for n in batch.q_lens())
-    dominant = "prefill" if (args.config == "varlen_prefill" or not has_decode) else "decode_splitkv"
+    def graph(self, n, fn):
+        g = self.torch.cuda.CUDAGraph()
+        with self.torch.cuda.graph(g, stream=self.stream):
+            for i in range(n):
+                fn(i)
+        return g
 
-    def call(i, events=None):
-        pa.forward(d.q, ks[i % R], vs[i % R], d.block_table, d.seq_lens, d.query_start_loc, out,
-                   scale=batch.scale, kv_chunk=args.kv_chunk, events=events, stream=stream)
 
-    # eager warm-up (loads the kernels, sets attributes)
+def time_kernel(wl, world):
+    """Mean, median, p10, p90 launch duration (ms) of the dominant kernel alone:
+    a graph of KERNEL_RUN consecutive launches (the pool copies in rotation)
+    bracketed by CUDA events recorded on the launching stream, replayed at least
+    KERNEL_MIN_RUNS times and for at least KERNEL_MIN_S."""
+    torch = wl.torch
+    key = "prefill" if wl.dominant == "prefill" else "decode"
+    only = (2 if key == "prefill" else 1) if wl.plan["launches"] > 1 else 0
+    run = max(KERNEL_RUN, wl.R) // wl.R * wl.R if wl.R <= KERNEL_RUN else wl.R
+    e_a, e_b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    # torch creates the CUDA event on its first record(); do that outside the
+    # capture so that the library receives real handles to re-record.
+    e_a.record(wl.stream)
+    e_b.record(wl.stream)
+    wl.stream.synchronize()
+
+    def launch(i):
+        ev = {}
+        if i == 0:
+            ev[f"{key}_start_event"] = e_a
+        if i == run - 1:
+            ev[f"{key}_stop_event"] = e_b
+        wl.call(i, events=ev, launch_only=only)
+
+    g = wl.graph(run, launch)
+    with torch.cuda.stream(wl.stream):  # a graph replays on the current stream
+        g.replay()
+    wl.stream.synchronize()
+    first = e_a.elapsed_time(e_b) / run
+    n_runs = max(KERNEL_MIN_RUNS, int(math.ceil(KERNEL_MIN_S / max(first * run / 1e3, 1e-6))))
+    per = []
+    for _ in range(n_runs):
+        with torch.cuda.stream(wl.stream):
+            g.replay()
+        wl.stream.synchronize()
+        per.append(e_a.elapsed_time(e_b) / run)
+    del g
+    per_max = reduce_max(statistics.mean(per), world, wl.dev)
+    st = stats_ms(per)
+    st["mean_max_over_ranks"] = per_max
+    st["how"] = (f"{'only the ' + key + ' kernel launched' if only else 'the whole step is this kernel'}; "
+                 f"CUDA events around runs of {run} consecutive launches, {n_runs} runs")
+    return st
+
+
+def time_e2e(wl, world, est_ms):
+    """The metric through the public API with host buffers: every step copies its
+    q and metadata in from pinned host memory (one packed copy) and its out back.
+    Best of eager calls, captured graphs of 64 steps, and a captured pipeline whose
+    copies overlap the neighbouring steps' forwards; each mode timed over at least
+    E2E_MIN_S after one untimed pass."""
+    torch, pa, b, dev, stream = wl.torch, wl.pa, wl.batch, wl.dev, wl.stream
+    parts = [b.q, b.block_table, b.seq_lens, b.query_start_loc]
+    offs, total = [], 0
+    for t in parts:
+        offs.append(total)
+        total += (t.numel() * t.element_size() + 15) // 16 * 16
+    hbuf = torch.empty(total, dtype=torch.uint8, pin_memory=True)
+    dbuf = torch.empty(total, dtype=torch.uint8, device=dev)
+
+    def view(buf, k):
+        t = parts[k]
+        return buf[offs[k]:offs[k] + t.numel() * t.element_size()].view(t.dtype).view(t.shape)
+
+    for k, t in enumerate(parts):
+        view(hbuf, k).copy_(t)
+    eq, ebt, esl, eqsl = (view(dbuf, k) for k in range(4))
+    out = wl.out
+    hout = torch.empty(out.shape, dtype=out.dtype, pin_memory=True)
+    R, ks, vs = wl.R, wl.ks, wl.vs
+    Me = 64
+    n_e2e = max(Me, int(math.ceil(E2E_MIN_S / max(est_ms / 1e3, 1e-7) / Me)) * Me)
+
+    def e2e_step(i):
+        dbuf.copy_(hbuf, non_blocking=True)
+        pa.forward(eq, ks[i % R], vs[i % R], ebt, esl, eqsl, out, scale=b.scale, kv_chunk=wl.kv_chunk, stream=stream)
+        hout.copy_(out, non_blocking=True)
+
+    def timed(fn, reps):
+        a0, a1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        stream.synchronize()
+        barrier(world)
+        with torch.cuda.stream(stream):
+            a0.record()
+            for r in range(reps):
+                fn(r)
+            a1.record()
+        stream.synchronize()
+        barrier(world)
+        return a0.elapsed_time(a1)
+
     with torch.cuda.stream(stream):
-        for i in range(max(3, args.warmup)):
-            call(i)
+        for i in range(3):
+            e2e_step(i)
+    # (a) eager: copies and pa_forward launched from the host every step
+    eager_ms = reduce_max(timed(e2e_step, n_e2e), world, dev) / n_e2e
+    # (b) the same steps captured in CUDA graphs of Me steps, replayed: what a
+    # serving loop that captures its decode step sees
+    ge = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(ge, stream=stream):
+        for i in range(Me):
+            e2e_step(i)
+    reps = n_e2e // Me
+    with torch.cuda.stream(stream):  # a graph replays on the current stream
+        ge.replay()
+    graph_ms = reduce_max(timed(lambda r: ge.replay(), reps), world, dev) / (reps * Me)
+    del ge
+    # (c) the same steps pipelined inside a CUDA graph: inputs copied in on one
+    # side stream, results copied out on another, two alternating input arenas
+    # and output buffers; step i+1's input copy and step i-1's output copy
+    # overlap step i's forward.  Every step still copies its own inputs in and
+    # its own result out.
+    cs_in, cs_out = torch.cuda.Stream(device=dev), torch.cuda.Stream(device=dev)
+    dbufs = [dbuf, torch.empty_like(dbuf)]
+    outs2 = [out, torch.empty_like(out)]
+    houts = [hout, torch.empty(out.shape, dtype=out.dtype, pin_memory=True)]
+    arenas = [[view(db, k) for k in range(4)] for db in dbufs]
+    gp = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(gp, stream=stream):
+        ev_fwd = [torch.cuda.Event(), torch.cuda.Event()]
+        ev_out = [torch.cuda.Event(), torch.cuda.Event()]
+        ev_start = torch.cuda.Event()
+        ev_start.record(stream)
+        cs_in.wait_event(ev_start)
+        cs_out.wait_event(ev_start)
+        for i in range(Me):
+            k = i & 1
+            ev_in = torch.cuda.Event()
+            with torch.cuda.stream(cs_in):
+                if i >= 2:
+                    cs_in.wait_event(ev_fwd[k])  # forward(i-2) has read arena k
+                dbufs[k].copy_(hbuf, non_blocking=True)
+                ev_in.record(cs_in)
+            stream.wait_event(ev_in)
+            if i >= 2:
+                stream.wait_event(ev_out[k])  # out k copied out by step i-2
+            qv, btv, slv, qslv = arenas[k]
+            pa.forward(qv, ks[i % R], vs[i % R], btv, slv, qslv, outs2[k], scale=b.scale,
+                       kv_chunk=wl.kv_chunk, stream=stream)
+            ev_fwd[k] = torch.cuda.Event()
+            ev_fwd[k].record(stream)
+            with torch.cuda.stream(cs_out):
+                cs_out.wait_event(ev_fwd[k])
+                houts[k].copy_(outs2[k], non_blocking=True)
+                ev_out[k] = torch.cuda.Event()
+                ev_out[k].record(cs_out)
+        ev_end_in, ev_end_out = torch.cuda.Event(), torch.cuda.Event()
+        ev_end_in.record(cs_in)
+        ev_end_out.record(cs_out)
+        stream.wait_event(ev_end_in)
+        stream.wait_event(ev_end_out)
+    with torch.cuda.stream(stream):
+        gp.replay()
+    pipe_ms = reduce_max(timed(lambda r: gp.replay(), reps), world, dev) / (reps * Me)
+    del gp
+    h2d = sum(t.numel() * t.element_size() for t in parts)
+    what = ("per step: q and metadata copied (one packed copy) from pinned host memory, pa_forward, out "
+            "copied to pinned host memory, serial on one stream; KV cache resident")
+    modes = {
+        "graph_pipelined": (pipe_ms, "per step: q and metadata copied (one packed copy) from pinned host memory "
+                                     "on a side stream, pa_forward, out copied to pinned host memory on a second "
+                                     "side stream, two alternating input/output buffers so that neighbouring "
+                                     f"steps' copies overlap the forward; captured in CUDA graphs of {Me} steps; "
+                                     "KV cache resident"),
+        "graph": (graph_ms, what + f"; steps captured in CUDA graphs of {Me} and replayed"),
+        "eager": (eager_ms, what + "; launched eagerly from the host"),
+    }
+    best = min(modes, key=lambda m: modes[m][0])
+    return {"ms_per_step": modes[best][0], "steps": n_e2e, "mode": best + ": " + modes[best][1],
+            "modes_ms_per_step": {m: v[0] for m, v in modes.items()},
+            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": hout.numel() * hout.element_size()}
+
+
+def measure(config, args, dev, rank, world, local, steps=None, warmup=None, with_e2e=True, region_s=2.0):
+    """One workload's record: timed region, kernel roofline, e2e, clocks."""
+    import torch
+    torch.cuda.synchronize(dev)
+    wl = Workload(config, rank_seed(args.seed, rank), dev, args.kv_chunk)
+    work, pa, stream = wl.work, wl.pa, wl.stream
+    metric, unit, _ = metric_of(config)
+    W_req = args.warmup if warmup is None else warmup
+
+    # W untimed warm-up steps (the first also loads the kernels)
+    with torch.cuda.stream(stream):
+        for i in range(max(1, W_req)):
+            wl.call(i)
     stream.synchronize()
     assert pa.device_error(stream) == 0
 
-    # time one eager step to size the default step count (about 2 s of timed work)
+    # one eager step's time sizes the default step count and the e2e phase
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     with torch.cuda.stream(stream):
         e0.record()
         for i in range(10):
-            call(i)
+            wl.call(i)
         e1.record()
     stream.synchronize()
     est_ms = e0.elapsed_time(e1) / 10
-    steps = args.steps if args.steps else int(min(200000, max(200, 2000.0 / max(est_ms, 1e-3))))
+    if steps is None:
+        steps = int(min(200000, max(200, region_s * 1e3 / max(est_ms, 1e-3))))
 
-    # graphs of M consecutive steps each, rotating over the R pool copies.  The
-    # dominant kernel's launches are timed by pairs of external events: when a
-    # step is that one kernel, each pair brackets a run of RUN consecutive
-    # launches (one run in every EVERY steps; the mean launch duration is the
-    # run's time / RUN); when a step launches more kernels, each pair brackets
-    # the dominant kernel of one step in EVERY.  (An event node between two
-    # kernels costs the graph a few microseconds, which a lone bracket charges
-    # to the kernel it surrounds.)  Their durations give roofline.achieved.
-    EVERY = 8
+    # graphs of M consecutive steps, rotating over the R pool copies
+    R = wl.R
     M = min(steps, max(R, 256))
     M = max(R, (M // R) * R) if M >= R else M
-    key = "prefill" if dominant == "prefill" else "decode"
-    RUN = 16 if plan["launches"] == 1 and M >= 16 else 1
-    if RUN > 1:
-        EVERY = 64
-
-    def make_graph(n):
-        starts = [i for i in range(0, n, EVERY) if i + RUN <= n]
-        evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in starts]
-        # torch creates the CUDA event on its first record(); do that outside the
-        # capture so that the library receives real handles to re-record.
-        for e_a, e_b in evs:
-            e_a.record(stream)
-            e_b.record(stream)
-        stream.synchronize()
-        g = torch.cuda.CUDAGraph()
-        with torch.cuda.graph(g, stream=stream):
-            for i in range(n):
-                ev = {}
-                k, r = divmod(i, EVERY)
-                if k < len(evs):
-                    if r == 0:
-                        ev[f"{key}_start_event"] = evs[k][0]
-                    if r == RUN - 1:
-                        ev[f"{key}_stop_event"] = evs[k][1]
-                call(i, events=ev or None)
-        return g, evs
-
     full, rem = divmod(steps, M)
-    g_main, ev_main = make_graph(M)
-    g_rem, ev_rem = make_graph(rem) if rem else (None, [])
+    g_main = wl.graph(M, wl.call)
+    g_rem = wl.graph(rem, wl.call) if rem else None
 
     sampler = ClockSampler(local).start()
-    # graph warm-up: at least W steps, and at least ~0.5 s so that clocks settle
-    warm_reps = max(1, int(math.ceil(args.warmup / M)), int(args.min_warm_ms / max(est_ms * M, 1e-3)))
-    for _ in range(warm_reps):
-        g_main.replay()
+    t_load0 = time.time()
+    # clock settling: graph replays for about args.settle_ms (not counted as warm-up)
+    settle_reps = int(math.ceil(args.settle_ms / max(est_ms * M, 1e-3))) if args.settle_ms > 0 else 0
+    with torch.cuda.stream(stream):  # a graph replays on the current stream
+        for _ in range(settle_reps):
+            g_main.replay()
     stream.synchronize()
 
     start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     barrier(world)
     torch.cuda.synchronize(dev)
-    t0 = time.time()
     with torch.cuda.stream(stream):
         start.record()
         for _ in range(full):
@@ -441,12 +652,14 @@ def run_ours(args):
         stop.record()
     stream.synchronize()
     torch.cuda.synchronize(dev)
-    t1 = time.time()
     barrier(world)
-    sampler.stop()
     region_ms = start.elapsed_time(stop)
-    # the last replay of each graph left its events' times
-    kernel_ms = [a.elapsed_time(b) / RUN for a, b in ev_main + ev_rem]
+    assert pa.device_error(stream) == 0
+    del g_main, g_rem
+
+    kern = time_kernel(wl, world)
+    t_load1 = time.time()
+    sampler.stop()
     assert pa.device_error(stream) == 0
 
     region_ms_max = reduce_max(region_ms, world, dev)
@@ -454,233 +667,88 @@ def run_ours(args):
     total_kv = reduce_sum(work["kv_bytes"], world, dev)
     total_flops = reduce_sum(work["flops"], world, dev)
     total_tokens = reduce_sum(work["tokens"], world, dev)
-    if args.config == "varlen_prefill":
-        value = total_flops * steps / (region_ms_max / 1e3) / 1e12
-    else:
-        value = total_kv * steps / (region_ms_max / 1e3) / 1e9
+    value = value_of(config, {"kv_bytes": total_kv, "flops": total_flops}, region_ms_max / 1e3 / steps)
 
-    # roofline of the dominant kernel
     peaks = measured_peaks()
-    k_ms = statistics.mean(kernel_ms)
-    if dominant == "prefill":
-        peak, src = peaks["bf16"]
+    k_ms = kern["mean"]
+    if wl.dominant == "prefill":
+        # The prefill kernel is timed over a second or more of back-to-back
+        # launches, under the power cap: the sustained bf16 rate is its peak.
+        peak, src = peaks["bf16_sustained"]
         achieved = work["flops"] / (k_ms / 1e3) / 1e12
-        roof = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
-                "frac": achieved / peak, "peak_source": src}
+        roof = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s", "frac": achieved / peak,
+                "peak_source": f"{src} (sustained bf16)", "frac_of_burst_peak": achieved / peaks["bf16"][0]}
+        per_launch = work["flops"]
     else:
         peak, src = peaks["hbm"]
         achieved = work["decode_bytes"] / (k_ms / 1e3) / 1e9
         roof = {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
-                "peak_source": src}
-    traffic = committed_traffic(dominant, args.config)
-    qs = statistics.quantiles(kernel_ms, n=10) if len(kernel_ms) >= 2 else [k_ms] * 9
-    roof.update({"traffic": traffic, "kernel": dominant, "kernel_ms_mean": k_ms,
-                 "kernel_ms_median": statistics.median(kernel_ms),
-                 "kernel_ms_p10": qs[0], "kernel_ms_p90": qs[-1],
-                 "algorithmic_per_launch": work["flops"] if dominant == "prefill" else work["decode_bytes"]})
+                "peak_source": f"{src} (copy bandwidth)"}
+        per_launch = work["decode_bytes"]
+    roof.update({"traffic": committed_traffic(wl.dominant, config), "kernel": wl.dominant,
+                 "kernel_ms_mean": k_ms, "kernel_ms_median": kern["median"], "kernel_ms_p10": kern["p10"],
+                 "kernel_ms_p90": kern["p90"], "kernel_runs": kern["n"], "kernel_timing": kern["how"],
+                 "algorithmic_per_launch": per_launch})
 
     hbm_frac = (total_kv / world) / (ms_per_step / 1e3) / 1e9 / peaks["hbm"][0]
-    tensor_frac = (total_flops / world) / (ms_per_step / 1e3) / 1e12 / peaks["bf16"][0]
+    # (the timed regions last half a second or more: the sustained bf16 rate)
+    tensor_frac = (total_flops / world) / (ms_per_step / 1e3) / 1e12 / peaks["bf16_sustained"][0]
 
-    # end to end through the public API: pinned host inputs -> device, forward, result -> host
     e2e = None
-    if not args.no_e2e:
-        # A step's inputs (q, block table, lengths, query offsets) packed in one
-        # pinned host buffer and one device arena (16-byte aligned parts), so a
-        # step is one host-to-device copy, pa_forward on views of the arena, and
-        # one device-to-host copy of out.
-        parts = [batch.q, batch.block_table, batch.seq_lens, batch.query_start_loc]
-        offs, total = [], 0
-        for t in parts:
-            offs.append(total)
-            total += (t.numel() * t.element_size() + 15) // 16 * 16
-        hbuf = torch.empty(total, dtype=torch.uint8, pin_memory=True)
-        dbuf = torch.empty(total, dtype=torch.uint8, device=dev)
+    if with_e2e and not args.no_e2e:
+        e = time_e2e(wl, world, est_ms)
+        e2e = {"value": value_of(config, {"kv_bytes": total_kv, "flops": total_flops}, e["ms_per_step"] / 1e3),
+               "unit": unit, **e}
+    assert pa.device_error(stream) == 0
 
-        def view(buf, k):
-            t = parts[k]
-            return buf[offs[k]:offs[k] + t.numel() * t.element_size()].view(t.dtype).view(t.shape)
-
-        for k, t in enumerate(parts):
-            view(hbuf, k).copy_(t)
-        eq, ebt, esl, eqsl = (view(dbuf, k) for k in range(4))
-        hout = torch.empty(out.shape, dtype=out.dtype, pin_memory=True)
-        n_e2e = min(steps, 2048)
-
-        def e2e_step(i):
-            dbuf.copy_(hbuf, non_blocking=True)
-            pa.forward(eq, ks[i % R], vs[i % R], ebt, esl, eqsl, out, scale=batch.scale, kv_chunk=args.kv_chunk,
-                       stream=stream)
-            hout.copy_(out, non_blocking=True)
-
-        def timed(fn, reps):
-            a0, a1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-            stream.synchronize()
-            barrier(world)
-            with torch.cuda.stream(stream):
-                a0.record()
-                for r in range(reps):
-                    fn(r)
-                a1.record()
-            stream.synchronize()
-            barrier(world)
-            return a0.elapsed_time(a1)
-
-        with torch.cuda.stream(stream):
-            for i in range(3):
-                e2e_step(i)
-        # (a) eager: copies and pa_forward launched from the host every step
-        eager_ms = reduce_max(timed(e2e_step, n_e2e), world, dev) / n_e2e
-        # (b) the same steps captured in a CUDA graph (copies from pinned memory
-        # and the forward), replayed: what a serving loop that captures its
-        # decode step sees
-        Me = min(64, n_e2e)
-        ge = torch.cuda.CUDAGraph()
-        with torch.cuda.graph(ge, stream=stream):
-            for i in range(Me):
-                e2e_step(i)
-        reps = max(1, n_e2e // Me)
-        ge.replay()
-        graph_ms = reduce_max(timed(lambda r: ge.replay(), reps), world, dev) / (reps * Me)
-        del ge
-        # (c) the same steps pipelined inside a CUDA graph: inputs copied in on one
-        # side stream, results copied out on another, two alternating input arenas
-        # and output buffers; step i+1's input copy and step i-1's output copy
-        # overlap step i's forward.  Every step still copies its own inputs in and
-        # its own result out.
-        cs_in, cs_out = torch.cuda.Stream(device=dev), torch.cuda.Stream(device=dev)
-        dbufs = [dbuf, torch.empty_like(dbuf)]
-        outs2 = [out, torch.empty_like(out)]
-        houts = [hout, torch.empty(out.shape, dtype=out.dtype, pin_memory=True)]
-        arenas = [[view(db, k) for k in range(4)] for db in dbufs]
-        gp = torch.cuda.CUDAGraph()
-        with torch.cuda.graph(gp, stream=stream):
-            ev_fwd = [torch.cuda.Event(), torch.cuda.Event()]
-            ev_out = [torch.cuda.Event(), torch.cuda.Event()]
-            ev_start = torch.cuda.Event()
-            ev_start.record(stream)
-            cs_in.wait_event(ev_start)
-            cs_out.wait_event(ev_start)
-            for i in range(Me):
-                k = i & 1
-                ev_in = torch.cuda.Event()
-                with torch.cuda.stream(cs_in):
-                    if i >= 2:
-                        cs_in.wait_event(ev_fwd[k])  # forward(i-2) has read arena k
-                    dbufs[k].copy_(hbuf, non_blocking=True)
-                    ev_in.record(cs_in)
-                stream.wait_event(ev_in)
-                if i >= 2:
-                    stream.wait_event(ev_out[k])  # out k copied out by step i-2
-                qv, btv, slv, qslv = arenas[k]
-                pa.forward(qv, ks[i % R], vs[i % R], btv, slv, qslv, outs2[k], scale=batch.scale,
-                           kv_chunk=args.kv_chunk, stream=stream)
-                ev_fwd[k] = torch.cuda.Event()
-                ev_fwd[k].record(stream)
-                with torch.cuda.stream(cs_out):
-                    cs_out.wait_event(ev_fwd[k])
-                    houts[k].copy_(outs2[k], non_blocking=True)
-                    ev_out[k] = torch.cuda.Event()
-                    ev_out[k].record(cs_out)
-            ev_end_in, ev_end_out = torch.cuda.Event(), torch.cuda.Event()
-            ev_end_in.record(cs_in)
-            ev_end_out.record(cs_out)
-            stream.wait_event(ev_end_in)
-            stream.wait_event(ev_end_out)
-        gp.replay()
-        pipe_ms = reduce_max(timed(lambda r: gp.replay(), reps), world, dev) / (reps * Me)
-        del gp
-        h2d = sum(t.numel() * t.element_size() for t in parts)
-        work_all = {"kv_bytes": total_kv, "flops": total_flops}
-        what = ("per step: q and metadata copied (one packed copy) from pinned host memory, pa_forward, out "
-                "copied to pinned host memory, serial on one stream; KV cache resident")
-        modes = {
-            "graph_pipelined": (pipe_ms, "per step: q and metadata copied (one packed copy) from pinned host memory "
-                                         "on a side stream, pa_forward, out copied to pinned host memory on a second "
-                                         "side stream, two alternating input/output buffers so that neighbouring "
-                                         "steps' copies overlap the forward; captured in CUDA graphs of 64 steps; "
-                                         "KV cache resident"),
-            "graph": (graph_ms, what + "; steps captured in CUDA graphs of 64 and replayed"),
-            "eager": (eager_ms, what + "; launched eagerly from the host"),
-        }
-        best = min(modes, key=lambda m: modes[m][0])
-        e_ms = modes[best][0]
-        e2e = {"value": value_of(args.config, work_all, e_ms / 1e3),
-               "unit": unit, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": hout.numel() * hout.element_size(),
-               "ms_per_step": e_ms, "steps": n_e2e, "mode": best + ": " + modes[best][1],
-               "modes_ms_per_step": {m: v[0] for m, v in modes.items()}}
-
-    cpu = None
-    if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        cpu = cpu_baseline(batch, args.config, args.cpu_seconds)
-
-    clocks = sampler.summary(t0, t1)
-    if rank == 0:
-        line = {
-            "metric": metric, "value": value, "unit": unit, "n_gpus": world, "steps": steps,
-            "warmup": warm_reps * M, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
-            "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-            "config": {
-                "workload": f"{args.config}: {DESCRIPTIONS.get(args.config, '')}",
-                "seed": args.seed, "global_batch": batch.num_seqs * world, "tokens_per_step": int(total_tokens),
-                "kv_bytes_per_step": int(total_kv), "causal_flops_per_step": int(total_flops),
-                "l2": f"inputs rotate over {R} KV pool copies ({R} x {work['kv_bytes'] / 2**20:.0f} MiB "
-                      f"> 3 x L2 {l2 / 2**20:.0f} MiB)" if R > 1 else "KV bytes per step > 3 x L2",
-                "graph": f"CUDA graphs of {M} steps", "kv_chunk": plan["kv_chunk"], "splits": plan["splits"],
-                "decode_stages": plan["decode_stages"],
-                "kernel_timing": (f"CUDA events around runs of {RUN} consecutive launches of the dominant "
-                                  f"kernel (the whole step), one run in {EVERY} steps of the timed graphs "
-                                  f"({len(kernel_ms)} runs of the last replays)" if RUN > 1 else
-                                  f"CUDA events around the dominant kernel of one step in {EVERY} of the "
-                                  f"timed graphs ({len(kernel_ms)} launches of the last replays)"),
-                "parallelism": f"dp{world}" if world > 1 else "single GPU",
-            },
-            "tok_s": total_tokens * steps / (region_ms_max / 1e3),
-            # one attention layer per step; a 32-layer model's attention alone
-            # could run at most this many tokens/s
-            "tok_s_32_layer_attention_ceiling": total_tokens * steps / (region_ms_max / 1e3) / 32,
-            # whole step against each roofline: KV bytes / HBM, causal FLOPs /
-            # bf16 tensor peak, and the binding one, max(B / BW, F / peak) / t
-            "hbm_frac_step": hbm_frac,
-            "tensor_frac_step": tensor_frac,
-            "roofline_frac_step": max(hbm_frac, tensor_frac),
-            "roofline": roof,
-            "cpu_baseline": cpu,
-            "e2e": e2e,
-            "gpu_launches": plan["launches"] * steps,
-            "clocks": clocks,
-        }
-        print(json.dumps(line))
-    if world > 1:
-        import torch.distributed as dist
-        dist.destroy_process_group()
-    return 0
+    rec = {
+        "metric": metric, "value": value, "unit": unit, "n_gpus": world, "steps": steps, "warmup": W_req,
+        "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "bf16", "data": "synthetic",
+        "config": {
+            "workload": f"{config}: {DESCRIPTIONS.get(config, '')}",
+            "seed": args.seed, "global_batch": wl.batch.num_seqs * world, "tokens_per_step": int(total_tokens),
+            "kv_bytes_per_step": int(total_kv), "causal_flops_per_step": int(total_flops),
+            "l2": (f"inputs rotate over {R} KV pool copies ({R} x {work['kv_bytes'] / 2**20:.0f} MiB "
+                   f"> 3 x L2 {wl.l2 / 2**20:.0f} MiB)") if R > 1 else "KV bytes per step > 3 x L2",
+            "graph": f"CUDA graphs of {M} steps", "settle_ms": round(settle_reps * M * est_ms, 1),
+            "kv_chunk": wl.plan["kv_chunk"], "splits": wl.plan["splits"],
+            "decode_variant": f"{wl.plan['decode_warps']} warps x {wl.plan['decode_stages']} stages, "
+                              f"cluster {wl.plan['decode_cluster']}",
+            "parallelism": f"dp{world}" if world > 1 else "single GPU",
+        },
+        "tok_s": total_tokens * steps / (region_ms_max / 1e3),
+        # one attention layer per step; a 32-layer model's attention alone could
+        # run at most this many tokens/s
+        "tok_s_32_layer_attention_ceiling": total_tokens * steps / (region_ms_max / 1e3) / 32,
+        # whole step against each roofline: KV bytes / HBM, causal FLOPs / bf16
+        # tensor peak, and the binding one, max(B / BW, F / peak) / t
+        "hbm_frac_step": hbm_frac,
+        "tensor_frac_step": tensor_frac,
+        "roofline_frac_step": max(hbm_frac, tensor_frac),
+        "roofline": roof,
+        "peaks": {"hbm_gbs": peaks["hbm"][0], "bf16_tflops": peaks["bf16"][0],
+                  "bf16_tflops_sustained": peaks["bf16_sustained"][0], "source": peaks["hbm"][1]},
+        "e2e": e2e,
+        "gpu_launches": wl.plan["launches"] * steps,
+        "clocks": sampler.summary(t_load0, t_load1, "the settle, timed and kernel-timing phases"),
+    }
+    batch = wl.batch
+    del wl
+    torch.cuda.empty_cache()
+    return rec, batch
 
 
-def run_layers(args):
-    """A decoder step of L attention layers: every layer has its own paged KV
-    cache (same shape, same block table), its own queries and output, and one
-    pa_forward call.  Times three ways of launching the same L calls: one CUDA
-    graph of the whole step, L one-layer graphs replayed back to back, and L
-    eager calls.  value = KV bytes of all layers per second in the one-graph mode."""
+def measure_layers(config, L, args, dev, rank, world, local, steps=50):
+    """A decoder step of L attention layers, every layer with its own paged KV
+    cache, queries and output, one pa_forward per layer: one CUDA graph of the
+    whole step against L one-layer graphs replayed back to back and L eager
+    calls.  Also checks that the one-graph step gives the eager outputs."""
     import torch
     import paged_kv_cache_forward_gb300 as pa
-    from paged_kv_cache_forward_gb300 import build as build_mod
     from paged_kv_cache_forward_gb300 import workloads as W
-
-    rank, world, local = dist_env()
-    if world > 1:
-        import torch.distributed as dist
-        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
-    torch.cuda.set_device(local)
-    dev = torch.device("cuda", local)
-    build_mod.build()
-    pa.load()
-
-    L = args.layers
-    batch = W.CONFIGS[args.config](seed=rank_seed(args.seed, rank))
+    batch = W.CONFIGS[config](seed=rank_seed(args.seed, rank))
     work = work_of(batch)
-    metric, unit, _ = metric_of(args.config)
     pool_bytes = 2 * batch.k_cache.numel() * batch.k_cache.element_size()
     if L * pool_bytes > (96 << 30):
         raise SystemExit(f"{L} layers x {pool_bytes / 2**30:.1f} GiB of KV pool exceed 96 GiB")
@@ -710,7 +778,6 @@ def run_layers(args):
             model_step()
     stream.synchronize()
     assert pa.device_error(stream) == 0
-
     g_full = torch.cuda.CUDAGraph()
     with torch.cuda.graph(g_full, stream=stream):
         model_step()
@@ -720,13 +787,11 @@ def run_layers(args):
         with torch.cuda.graph(g, stream=stream):
             layer(i)
         g_layers.append(g)
-
     modes = {
         "graph_full": lambda: g_full.replay(),
         "graph_per_layer": lambda: [g.replay() for g in g_layers],
         "eager": model_step,
     }
-    steps = args.steps or 50
     sampler = ClockSampler(local).start()
     times = {}
     t0 = time.time()
@@ -750,40 +815,113 @@ def run_layers(args):
     t1 = time.time()
     sampler.stop()
     assert pa.device_error(stream) == 0
-
-    # the one-graph step must give the eager step's outputs
     ref = [o.clone() for o in outs]
-    g_full.replay()
+    with torch.cuda.stream(stream):
+        g_full.replay()
     stream.synchronize()
     identical = all(torch.equal(a, b) for a, b in zip(ref, outs))
-
     total_kv = reduce_sum(work["kv_bytes"], world, dev) * L
     total_flops = reduce_sum(work["flops"], world, dev) * L
     ms = times["graph_full"]
-    value = value_of(args.config, {"kv_bytes": total_kv, "flops": total_flops}, ms / 1e3)
+    metric, unit, _ = metric_of(config)
     peaks = measured_peaks()
+    rec = {
+        "metric": metric, "value": value_of(config, {"kv_bytes": total_kv, "flops": total_flops}, ms / 1e3),
+        "unit": unit, "n_gpus": world, "steps": steps, "warmup": max(3, args.warmup), "ms_per_step": ms,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {
+            "workload": f"{L} layers x {config}: {DESCRIPTIONS.get(config, '')}",
+            "layers": L, "kv_bytes_per_step": int(total_kv), "kv_chunk": plan["kv_chunk"],
+            "splits": plan["splits"],
+            "l2": f"KV bytes per step {total_kv / 2**20:.0f} MiB (> 3 x L2)" if total_kv > 3 * (128 << 20)
+            else f"KV bytes per step {total_kv / 2**20:.0f} MiB (<= 3 x L2)",
+            "parallelism": f"dp{world}" if world > 1 else "single GPU",
+        },
+        "graph_modes_ms_per_step": times,
+        "launch_overhead_us_per_layer": {
+            k: (v - times["graph_full"]) * 1e3 / L for k, v in times.items() if k != "graph_full"},
+        "us_per_layer": ms * 1e3 / L,
+        "hbm_frac_step": (total_kv / world) / (ms / 1e3) / 1e9 / peaks["hbm"][0],
+        "graph_matches_eager": identical,
+        "gpu_launches": plan["launches"] * L * steps,
+        "clocks": sampler.summary(t0, t1, "the timed modes"),
+    }
+    del g_full, g_layers, ks, vs, qs, outs
+    torch.cuda.empty_cache()
+    return rec, identical
+
+
+def _brief(rec):
+    """The figures of a sub-record that a reader compares across workloads."""
+    keep = ("metric", "value", "unit", "steps", "warmup", "ms_per_step", "hbm_frac_step", "tensor_frac_step",
+            "roofline_frac_step", "tok_s", "roofline", "e2e", "gpu_launches", "clocks", "config", "graph_modes_ms_per_step",
+            "launch_overhead_us_per_layer", "us_per_layer", "graph_matches_eager")
+    out = {k: rec[k] for k in keep if k in rec}
+    if out.get("e2e"):
+        out["e2e"] = {k: v for k, v in out["e2e"].items() if k != "mode"}
+    return out
+
+
+def run_ours(args):
+    import torch
+    import paged_kv_cache_forward_gb300 as pa
+    from paged_kv_cache_forward_gb300 import build as build_mod
+
+    rank, world, local = dist_env()
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    build_mod.build()
+    pa.load()
+
+    line, batch = measure(args.config, args, dev, rank, world, local, steps=args.steps)
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        cpu = cpu_baseline(batch, args.config, args.cpu_seconds)
+    del batch
+    line["cpu_baseline"] = cpu
+
+    ok = True
+    if world == 1 and not args.no_sub_records:
+        subs = {}
+        for cfg in SUB_CONFIGS:
+            if cfg == args.config:
+                continue
+            rec, _ = measure(cfg, args, dev, rank, world, local, warmup=args.warmup, region_s=0.5)
+            subs[cfg] = _brief(rec)
+        cfg, L = LAYERS_SUB
+        rec, identical = measure_layers(cfg, L, args, dev, rank, world, local)
+        ok = ok and identical
+        subs[f"layers{L}_{cfg}"] = _brief(rec)
+        line["sub_records"] = subs
+        line["gpu_launches_sub_records"] = sum(r["gpu_launches"] for r in subs.values())
     if rank == 0:
-        line = {
-            "metric": metric, "value": value, "unit": unit, "n_gpus": world, "steps": steps,
-            "warmup": max(3, args.warmup), "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
-            "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-            "config": {
-                "workload": f"{L} layers x {args.config}: {DESCRIPTIONS.get(args.config, '')}",
-                "layers": L, "kv_bytes_per_step": int(total_kv), "kv_chunk": plan["kv_chunk"],
-                "splits": plan["splits"], "l2": f"KV bytes per step {total_kv / 2**20:.0f} MiB "
-                                                 f"({'>' if total_kv > 3 * (128 << 20) else '<='} 3 x L2)",
-                "parallelism": f"dp{world}" if world > 1 else "single GPU",
-            },
-            "graph_modes_ms_per_step": times,
-            "launch_overhead_us_per_layer": {
-                k: (v - times["graph_full"]) * 1e3 / L for k, v in times.items() if k != "graph_full"},
-            "us_per_layer": ms * 1e3 / L,
-            "hbm_frac_step": (total_kv / world) / (ms / 1e3) / 1e9 / peaks["hbm"][0],
-            "graph_matches_eager": identical,
-            "gpu_launches": plan["launches"] * L * steps,
-            "clocks": sampler.summary(t0, t1),
-        }
         print(json.dumps(line))
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+    return 0 if ok else 1
+
+
+def run_layers(args):
+    """--layers L: the L-layer decoder step of --config as the JSON line."""
+    import torch
+    import paged_kv_cache_forward_gb300 as pa
+    from paged_kv_cache_forward_gb300 import build as build_mod
+
+    rank, world, local = dist_env()
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    build_mod.build()
+    pa.load()
+    rec, identical = measure_layers(args.config, args.layers, args, dev, rank, world, local, steps=args.steps or 50)
+    if rank == 0:
+        print(json.dumps(rec))
     if world > 1:
         import torch.distributed as dist
         dist.destroy_process_group()
