@@ -31,9 +31,11 @@ pa_status cuda_fail(cudaError_t e, const char* what) {
 }
 
 // ---------------------------------------------------------------- split table
-// Keys per split, picked from the context bound (max_pages * page_size) and the
-// number of sequences, as measured by the offline sweep (lut_gb300.inc).
+// Keys per split and decode kernel variant, picked from the head dim, the
+// context bound (max_pages * page_size) and the number of decode units, as
+// measured by the offline sweep (lut_gb300.inc).
 struct LutEntry {
+    int32_t head_dim;
     int32_t max_bound;  // applies when context bound <= max_bound
     int32_t max_units;  // ... and (sequences x KV heads x row groups) <= max_units
     int32_t kv_chunk;
@@ -46,13 +48,15 @@ struct LutEntry {
 constexpr int32_t kDefaultDecodeStages = 2, kDefaultDecodeWarps = 4;
 constexpr int32_t kMaxDecodeCluster = 16;  // largest thread-block cluster (non-portable size)
 
-// The key is the context bound and the number of independent (sequence, KV
-// head, row group) units: the decode grid is units x splits, so a shape with
-// the same units and bound needs the same split (an MQA batch of 8 behaves like
-// one Llama sequence with 8 KV heads).
-const LutEntry& table_entry(int64_t bound, int64_t units) {
+// The key is the head dim, the context bound and the number of independent
+// (sequence, KV head, row group) units: the decode grid is units x splits, so a
+// shape with the same units and bound needs the same split (an MQA batch of 8
+// behaves like one Llama sequence with 8 KV heads).  Every built head dim has
+// rows ending in a catch-all; a table without the head dim would fall back to
+// its last row.
+const LutEntry& table_entry(int32_t head_dim, int64_t bound, int64_t units) {
     for (const LutEntry& e : kSplitTable)
-        if (bound <= e.max_bound && units <= e.max_units) return e;
+        if (e.head_dim == head_dim && bound <= e.max_bound && units <= e.max_units) return e;
     return kSplitTable[sizeof(kSplitTable) / sizeof(kSplitTable[0]) - 1];
 }
 
@@ -97,8 +101,8 @@ pa_status make_plan(const pa_dims* d, const pa_options* o, Plan* p) {
     if (st != PA_OK) return st;
     const int64_t bound = static_cast<int64_t>(d->max_pages) * d->page_size;
     const int32_t group0 = d->num_q_heads / d->num_kv_heads;
-    const LutEntry& te =
-        table_entry(bound, static_cast<int64_t>(d->num_seqs) * d->num_kv_heads * ((group0 + 15) / 16));
+    const LutEntry& te = table_entry(d->head_dim, bound,
+                                     static_cast<int64_t>(d->num_seqs) * d->num_kv_heads * ((group0 + 15) / 16));
     int64_t chunk = (o && o->kv_chunk) ? o->kv_chunk : te.kv_chunk;
     if (chunk < d->page_size || chunk % d->page_size)
         return fail(PA_ERR_INVALID_ARG, "kv_chunk %lld must be a positive multiple of page_size",
@@ -106,10 +110,10 @@ pa_status make_plan(const pa_dims* d, const pa_options* o, Plan* p) {
     // the table's variant, unless the caller forces one (fully or in part)
     int32_t stages = te.decode_stages ? te.decode_stages : kDefaultDecodeStages;
     int32_t warps = te.decode_warps ? te.decode_warps : kDefaultDecodeWarps;
-    if (d->head_dim == 256 && !pa::decode_variant_supported(256, warps, stages)) {
-        // the table was swept at head_dim 128; the nearest variant built for 256
-        warps = 4;
-        stages = stages >= 3 ? 3 : 2;
+    if (!pa::decode_variant_supported(d->head_dim, warps, stages)) {
+        // (only a table without rows for this head dim gets here)
+        warps = kDefaultDecodeWarps;
+        stages = kDefaultDecodeStages;
     }
     if (o && (o->decode_stages || o->decode_warps)) {
         stages = o->decode_stages ? o->decode_stages : kDefaultDecodeStages;

@@ -3,13 +3,22 @@
 The Triton unified-attention page (section "What three things the IBM paper got
 right", third item) replaces run-time autotuning by offline micro-benchmarks
 distilled into a small decision tree keyed on GPU, sequence length and batch.
-This is that step for GB300: for every (context bound, batch size) cell of a
-grid it times pa_forward on Llama-3.1-8B-shaped decode batches (32 query heads,
-8 KV heads, head_dim 128; one sequence at the context bound, or a batch with
-lengths uniform in [bound/16, bound]) for a set of
-(split size, decode kernel variant) pairs -- a variant is the warps per CTA
-and the pipeline depth per warp -- and keeps the fastest.  The result is written as a table that the
-library compiles in; nothing is tuned at run time.
+This is that step for GB300: for every (head dim, batch size, context bound)
+cell of a grid it times pa_forward on decode batches (32 query heads, 8 KV
+heads; one sequence at the context bound, or a batch with lengths uniform in
+[bound/16, bound]) for a set of (split, decode kernel variant) candidates -- a
+split is a number of keys per CTA merged through the workspace, or a
+thread-block cluster of C CTAs that the sequence's pages are dealt to; a
+variant is the warps per CTA and the pipeline depth per warp -- and keeps the
+fastest.  Every candidate is timed once; the five fastest are timed twice more
+and the cell takes the best median of three.  The result is written as a table
+that the library compiles in; nothing is tuned at run time.
+
+The table is keyed on decode units (sequences x KV heads x row groups of 16
+query heads), not on the batch, so other head counts map onto the sweep by their
+parallelism; --validate-groups times, for a few cells with 1, 8 and 32 query
+heads per KV head, the table's pick against the best candidate and records the
+ratio in the log.
 
     python -m paged_kv_cache_forward_gb300.sweep [--out csrc/lut_gb300.inc] [--log profiles/...md]
 
@@ -25,6 +34,7 @@ import datetime
 import math
 import re
 import os
+import statistics
 import sys
 
 import torch
@@ -34,36 +44,44 @@ sys.path.insert(0, os.path.dirname(HERE))
 
 import paged_kv_cache_forward_gb300 as pa  # noqa: E402
 
+DIMS = [128, 64, 256]
 BOUNDS = [1024, 2048, 4096, 8192, 16384, 32768, 65536, 131072]
-BATCHES = [1, 2, 4, 8, 16, 32, 64, 128, 256]
-HQ, HKV, D, PAGE = 32, 8, 128, 16
+BATCHES = {128: [1, 2, 4, 8, 16, 32, 64, 128, 256], 64: [1, 4, 16, 64, 256], 256: [1, 4, 16, 64, 256]}
+HQ, HKV, PAGE = 32, 8, 16
 MAX_KV_BYTES = 6 << 30
-
+TOP = 5          # candidates re-timed after the first pass
+REPEATS = 3      # timings per re-timed candidate (the cell takes the best median)
+MIN_MS = 20.0    # graph replays per timing: at least this long, and at least 3
 
 SMEM_PER_SM = 228 << 10
 REGS_PER_SM = 65536
 REGS_PER_THREAD = 168
-VARIANTS = "4x2,4x3,4x4,8x2,8x3,12x2"  # warps x stages
+VARIANTS = {64: "4x2,4x3,4x4,8x2,8x3,12x2", 128: "4x2,4x3,4x4,8x2,8x3,12x2", 256: "4x2,4x3"}
+CLUSTERS = "2,4,8,12,16"
+GROUP_CELLS = [(1, 2048), (1, 8192), (1, 32768), (8, 8192), (64, 4096)]  # (batch, bound) for --validate-groups
+GROUP_SHAPES = [(8, 8), (64, 8), (32, 1)]  # (Hq, Hkv): 1, 8 and 32 query heads per KV head
 
 
-def resident_ctas(warps: int, stages: int) -> int:
+def resident_ctas(warps: int, stages: int, d: int) -> int:
     """Decode CTAs an SM holds: shared memory (K and V of one page per stage per
     warp, 1 KiB reserved per CTA) and registers (at most 168 per thread)."""
-    per_cta = warps * stages * 2 * PAGE * D * 2 + 1024
+    per_cta = warps * stages * 2 * PAGE * d * 2 + 1024
     return max(1, min(SMEM_PER_SM // per_cta, REGS_PER_SM // (warps * 32 * REGS_PER_THREAD)))
 
 
-def candidates(bound: int, batch: int, sms: int, warps: int, stages: int):
+def candidates(bound: int, units: int, sms: int, warps: int, stages: int, d: int):
+    """Split sizes: powers of two, and those that give whole waves of CTAs at this
+    variant's residency."""
     base = {64, 128, 256, 512, 1024, 2048, 4096, 8192, 16384}
-    # split sizes that give whole waves of CTAs at this variant's residency
-    per_sm = resident_ctas(warps, stages)
+    per_sm = resident_ctas(warps, stages, d)
     for k in (1, 2, 3):
-        pages = math.ceil(bound * batch * HKV / (k * per_sm * sms) / PAGE)
+        pages = math.ceil(bound * units / (k * per_sm * sms) / PAGE)
         base.add(max(1, pages) * PAGE)
     return sorted(c for c in base if 16 <= c <= bound)
 
 
-def time_shape(bound, batch, chunk, pools, stream, warps=0, stages=0, cluster=0, steps_per_graph=16, reps=30):
+def time_shape(pools, stream, chunk=0, warps=0, stages=0, cluster=0, steps_per_graph=16):
+    """Microseconds per pa_forward step, from graph replays on `stream`."""
     q, ks, vs, bt, sl, qsl, out = pools
     R = len(ks)
     pa.prepare(q, ks[0], bt, sl, kv_chunk=chunk, stream=stream, decode_stages=stages,
@@ -79,9 +97,14 @@ def time_shape(bound, batch, chunk, pools, stream, warps=0, stages=0, cluster=0,
         for i in range(M):
             pa.forward(q, ks[i % R], vs[i % R], bt, sl, qsl, out, kv_chunk=chunk, stream=stream,
                        decode_stages=stages, decode_warps=warps, decode_cluster=cluster)
-    for _ in range(3):
-        g.replay()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):  # a graph replays on the current stream
+        g.replay()
+        e0.record()
+        g.replay()
+        e1.record()
+    stream.synchronize()
+    reps = max(3, int(math.ceil(MIN_MS / max(e0.elapsed_time(e1), 1e-3))))
     with torch.cuda.stream(stream):
         e0.record()
         for _ in range(reps):
@@ -90,9 +113,9 @@ def time_shape(bound, batch, chunk, pools, stream, warps=0, stages=0, cluster=0,
     stream.synchronize()
     code = pa.device_error(stream)
     if code:
-        raise RuntimeError(f"device error {code} ({pa.DEVICE_ERRORS.get(code)}) at bound {bound}, batch {batch}, "
-                           f"split {chunk}, variant {warps}x{stages}, cluster {cluster}")
-    return e0.elapsed_time(e1) * 1e3 / (reps * M)  # us per step
+        raise RuntimeError(f"device error {code} ({pa.DEVICE_ERRORS.get(code)}) at split {chunk}, "
+                           f"variant {warps}x{stages}, cluster {cluster}")
+    return e0.elapsed_time(e1) * 1e3 / (reps * M)
 
 
 def seq_lengths(bound, batch):
@@ -106,24 +129,91 @@ def seq_lengths(bound, batch):
     return torch.randint(lo, bound + 1, (batch,), generator=g).tolist()
 
 
-def make_pools(bound, batch, l2_bytes, gen):
+def make_pools(bound, batch, d, hq, hkv, l2_bytes, gen):
     pages = bound // PAGE
     lens = seq_lengths(bound, batch)
-    kv = sum(lens) * HKV * D * 2 * 2
+    kv = sum(lens) * hkv * d * 2 * 2
     R = 1 if kv > 3 * l2_bytes else int(math.ceil(3 * l2_bytes / kv)) + 1
     nb = batch * pages + 1
     dev = "cuda"
-    q = torch.randn(batch, HQ, D, device=dev, generator=gen).to(torch.bfloat16)
+    q = torch.randn(batch, hq, d, device=dev, generator=gen).to(torch.bfloat16)
     ks, vs = [], []
     for _ in range(R):
-        ks.append(torch.randn(nb, PAGE, HKV, D, device=dev, generator=gen).to(torch.bfloat16))
-        vs.append(torch.randn(nb, PAGE, HKV, D, device=dev, generator=gen).to(torch.bfloat16))
+        ks.append(torch.randn(nb, PAGE, hkv, d, device=dev, generator=gen).to(torch.bfloat16))
+        vs.append(torch.randn(nb, PAGE, hkv, d, device=dev, generator=gen).to(torch.bfloat16))
     perm = torch.randperm(nb, device=dev, generator=gen).to(torch.int32)
     bt = perm[: batch * pages].reshape(batch, pages).contiguous()
     sl = torch.tensor(lens, dtype=torch.int32, device=dev)
     qsl = torch.arange(batch + 1, dtype=torch.int32, device=dev)
     out = torch.empty_like(q)
+    torch.cuda.synchronize()  # filled on the default stream; timing runs on another
     return (q, ks, vs, bt, sl, qsl, out), kv
+
+
+def all_candidates(bound, units, sms, d, variants, clusters):
+    """(split keys, stages, warps, cluster) for every variant: static splits of the
+    given keys (cluster 1), and clusters of C CTAs (split 0)."""
+    out = []
+    for w, st in variants:
+        out += [(c, st, w, 1) for c in candidates(bound, units, sms, w, st, d)]
+        out += [(0, st, w, c) for c in clusters]
+    return out
+
+
+def sweep_cell(pools, stream, cands):
+    """Every candidate once, the TOP fastest REPEATS times in all; returns
+    [(median us, cand, [timings])] sorted, with the unrepeated ones after."""
+    first = []
+    for cand in cands:
+        chunk, st, w, cl = cand
+        try:
+            us = time_shape(pools, stream, chunk=chunk, warps=w, stages=st, cluster=cl)
+        except RuntimeError as e:  # reported, and the candidate is not used
+            print(f"skipped: {e}", flush=True)
+            continue
+        first.append((us, cand))
+    first.sort()
+    res = []
+    for us, cand in first[:TOP]:
+        chunk, st, w, cl = cand
+        ts = [us] + [time_shape(pools, stream, chunk=chunk, warps=w, stages=st, cluster=cl)
+                     for _ in range(REPEATS - 1)]
+        res.append((statistics.median(ts), cand, ts))
+    res.sort()
+    return res + [(us, cand, [us]) for us, cand in first[TOP:]]
+
+
+def name_of(chunk, cl):
+    return f"c{cl}" if cl > 1 else f"{chunk}"
+
+
+def validate_groups(args, sms, l2, stream, gen, lines):
+    """The table's pick against the best candidate for other group sizes."""
+    lines.append("")
+    lines.append("## Other group sizes (head_dim 128): the table's pick (keyed on decode units) against the best "
+                 "candidate")
+    lines.append("")
+    lines.append("| Hq / Hkv | batch | bound | table pick | us | best | us | pick / best |")
+    lines.append("|---|---|---|---|---|---|---|---|")
+    variants = [tuple(int(y) for y in v.split("x")) for v in VARIANTS[128].split(",")]
+    clusters = [int(c) for c in args.clusters.split(",") if c]
+    for hq, hkv in GROUP_SHAPES:
+        for batch, bound in GROUP_CELLS:
+            pools, kv = make_pools(bound, batch, 128, hq, hkv, l2, gen)
+            p = pa.plan_for(pools[0], pools[1][0], pools[3], pools[4])
+            cl = p["decode_cluster"]
+            pick = (0 if cl > 1 else p["kv_chunk"], p["decode_stages"], p["decode_warps"], cl)
+            t_pick = statistics.median(
+                time_shape(pools, stream, chunk=pick[0], warps=pick[2], stages=pick[1], cluster=pick[3])
+                for _ in range(REPEATS))
+            units = batch * hkv * ((hq // hkv + 15) // 16)
+            res = sweep_cell(pools, stream, all_candidates(bound, units, sms, 128, variants, clusters))
+            us, (chunk, st, w, c2), _ = res[0]
+            lines.append(f"| {hq} / {hkv} | {batch} | {bound} | {name_of(pick[0], pick[3])} {pick[2]}x{pick[1]} | "
+                         f"{t_pick:.1f} | {name_of(chunk, c2)} {w}x{st} | {us:.1f} | {t_pick / us:.3f} |")
+            print(lines[-1], flush=True)
+            del pools
+            torch.cuda.empty_cache()
 
 
 def main(argv=None):
@@ -131,16 +221,19 @@ def main(argv=None):
     ap.add_argument("--out", default=os.path.join(HERE, "csrc", "lut_gb300.inc"))
     ap.add_argument("--no-write", action="store_true", help="print the results only")
     ap.add_argument("--log", default=os.path.join(os.path.dirname(HERE), "profiles", "split_table_sweep__gb300.md"))
+    ap.add_argument("--dims", default=",".join(map(str, DIMS)))
     ap.add_argument("--bounds", default=",".join(map(str, BOUNDS)))
-    ap.add_argument("--batches", default=",".join(map(str, BATCHES)))
-    ap.add_argument("--variants", default=VARIANTS, help="decode variants to try: warps x stages")
-    ap.add_argument("--clusters", default="2,4,8,16", help="cluster sizes to try (pages dealt round-robin, merge in DSMEM)")
+    ap.add_argument("--batches", default="", help="batch sizes (default: per head dim)")
+    ap.add_argument("--variants", default="", help="decode variants to try: warps x stages (default: per head dim)")
+    ap.add_argument("--clusters", default=CLUSTERS, help="cluster sizes to try (pages dealt round-robin, merge in DSMEM)")
+    ap.add_argument("--validate-groups", action="store_true",
+                    help="instead of sweeping: time the built table's pick against the best candidate for 1, 8 and "
+                         "32 query heads per KV head, and write that to --log")
     ap.add_argument("--merge", action="store_true",
-                    help="replace only the swept (bound, batch) cells of the existing table and log")
+                    help="replace only the swept cells of the existing table and log")
     args = ap.parse_args(argv)
+    dims = [int(x) for x in args.dims.split(",") if x]
     bounds = [int(x) for x in args.bounds.split(",")]
-    batches = [int(x) for x in args.batches.split(",")]
-    variants = [tuple(int(y) for y in v.split("x")) for v in args.variants.split(",")]
     clusters = [int(c) for c in args.clusters.split(",") if c]
 
     from paged_kv_cache_forward_gb300 import build
@@ -151,112 +244,117 @@ def main(argv=None):
     l2 = getattr(props, "L2_cache_size", 128 << 20)
     stream = torch.cuda.Stream()
     gen = torch.Generator(device="cuda").manual_seed(0)
+    if args.validate_groups:
+        extra = [f"# Split table check for other group sizes on {props.name} ({datetime.date.today().isoformat()})",
+                 "", f"Command: `python -m paged_kv_cache_forward_gb300.sweep {' '.join(argv or sys.argv[1:])}`"]
+        validate_groups(args, sms, l2, stream, gen, extra)
+        with open(args.log, "w") as f:
+            f.write("\n".join(extra) + "\n")
+        print(f"wrote {args.log}")
+        return
     best = {}
-    lines = []
-    for batch in batches:
-        for bound in bounds:
-            if batch * bound * HKV * D * 4 > MAX_KV_BYTES:
-                continue
-            pools, kv = make_pools(bound, batch, l2, gen)
-            # the pools were filled on the default stream; the timing runs on
-            # `stream`, which does not order itself after it
-            torch.cuda.synchronize()
-            res = []
-            for w, st in variants:
-                # (split size, 1): splits merged through the workspace;
-                # (0, C): the pages dealt round-robin to a cluster of C CTAs
-                cands = [(c, 1) for c in candidates(bound, batch, sms, w, st)] + [(0, c) for c in clusters]
-                for chunk, cl in cands:
-                    try:
-                        us = time_shape(bound, batch, chunk, pools, stream, warps=w, stages=st, cluster=cl)
-                    except RuntimeError as e:  # reported, and the candidate is not used
-                        print(f"skipped: {e}", flush=True)
-                        continue
-                    res.append((us, chunk, st, w, cl))
-            res.sort()
-            us, chunk, st, w, cl = res[0]
-            best[(bound, batch)] = (chunk, st, w, cl)
-            name = lambda c, cl: f"c{cl}" if cl > 1 else f"{c}"
-            row = " ".join(f"{name(c, k)}/{ww}x{t}:{kv / u / 1e3:.0f}"
-                           for u, c, t, ww, k in sorted(res, key=lambda x: (x[3], x[2], x[4], x[1])))
-            lines.append(f"| {batch} | {bound} | {name(chunk, cl)} | {w}x{st} | {us:.1f} | {kv / us / 1e3:.0f} | {row} |")
-            print(lines[-1], flush=True)
-            del pools
-            torch.cuda.empty_cache()
+    lines = {}
+    for d in dims:
+        batches = [int(x) for x in args.batches.split(",")] if args.batches else BATCHES[d]
+        variants = [tuple(int(y) for y in v.split("x")) for v in (args.variants or VARIANTS[d]).split(",")]
+        variants = [v for v in variants if d != 256 or v[0] == 4]
+        for batch in batches:
+            for bound in bounds:
+                if batch * bound * HKV * d * 4 > MAX_KV_BYTES:
+                    continue
+                pools, kv = make_pools(bound, batch, d, HQ, HKV, l2, gen)
+                units = batch * HKV
+                res = sweep_cell(pools, stream, all_candidates(bound, units, sms, d, variants, clusters))
+                us, (chunk, st, w, cl), ts = res[0]
+                best[(d, bound, batch)] = (chunk, st, w, cl)
+                row = " ".join(f"{name_of(c, k)}/{ww}x{t}:{kv / u / 1e3:.0f}" + ("*" if len(tsx) > 1 else "")
+                               for u, (c, t, ww, k), tsx in sorted(res, key=lambda x: (x[1][2], x[1][1], x[1][3],
+                                                                                      x[1][0])))
+                spread = f"{min(ts):.1f}-{max(ts):.1f}"
+                lines[(d, batch, bound)] = (f"| {d} | {batch} | {bound} | {name_of(chunk, cl)} | {w}x{st} | "
+                                            f"{us:.1f} ({spread}) | {kv / us / 1e3:.0f} | {row} |")
+                print(lines[(d, batch, bound)], flush=True)
+                del pools
+                torch.cuda.empty_cache()
 
-    # table: (max_bound, max_units) cells, batch-major, so the first match is the
-    # smallest swept batch >= B and, within it, the smallest swept bound >= bound;
-    # units = sequences x KV heads (x row groups), so other head counts map onto
-    # the Llama-shaped sweep by their parallelism
     if args.merge:
         cells, old_lines = read_table(args.out), read_log(args.log)
         cells.update(best)
-        for line in lines:
-            old_lines[tuple(int(x) for x in line.split("|")[1:3])] = line
-        best = cells
-        batches = sorted({k[1] for k in best})
-        bounds = sorted({k[0] for k in best})
-        lines = [old_lines[(bt, bd)] for bt in batches for bd in bounds if (bt, bd) in old_lines]
-    entries = []
-    for batch in batches:
-        for bound in bounds:
-            if (bound, batch) in best:
-                entries.append((bound, batch) + best[(bound, batch)])
-    last_batch = max(e[1] for e in entries)
-    fallback = max(entries, key=lambda e: (e[1], e[0]))[2:]
+        old_lines.update(lines)
+        best, lines = cells, old_lines
     stamp = datetime.date.today().isoformat()
     if not args.no_write:
-        write_table(args.out, entries, last_batch, fallback, props.name, stamp)
+        write_table(args.out, best, props.name, stamp)
     with open(args.log, "w") as f:
         f.write(f"# Split-size sweep on {props.name} ({stamp})\n\n"
                 f"Command: `python -m paged_kv_cache_forward_gb300.sweep {' '.join(argv or sys.argv[1:])}`\n\n"
-                "Llama-3.1-8B-shaped decode (Hq 32, Hkv 8, D 128); batch 1 at the bound, larger batches\n"
+                "Decode batches with 32 query heads and 8 KV heads; batch 1 at the bound, larger batches\n"
                 "with lengths uniform in [bound/16, bound] (seeded per cell),\n"
                 "graph-replayed pa_forward steps rotating over KV pool copies larger than 3 x L2.\n"
-                "GB/s = KV bytes per step / step time.\n\n"
+                "GB/s = KV bytes per step / step time.  Every candidate is timed once; the five fastest\n"
+                f"(marked *) {REPEATS} times, and the cell keeps the best median (its spread in brackets).\n\n"
                 "Split `cN`: the pages dealt round-robin to a thread-block cluster of N CTAs.\n\n"
-                "| batch | bound | best split | warps x stages | us/step | GB/s | split/variant:GB/s for every candidate |\n"
-                "|---|---|---|---|---|---|---|\n")
-        f.write("\n".join(lines) + "\n")
+                "| head_dim | batch | bound | best split | warps x stages | us/step | GB/s | "
+                "split/variant:GB/s for every candidate |\n"
+                "|---|---|---|---|---|---|---|---|\n")
+        f.write("\n".join(lines[k] for k in sorted(lines)) + "\n")
     print(f"wrote {args.log}" + ("" if args.no_write else f" and {args.out}"))
 
 
 def read_table(path):
-    """The cells of an existing table: {(bound, batch): (chunk, stages, warps, cluster)}
-    (the last batch's cells carry max_units 1 << 30; the fallback row is dropped)."""
+    """The cells of an existing table: {(head_dim, bound, batch): (chunk, stages, warps, cluster)}
+    (the catch-all rows are dropped)."""
     cells = {}
-    rows = re.findall(r"\{(\d+), (\d+|1 << 30), (\d+), (\d+), (\d+), (\d+)\}", open(path).read())
-    for bound, units, chunk, st, w, cl in rows:
-        batch = max(BATCHES) if units == "1 << 30" or int(units) >= 1 << 30 else int(units) // HKV
-        cells[(int(bound), batch)] = (int(chunk), int(st), int(w), int(cl))
+    rows = re.findall(r"\{(\d+), (\d+), (\d+), (\d+), (\d+), (\d+), (\d+)\}", open(path).read())
+    for d, bound, units, chunk, st, w, cl in rows:
+        d, units = int(d), int(units)
+        if units >= 1 << 30 or int(bound) >= 1 << 30:
+            continue
+        cells[(d, int(bound), units // HKV)] = (int(chunk), int(st), int(w), int(cl))
     return cells
 
 
 def read_log(path):
-    """The rows of an existing sweep log: {(batch, bound): line}."""
+    """The rows of an existing sweep log: {(head_dim, batch, bound): line}."""
     out = {}
     if os.path.exists(path):
         for line in open(path):
-            m = re.match(r"\| (\d+) \| (\d+) \|", line)
+            m = re.match(r"\| (\d+) \| (\d+) \| (\d+) \|", line)
             if m:
-                out[(int(m.group(1)), int(m.group(2)))] = line.rstrip("\n")
+                out[(int(m.group(1)), int(m.group(2)), int(m.group(3)))] = line.rstrip("\n")
     return out
 
 
-def write_table(path, entries, last_batch, fallback, gpu_name, stamp):
+def write_table(path, best, gpu_name, stamp):
+    """Rows {head_dim, max_bound, max_units, ...}: per head dim, batch-major, so the
+    first match is the smallest swept batch (in decode units) >= the call's and,
+    within it, the smallest swept bound >= the call's.  Each head dim ends with
+    catch-all rows: its largest batch's cells for any number of units, and that
+    batch's largest bound for any bound."""
     with open(path, "w") as f:
-        f.write("// Keys per split and decode kernel variant, keyed on the context bound\n"
-                "// (max_pages * page_size) and the number of decode units:\n"
-                "// {max_bound, max_units, kv_chunk, decode_stages, decode_warps, decode_cluster}\n"
-                "// (units = sequences x KV heads x row groups)\n"
+        f.write("// Keys per split and decode kernel variant, keyed on the head dim, the\n"
+                "// context bound (max_pages * page_size) and the number of decode units:\n"
+                "// {head_dim, max_bound, max_units, kv_chunk, decode_stages, decode_warps, decode_cluster}\n"
+                "// (units = sequences x KV heads x row groups of 16 query heads)\n"
                 "// (cluster > 1: the pages dealt round-robin to a cluster of that many CTAs).  The first\n"
-                "// entry that matches wins; the last entry is the fallback.  Written by\n"
-                f"// paged_kv_cache_forward_gb300/sweep.py on {gpu_name} ({stamp}).\n"
+                "// entry that matches wins.  Written by paged_kv_cache_forward_gb300/sweep.py on\n"
+                f"// {gpu_name} ({stamp}).\n"
                 "static const LutEntry kSplitTable[] = {\n")
-        for bound, batch, chunk, st, w, cl in entries:
-            mb = (1 << 30) if batch == last_batch else batch * HKV
-            f.write(f"    {{{bound}, {mb}, {chunk or 16}, {st}, {w}, {cl}}},\n")
-        f.write(f"    {{1 << 30, 1 << 30, {fallback[0] or 16}, {fallback[1]}, {fallback[2]}, {fallback[3]}}},\n}};\n")
+        for d in sorted({k[0] for k in best}):
+            cells = {k[1:]: v for k, v in best.items() if k[0] == d}
+            batches = sorted({b for _, b in cells})
+            bounds = sorted({bd for bd, _ in cells})
+            row = lambda bound, units, c: f"    {{{d}, {bound}, {units}, {c[0] or 16}, {c[1]}, {c[2]}, {c[3]}}},\n"
+            for batch in batches:
+                for bound in bounds:
+                    if (bound, batch) in cells:
+                        f.write(row(bound, batch * HKV, cells[(bound, batch)]))
+            top = batches[-1]
+            for bound in bounds:
+                if (bound, top) in cells:
+                    f.write(row(bound, "1 << 30", cells[(bound, top)]))
+            f.write(row("1 << 30", "1 << 30", cells[max(b for b, bt in cells if bt == top), top]))
+        f.write("};\n")
 
 
 if __name__ == "__main__":

@@ -15,31 +15,30 @@ def _rows(path):
     return [line for line in open(path) if line.startswith("    {")]
 
 
-def _write(cells, path):
-    batches = sorted({k[1] for k in cells})
-    bounds = sorted({k[0] for k in cells})
-    entries = [(bd, bt) + cells[(bd, bt)] for bt in batches for bd in bounds if (bd, bt) in cells]
-    fallback = max(entries, key=lambda e: (e[1], e[0]))[2:]
-    S.write_table(path, entries, max(batches), fallback, "test", "today")
-
-
 def test_table_round_trip():
     cells = S.read_table(TABLE)
-    assert cells and max(k[1] for k in cells) == max(S.BATCHES)
+    assert cells and {k[0] for k in cells} == {64, 128, 256}
     with tempfile.TemporaryDirectory() as d:
         out = os.path.join(d, "t.inc")
-        _write(cells, out)
+        S.write_table(out, cells, "test", "today")
         assert _rows(out) == _rows(TABLE)
+
+
+def test_every_head_dim_ends_with_a_catch_all():
+    rows = [r.strip() for r in _rows(TABLE)]
+    for d in (64, 128, 256):
+        mine = [r for r in rows if r.startswith(f"{{{d}, ")]
+        assert mine[-1].startswith(f"{{{d}, 1 << 30, 1 << 30, ")
 
 
 def test_merge_replaces_one_cell():
     cells = S.read_table(TABLE)
-    key = (4096, 1)
+    key = (128, 4096, 1)
     merged = dict(cells)
-    merged.update({key: (0, 2, 8, 8)})
+    merged[key] = (0, 2, 8, 12)
     with tempfile.TemporaryDirectory() as d:
         out = os.path.join(d, "t.inc")
-        _write(merged, out)
+        S.write_table(out, merged, "test", "today")
         a, b = _rows(TABLE), _rows(out)
         diff = [(x, y) for x, y in zip(a, b) if x != y]
-        assert len(a) == len(b) and len(diff) == 1 and diff[0][1].strip() == "{4096, 8, 16, 2, 8, 8},"
+        assert len(a) == len(b) and len(diff) == 1 and diff[0][1].strip() == "{128, 4096, 8, 16, 2, 8, 12},"
