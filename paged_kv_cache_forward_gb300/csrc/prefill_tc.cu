@@ -59,14 +59,7 @@
 namespace pa {
 namespace {
 
-constexpr int kThreads = 384;
 constexpr int kWarpV = 2;  // the V producer
-// Registers per thread after the split: warpgroup 0 (producers, MMA issuer)
-// gives registers to the two softmax warpgroups, whose whole S row (128 fp32)
-// stays in registers.  384 threads launch with 168 each (64512);
-// 128 x 104 + 256 x 200 = 64512.  The launcher checks the launch count.
-constexpr uint32_t kRegsLaunch = 168, kRegsIssue = 104, kRegsSoftmax = 200;
-static_assert(128 * kRegsIssue + 256 * kRegsSoftmax <= kThreads * kRegsLaunch, "register split above the launch");
 constexpr int kM = 128;            // rows per tile
 constexpr int kKeys = 128;         // keys per KV tile
 constexpr int kPage = 16;
@@ -77,16 +70,32 @@ constexpr uint32_t kTmemCols = 512;
 // TMEM columns of tile x: S at 128 x (P over its last 64 columns), O at 256 + 128 x.
 __device__ __forceinline__ uint32_t tmem_s(int x) { return x ? 128u : 0u; }
 __device__ __forceinline__ uint32_t tmem_o(int x) { return x ? 384u : 256u; }
-// Query tiles per CTA and ring depths.  At D <= 128 a CTA holds a pair of tiles
-// (S and O of both in the 512 TMEM columns) with a 3-stage K and a 2-stage V
-// ring; at D = 256 one tile's O alone takes 256 columns, so a CTA holds one tile,
-// and a 64 KiB K or V tile leaves room for single-stage rings (K(j+1) loads
-// during the softmax and P V of tile j, V(j+1) during S(j+1) and its softmax).
+// Query tiles per CTA, ring depths, softmax warps and registers.
+//  * D <= 128: a pair of query tiles per CTA (S and O of both in the 512 TMEM
+//    columns), 2-stage K and V rings, and two softmax warps per TMEM lane
+//    quarter of each tile, each taking 64 of the tile's 128 key columns (the
+//    row max is exchanged through shared memory).  640 threads launch with 96
+//    registers each; each softmax warp holds 64 S values within those, and
+//    warpgroup 0 (producers, MMA issuer) drops to 88.
+//  * D = 256: one tile's O alone takes 256 columns, so a CTA holds one tile, with
+//    single-stage 64 KiB K and V rings (K(j+1) loads during the softmax and P V
+//    of tile j, V(j+1) during S(j+1) and its softmax) and one softmax warp per
+//    lane quarter holding the whole 128-column S row: 384 threads at 168
+//    registers, 128 x 104 + 256 x 200 = 384 x 168 (warps 8-11 idle).
+// The launcher checks the launch register count, so a split that does not fit
+// is an error, not a wait in setmaxnreg.
 template <int D>
 struct Cfg {
     static constexpr int kTiles = D <= 128 ? 2 : 1;
-    static constexpr int kKStages = D <= 128 ? 3 : 1;
+    static constexpr int kKStages = D <= 128 ? 2 : 1;
     static constexpr int kVStages = D <= 128 ? 2 : 1;
+    static constexpr int kColSplit = D <= 128 ? 2 : 1;  // softmax warps per lane quarter of a tile
+    static constexpr int kThreads = D <= 128 ? 640 : 384;
+    static constexpr uint32_t kRegsLaunch = D <= 128 ? 96 : 168;
+    static constexpr uint32_t kRegsIssue = D <= 128 ? 88 : 104;
+    static constexpr uint32_t kRegsSoftmax = D <= 128 ? 96 : 200;
+    static_assert(128 * kRegsIssue + (kThreads - 128) * kRegsSoftmax <= kThreads * kRegsLaunch,
+                  "register split above the launch");
 };
 constexpr int kMaxKStages = 3, kMaxVStages = 2;  // barrier slots
 constexpr int kTilesPerGroup = 4;  // block-table prefetch: 4 tiles x 8 pages = one entry per lane
@@ -107,7 +116,11 @@ struct Smem {
     static constexpr int kNumBars = 23;
     static constexpr int kMisc = kBar + kNumBars * 8;  // tmem address, abort flag
     static constexpr int kItems = kMisc + 32;          // 2-slot item ring, 32 bytes a slot
-    static constexpr int kBytes = kItems + 64;
+    // row-max exchange of the two softmax warps of a lane quarter: [2 buffers]
+    // [2 tiles][2 halves][128 rows] fp32, then the final l: [2 tiles][2 halves][128]
+    static constexpr int kXMax = kItems + 64;
+    static constexpr int kXL = kXMax + (Cfg<D>::kColSplit > 1 ? 2 * 2 * 2 * 128 * 4 : 0);
+    static constexpr int kBytes = kXL + (Cfg<D>::kColSplit > 1 ? 2 * 2 * 128 * 4 : 0);
     static constexpr int kAlloc = kBytes + 1024;  // slack to align the base to 1024
     static_assert(kAlloc <= 227 * 1024, "shared memory above the per-CTA limit");
 };
@@ -120,7 +133,7 @@ enum Bar {
     kVFull0 = 7,    // [kMaxVStages = 2]
     kVEmpty0 = 9,   // [2]
     kSFull0 = 11,   // [2] per tile: S(j) in TMEM
-    kPFull0 = 13,   // [2] per tile: P(j) in TMEM (its 4 softmax warps arrive)
+    kPFull0 = 13,   // [2] per tile: P(j) in TMEM (every softmax warp of the tile arrives)
     kODone0 = 15,   // [2] per tile: the tile's last O += P V of an item done
     kDrain = 17,
     kQEmpty = 18,      // the item's last S MMA has read Q
@@ -316,11 +329,15 @@ __device__ __forceinline__ ItemShape shape_of(const Item& it, int tq_tokens, int
 // and barrier positions run on across items, so the next item's Q, K and first
 // S MMAs proceed while the softmax warps still finish the previous one.
 template <int D>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(Cfg<D>::kThreads, 1)
     prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                       const __grid_constant__ CUtensorMap tm_v, const Args a, int tq_tokens) {
     using S = Smem<D>;
     constexpr int kTiles = Cfg<D>::kTiles, kKStages = Cfg<D>::kKStages, kVStages = Cfg<D>::kVStages;
+    constexpr int kColSplit = Cfg<D>::kColSplit;
+    constexpr uint32_t kRegsIssue = Cfg<D>::kRegsIssue, kRegsSoftmax = Cfg<D>::kRegsSoftmax;
+    // setmaxnreg only where a budget differs from the launch's
+    constexpr bool kDecRegs = kRegsIssue < Cfg<D>::kRegsLaunch, kIncRegs = kRegsSoftmax > Cfg<D>::kRegsLaunch;
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = smem_u32(smem_raw);
     const uint32_t base = (raw + 1023u) & ~1023u;
@@ -348,11 +365,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         for (int x = 0; x < 2; ++x) {
             tc::mbar_init(bar(kSFull0 + x), 1);
-            tc::mbar_init(bar(kPFull0 + x), 4);
+            tc::mbar_init(bar(kPFull0 + x), 4 * kColSplit);
             tc::mbar_init(bar(kODone0 + x), 1);
             tc::mbar_init(bar(kItemFull0 + x), 1);
             // readers of an item: the MMA thread, the V producer, the softmax warps
-            tc::mbar_init(bar(kItemEmpty0 + x), 2 + 4 * kTiles);
+            tc::mbar_init(bar(kItemEmpty0 + x), 2 + 4 * kTiles * kColSplit);
         }
         tc::mbar_init(bar(kDrain), 1);
         *s_abort = 0;
@@ -369,7 +386,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     bool ok = true;
 
     if (warp == 0 || warp == kWarpV) {
-        reg_dec<kRegsIssue>();
+        if constexpr (kDecRegs) reg_dec<kRegsIssue>();
         // ===================== scheduler + Q and K producer (warp 0), V producer (warp 2)
         const bool is_v = warp == kWarpV;
         if (lane == 0) {
@@ -526,7 +543,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
     } else if (warp == 1) {
         // ===================================================== MMA issuer
-        reg_dec<kRegsIssue>();
+        if constexpr (kDecRegs) reg_dec<kRegsIssue>();
         if (lane == 0) {
             constexpr uint32_t kIdQK = tc::idesc_bf16_f32(kM, kKeys, false, false);
             constexpr uint32_t kIdPV = tc::idesc_bf16_f32(kM, D, false, true);
@@ -620,20 +637,59 @@ __global__ void __launch_bounds__(kThreads, 1)
             tc::mbar_wait(bar(kDrain), 0, nullptr, kTimeoutNs);
         }
         __syncwarp();
-    } else if (warp >= 4 && warp < 4 + 4 * kTiles) {
+    } else if (warp >= 4 && warp < 4 + 4 * kTiles * kColSplit) {
         // ======================================================== softmax
-        reg_inc<kRegsSoftmax>();
-        const int x = (warp - 4) >> 2;        // tile: warps 4-7 -> A, 8-11 -> B
-        const int quarter = warp & 3;         // TMEM lanes 32 * (warp % 4) ..
-        const int r = quarter * 32 + lane;    // row == TMEM lane
+        // Warp 4 + 4 t + q (t = tile, q = TMEM lane quarter) takes the tile's S
+        // columns [0, kCols) and, with the column split, warp 4 + 8 + 4 t + q
+        // takes [kCols, 128) of the same 32 rows; the two exchange their row
+        // maxima (and at the end their sums l) through shared memory.
+        if constexpr (kIncRegs) reg_inc<kRegsSoftmax>();
+        constexpr int kCols = kKeys / kColSplit;  // S columns of this warp
+        constexpr int kOCols = D / kColSplit;     // O columns this warp rescales and writes
+        const int sw = warp - 4;
+        const int x = (sw >> 2) & (kTiles - 1);   // tile: A or B
+        const int half = sw >> 3;                 // column half (0 without the split)
+        const int quarter = warp & 3;             // TMEM lanes 32 * (warp % 4) ..
+        const int r = quarter * 32 + lane;        // row == TMEM lane
         const uint32_t lane_addr = tmem + (static_cast<uint32_t>(quarter * 32) << 16);
         const uint32_t s_addr = lane_addr + tmem_s(x);
-        const uint32_t o_addr = lane_addr + tmem_o(x);
+        const uint32_t my_s = s_addr + half * kCols;
+        const uint32_t my_p = s_addr + 64 + half * (kCols / 2);  // key k -> column 64 + k / 2
+        const uint32_t o_addr = lane_addr + tmem_o(x) + half * kOCols;
+        float* const xmax = reinterpret_cast<float*>(sp + S::kXMax);  // [buf][tile][half][row]
+        float* const xl = reinterpret_cast<float*>(sp + S::kXL);      // [tile][half][row]
+        // The pair meets at a named barrier (1 + tile * 4 + quarter; 0 is
+        // __syncthreads) after each of its bounded mbarrier waits, with a
+        // reduction of the two warps' wait results: both continue, or both
+        // leave (on a timeout or an abort seen by either), so neither can be
+        // left waiting at the barrier for a partner that has gone.  The barrier
+        // also publishes the values each warp wrote to shared memory before it.
+        const int pair_bar = 1 + x * 4 + quarter;
+        auto pair_and = [&](bool v) -> bool {
+            if constexpr (kColSplit > 1) {
+                uint32_t both;
+                tc::tc_fence_before();
+                asm volatile(
+                    "{\n"
+                    ".reg .pred p, q;\n"
+                    "setp.ne.u32 p, %1, 0;\n"
+                    "bar.red.and.pred q, %2, 64, p;\n"
+                    "selp.u32 %0, 1, 0, q;\n"
+                    "}\n"
+                    : "=r"(both)
+                    : "r"(static_cast<uint32_t>(v)), "r"(pair_bar)
+                    : "memory");
+                tc::tc_fence_after();
+                return both != 0;
+            } else {
+                return v;
+            }
+        };
         const float c = a.scale_log2;
         uint32_t sc = 0, oc = 0;  // S tiles and finished O of this tile so far
         for (int it = 0; ok; ++it) {
             const int slot = it & 1;
-            if (!warp_wait(bar(kItemFull0 + slot), (it >> 1) & 1, s_abort)) {
+            if (!pair_and(warp_wait(bar(kItemFull0 + slot), (it >> 1) & 1, s_abort))) {
                 ok = false;
                 break;
             }
@@ -648,22 +704,27 @@ __global__ void __launch_bounds__(kThreads, 1)
             const bool valid = r < (x ? shp.ntok[1] : shp.ntok[0]) * G;
             const int pos = valid ? shp.prefix + t0 + r / G : -1;  // causal limit of this row
             float m_used = -INFINITY;  // running max, log2 units
-            uint64_t lsum[4] = {0, 0, 0, 0};  // 8 independent partial sums, in f32x2 pairs (0 = +0.0f, +0.0f)
+            uint64_t lsum[2] = {0, 0};  // 4 independent partial sums, in f32x2 pairs (0 = +0.0f, +0.0f)
             for (int kt = 0; kt < nt; ++kt) {
-                if (!warp_wait(bar(kSFull0 + x), sc & 1, s_abort)) {
+                const bool s_ready = warp_wait(bar(kSFull0 + x), sc & 1, s_abort);
+                if (kColSplit == 1 && !s_ready) {
                     ok = false;
                     break;
                 }
+                const int buf = sc & 1;
                 ++sc;
                 tc::tc_fence_after();
-                const int j0 = kt * kKeys;
-                const bool diag = __any_sync(0xffffffffu, j0 + kKeys - 1 > pos);
-                // The whole S row in one load and one wait.
-                uint32_t sh[128];
-                tc::tmem_ld128(s_addr, sh);
+                const int j0 = kt * kKeys + half * kCols;  // key of this warp's first column
+                const bool diag = __any_sync(0xffffffffu, j0 + kCols - 1 > pos);
+                // This warp's S columns in one load and one wait.
+                uint32_t sh[kCols];
+                if constexpr (kCols == 128)
+                    tc::tmem_ld128(my_s, sh);
+                else
+                    tc::tmem_ld64(my_s, sh);
                 if (diag) {
 #pragma unroll
-                    for (int j = 0; j < 128; ++j)
+                    for (int j = 0; j < kCols; ++j)
                         if (j0 + j > pos) sh[j] = __float_as_uint(-INFINITY);
                 }
                 float mx8[8];
@@ -671,14 +732,25 @@ __global__ void __launch_bounds__(kThreads, 1)
                 for (int e = 0; e < 8; ++e) mx8[e] = max3(__uint_as_float(sh[e]), __uint_as_float(sh[8 + e]),
                                                           __uint_as_float(sh[16 + e]));
 #pragma unroll
-                for (int j = 24; j < 120; j += 16)
+                for (int j = 24; j < kCols - 8; j += 16)
 #pragma unroll
                     for (int e = 0; e < 8; ++e)
                         mx8[e] = max3(mx8[e], __uint_as_float(sh[j + e]), __uint_as_float(sh[j + 8 + e]));
 #pragma unroll
-                for (int e = 0; e < 8; ++e) mx8[e] = fmaxf(mx8[e], __uint_as_float(sh[120 + e]));
-                const float mx =
-                    max3(max3(mx8[0], mx8[1], mx8[2]), max3(mx8[3], mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7]));
+                for (int e = 0; e < 8; ++e) mx8[e] = fmaxf(mx8[e], __uint_as_float(sh[kCols - 8 + e]));
+                float mx = max3(max3(mx8[0], mx8[1], mx8[2]), max3(mx8[3], mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7]));
+                if constexpr (kColSplit > 1) {
+                    // the row max over both halves; both warps of the pair then
+                    // take the same rescale decisions.  (Two buffers: a warp may
+                    // write the next tile's max before its partner read this one.)
+                    float* const xm = xmax + ((buf * 2 + x) * 2) * kM;
+                    xm[half * kM + r] = mx;
+                    if (!pair_and(s_ready)) {
+                        ok = false;
+                        break;
+                    }
+                    mx = fmaxf(mx, xm[(1 - half) * kM + r]);
+                }
                 const float mnew = mx * c;  // scale > 0, so the max commutes with it
                 float alpha = 1.f;
                 bool rescale = false;
@@ -690,7 +762,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                         alpha = need ? fast_exp2(m_used - mnew) : 1.f;
                         rescale = true;
 #pragma unroll
-                        for (int e = 0; e < 4; ++e) {
+                        for (int e = 0; e < 2; ++e) {
                             const float2 v = unpack2(lsum[e]);
                             asm("mov.b64 %0, {%1, %2};\n" : "=l"(lsum[e]) : "f"(v.x * alpha), "f"(v.y * alpha));
                         }
@@ -698,13 +770,15 @@ __global__ void __launch_bounds__(kThreads, 1)
                     }
                 }
                 const float nmu = m_used == -INFINITY ? 0.f : -m_used;
-                // P = 2^(s*c - m) as bf16 pairs into the last 64 columns of S
-                // (key k to column 64 + k / 2), 32 keys per store; S is all in
-                // registers, so any column may be overwritten.  The P V that read
-                // the previous P finished before this S was written.  l sums the
-                // same bf16-rounded values, so V rows all equal to c give c.
+                // P = 2^(s*c - m) as bf16 pairs over the last 64 columns of S (key
+                // k of the tile to column 64 + k / 2), 32 keys per store.  Every S
+                // column of the tile is in the registers of one of the pair's
+                // warps by now (the exchange above follows both loads), so any
+                // column may be overwritten; the P V that read the previous P
+                // finished before this S was written.  l sums the same bf16
+                // values, so V rows all equal to c give c.
 #pragma unroll
-                for (int ch = 0; ch < 4; ++ch) {
+                for (int ch = 0; ch < kCols / 32; ++ch) {
                     uint32_t pk[16];
 #pragma unroll
                     for (int e = 0; e < 16; ++e) {
@@ -713,18 +787,19 @@ __global__ void __launch_bounds__(kThreads, 1)
                              nmu);
                         const float x0 = fast_exp2(y0), x1 = fast_exp2(y1);
                         pk[e] = pack_bf16(x0, x1);
-                        add_bf16_pair(lsum[e & 3], pk[e]);
+                        add_bf16_pair(lsum[e & 1], pk[e]);
                     }
-                    tc::tmem_st16_async(s_addr + 64 + 16 * ch, pk);
+                    tc::tmem_st16_async(my_p + 16 * ch, pk);
                 }
                 tc::tmem_wait_st();
                 if (rescale) {
                     // O holds tiles < kt: P V(kt-1) was issued before S(kt), and
                     // the commit this warp waited for to read S(kt) completes only
                     // after every earlier MMA of the issuing thread; P V(kt) waits
-                    // for this warp's arrival below.
+                    // for this warp's arrival below.  Each warp of a pair rescales
+                    // its own columns of O.
 #pragma unroll
-                    for (int q = 0; q < D / 32; ++q) {
+                    for (int q = 0; q < kOCols / 32; ++q) {
                         uint32_t o[32];
                         tc::tmem_ld32(o_addr + q * 32, o);
 #pragma unroll
@@ -737,20 +812,29 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (lane == 0) tc::mbar_arrive(bar(kPFull0 + x));
             }
             if (!ok) break;
-            if (!warp_wait(bar(kODone0 + x), oc & 1, s_abort)) {
+            const bool o_ready = warp_wait(bar(kODone0 + x), oc & 1, s_abort);
+            ++oc;
+            tc::tc_fence_after();
+            const float2 l0 = unpack2(lsum[0]), l1 = unpack2(lsum[1]);
+            float l = (l0.x + l0.y) + (l1.x + l1.y);
+            if constexpr (kColSplit > 1) {
+                // l over both halves (the partner reads this slot before either
+                // warp can write it again: the next item's max exchanges come
+                // in between)
+                xl[(x * 2 + half) * kM + r] = l;
+            }
+            if (!pair_and(o_ready)) {
                 ok = false;
                 break;
             }
-            ++oc;
-            tc::tc_fence_after();
-            const float2 l0 = unpack2(lsum[0]), l1 = unpack2(lsum[1]), l2 = unpack2(lsum[2]), l3 = unpack2(lsum[3]);
-            const float l = ((l0.x + l0.y) + (l1.x + l1.y)) + ((l2.x + l2.y) + (l3.x + l3.y));
+            if constexpr (kColSplit > 1) l += xl[(x * 2 + 1 - half) * kM + r];
             const float inv = valid ? 1.f / l : 0.f;
             __nv_bfloat16* orow =
                 reinterpret_cast<__nv_bfloat16*>(a.out) +
-                (static_cast<int64_t>(itm.q0 + t0 + (valid ? r / G : 0)) * a.num_q_heads + itm.h * G + r % G) * D;
+                (static_cast<int64_t>(itm.q0 + t0 + (valid ? r / G : 0)) * a.num_q_heads + itm.h * G + r % G) * D +
+                half * kOCols;
 #pragma unroll
-            for (int q = 0; q < D / 32; ++q) {
+            for (int q = 0; q < kOCols / 32; ++q) {
                 uint32_t o[32];
                 tc::tmem_ld32(o_addr + q * 32, o);
                 if (valid) {
@@ -773,9 +857,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             flag_error(a.err, kDevWaitTimeout);
         }
     } else if (warp < 4) {
-        reg_dec<kRegsIssue>();  // idle warp of warpgroup 0
+        if constexpr (kDecRegs) reg_dec<kRegsIssue>();  // idle warp of warpgroup 0
     } else {
-        reg_inc<kRegsSoftmax>();  // idle softmax warps (one query tile per CTA)
+        if constexpr (kIncRegs) reg_inc<kRegsSoftmax>();  // idle softmax warps (one query tile per CTA)
     }
 
     // ---- teardown: every role is out of its loop; the MMA thread has drained.
@@ -828,7 +912,7 @@ cudaError_t launch_d(const Args& a, cudaStream_t stream) {
         cudaFuncAttributes fa{};
         e = cudaFuncGetAttributes(&fa, prefill_tc_kernel<D>);
         if (e != cudaSuccess) return e;
-        if (static_cast<uint32_t>(fa.numRegs) < kRegsLaunch) return cudaErrorInvalidConfiguration;
+        if (static_cast<uint32_t>(fa.numRegs) < Cfg<D>::kRegsLaunch) return cudaErrorInvalidConfiguration;
         int n = 0;
         e = cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
         if (e != cudaSuccess) return e;
@@ -846,7 +930,7 @@ cudaError_t launch_d(const Args& a, cudaStream_t stream) {
         !encode_cache_map(&tk_map, a.k_cache, D, a.num_kv_heads, a.num_blocks) ||
         !encode_cache_map(&tv_map, a.v_cache, D, a.num_kv_heads, a.num_blocks))
         return cudaErrorInvalidValue;
-    return launch_kernel(prefill_tc_kernel<D>, static_cast<unsigned>(ctas), kThreads, S::kAlloc, stream, 1, tq_map,
+    return launch_kernel(prefill_tc_kernel<D>, static_cast<unsigned>(ctas), Cfg<D>::kThreads, S::kAlloc, stream, 1, tq_map,
                          tk_map, tv_map, a, tq);
 }
 
