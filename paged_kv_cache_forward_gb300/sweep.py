@@ -48,10 +48,11 @@ DIMS = [128, 64, 256]
 BOUNDS = [1024, 2048, 4096, 8192, 16384, 32768, 65536, 131072]
 BATCHES = {128: [1, 2, 4, 8, 16, 32, 64, 128, 256], 64: [1, 4, 16, 64, 256], 256: [1, 4, 16, 64, 256]}
 HQ, HKV, PAGE = 32, 8, 16
+SUB_UNIT_KV_HEADS = [1, 2, 4]  # batch-1 cells with fewer KV heads: 1, 2 and 4 decode units
 MAX_KV_BYTES = 6 << 30
 TOP = 5          # candidates re-timed after the first pass
 REPEATS = 3      # timings per re-timed candidate (the cell takes the best median)
-MIN_MS = 20.0    # graph replays per timing: at least this long, and at least 3
+MIN_MS = 10.0    # graph replays per timing: at least this long, and at least 3
 
 SMEM_PER_SM = 228 << 10
 REGS_PER_SM = 65536
@@ -92,11 +93,17 @@ def time_shape(pools, stream, chunk=0, warps=0, stages=0, cluster=0, steps_per_g
                        decode_stages=stages, decode_warps=warps, decode_cluster=cluster)
     stream.synchronize()
     M = max(R, (steps_per_graph // R) * R)
+    # (captured directly: the torch.cuda.graph context manager also runs a
+    # garbage collection per capture, which dominated the sweep's time)
     g = torch.cuda.CUDAGraph()
-    with torch.cuda.graph(g, stream=stream):
-        for i in range(M):
-            pa.forward(q, ks[i % R], vs[i % R], bt, sl, qsl, out, kv_chunk=chunk, stream=stream,
-                       decode_stages=stages, decode_warps=warps, decode_cluster=cluster)
+    with torch.cuda.stream(stream):
+        g.capture_begin()
+        try:
+            for i in range(M):
+                pa.forward(q, ks[i % R], vs[i % R], bt, sl, qsl, out, kv_chunk=chunk, stream=stream,
+                           decode_stages=stages, decode_warps=warps, decode_cluster=cluster)
+        finally:
+            g.capture_end()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     with torch.cuda.stream(stream):  # a graph replays on the current stream
         g.replay()
@@ -229,6 +236,8 @@ def main(argv=None):
     ap.add_argument("--validate-groups", action="store_true",
                     help="instead of sweeping: time the built table's pick against the best candidate for 1, 8 and "
                          "32 query heads per KV head, and write that to --log")
+    ap.add_argument("--only-sub-units", action="store_true",
+                    help="sweep only the batch-1 cells with 1, 2 and 4 KV heads (fewer than 8 decode units)")
     ap.add_argument("--merge", action="store_true",
                     help="replace only the swept cells of the existing table and log")
     args = ap.parse_args(argv)
@@ -258,22 +267,27 @@ def main(argv=None):
         batches = [int(x) for x in args.batches.split(",")] if args.batches else BATCHES[d]
         variants = [tuple(int(y) for y in v.split("x")) for v in (args.variants or VARIANTS[d]).split(",")]
         variants = [v for v in variants if d != 256 or v[0] == 4]
-        for batch in batches:
+        # (batch, KV heads): one sequence with fewer KV heads gives the cells
+        # below 8 units; then batches of the 8-KV-head shape
+        shapes = [(1, h) for h in SUB_UNIT_KV_HEADS] if not args.batches else []
+        if not args.only_sub_units:
+            shapes += [(b, HKV) for b in batches]
+        for batch, hkv in shapes:
+            units = batch * hkv
             for bound in bounds:
-                if batch * bound * HKV * d * 4 > MAX_KV_BYTES:
+                if batch * bound * hkv * d * 4 > MAX_KV_BYTES:
                     continue
-                pools, kv = make_pools(bound, batch, d, HQ, HKV, l2, gen)
-                units = batch * HKV
+                pools, kv = make_pools(bound, batch, d, 4 * hkv, hkv, l2, gen)
                 res = sweep_cell(pools, stream, all_candidates(bound, units, sms, d, variants, clusters))
                 us, (chunk, st, w, cl), ts = res[0]
-                best[(d, bound, batch)] = (chunk, st, w, cl)
+                best[(d, bound, units)] = (chunk, st, w, cl)
                 row = " ".join(f"{name_of(c, k)}/{ww}x{t}:{kv / u / 1e3:.0f}" + ("*" if len(tsx) > 1 else "")
                                for u, (c, t, ww, k), tsx in sorted(res, key=lambda x: (x[1][2], x[1][1], x[1][3],
                                                                                       x[1][0])))
                 spread = f"{min(ts):.1f}-{max(ts):.1f}"
-                lines[(d, batch, bound)] = (f"| {d} | {batch} | {bound} | {name_of(chunk, cl)} | {w}x{st} | "
-                                            f"{us:.1f} ({spread}) | {kv / us / 1e3:.0f} | {row} |")
-                print(lines[(d, batch, bound)], flush=True)
+                lines[(d, units, bound)] = (f"| {d} | {batch} x {hkv} | {units} | {bound} | {name_of(chunk, cl)} | "
+                                            f"{w}x{st} | {us:.1f} ({spread}) | {kv / us / 1e3:.0f} | {row} |")
+                print(lines[(d, units, bound)], flush=True)
                 del pools
                 torch.cuda.empty_cache()
 
@@ -288,49 +302,47 @@ def main(argv=None):
     with open(args.log, "w") as f:
         f.write(f"# Split-size sweep on {props.name} ({stamp})\n\n"
                 f"Command: `python -m paged_kv_cache_forward_gb300.sweep {' '.join(argv or sys.argv[1:])}`\n\n"
-                "Decode batches with 32 query heads and 8 KV heads; batch 1 at the bound, larger batches\n"
-                "with lengths uniform in [bound/16, bound] (seeded per cell),\n"
+                "Decode batches with 4 query heads per KV head: one sequence with 1, 2, 4 or 8 KV heads at\n"
+                "the bound, larger batches (8 KV heads) with lengths uniform in [bound/16, bound] (seeded\n"
+                "per cell); units = sequences x KV heads, the table's key,\n"
                 "graph-replayed pa_forward steps rotating over KV pool copies larger than 3 x L2.\n"
                 "GB/s = KV bytes per step / step time.  Every candidate is timed once; the five fastest\n"
                 f"(marked *) {REPEATS} times, and the cell keeps the best median (its spread in brackets).\n\n"
                 "Split `cN`: the pages dealt round-robin to a thread-block cluster of N CTAs.\n\n"
-                "| head_dim | batch | bound | best split | warps x stages | us/step | GB/s | "
+                "| head_dim | batch x KV heads | units | bound | best split | warps x stages | us/step | GB/s | "
                 "split/variant:GB/s for every candidate |\n"
-                "|---|---|---|---|---|---|---|---|\n")
+                "|---|---|---|---|---|---|---|---|---|\n")
         f.write("\n".join(lines[k] for k in sorted(lines)) + "\n")
     print(f"wrote {args.log}" + ("" if args.no_write else f" and {args.out}"))
 
 
 def read_table(path):
-    """The cells of an existing table: {(head_dim, bound, batch): (chunk, stages, warps, cluster)}
+    """The cells of an existing table: {(head_dim, bound, units): (chunk, stages, warps, cluster)}
     (the catch-all rows are dropped)."""
     cells = {}
     rows = re.findall(r"\{(\d+), (\d+), (\d+), (\d+), (\d+), (\d+), (\d+)\}", open(path).read())
     for d, bound, units, chunk, st, w, cl in rows:
-        d, units = int(d), int(units)
-        if units >= 1 << 30 or int(bound) >= 1 << 30:
-            continue
-        cells[(d, int(bound), units // HKV)] = (int(chunk), int(st), int(w), int(cl))
+        cells[(int(d), int(bound), int(units))] = (int(chunk), int(st), int(w), int(cl))
     return cells
 
 
 def read_log(path):
-    """The rows of an existing sweep log: {(head_dim, batch, bound): line}."""
+    """The rows of an existing sweep log: {(head_dim, units, bound): line}."""
     out = {}
     if os.path.exists(path):
         for line in open(path):
-            m = re.match(r"\| (\d+) \| (\d+) \| (\d+) \|", line)
+            m = re.match(r"\| (\d+) \| [^|]+ \| (\d+) \| (\d+) \|", line)
             if m:
                 out[(int(m.group(1)), int(m.group(2)), int(m.group(3)))] = line.rstrip("\n")
     return out
 
 
 def write_table(path, best, gpu_name, stamp):
-    """Rows {head_dim, max_bound, max_units, ...}: per head dim, batch-major, so the
-    first match is the smallest swept batch (in decode units) >= the call's and,
-    within it, the smallest swept bound >= the call's.  Each head dim ends with
-    catch-all rows: its largest batch's cells for any number of units, and that
-    batch's largest bound for any bound."""
+    """Rows {head_dim, max_bound, max_units, ...}: per head dim, units-major, so the
+    first match is the smallest swept number of units >= the call's and, within
+    it, the smallest swept bound >= the call's.  Each head dim ends with
+    catch-all rows: its largest units' cells for any number of units, and that
+    group's largest bound for any bound."""
     with open(path, "w") as f:
         f.write("// Keys per split and decode kernel variant, keyed on the head dim, the\n"
                 "// context bound (max_pages * page_size) and the number of decode units:\n"
@@ -342,18 +354,18 @@ def write_table(path, best, gpu_name, stamp):
                 "static const LutEntry kSplitTable[] = {\n")
         for d in sorted({k[0] for k in best}):
             cells = {k[1:]: v for k, v in best.items() if k[0] == d}
-            batches = sorted({b for _, b in cells})
+            units = sorted({u for _, u in cells})
             bounds = sorted({bd for bd, _ in cells})
-            row = lambda bound, units, c: f"    {{{d}, {bound}, {units}, {c[0] or 16}, {c[1]}, {c[2]}, {c[3]}}},\n"
-            for batch in batches:
+            row = lambda bound, mu, c: f"    {{{d}, {bound}, {mu}, {c[0] or 16}, {c[1]}, {c[2]}, {c[3]}}},\n"
+            for u in units:
                 for bound in bounds:
-                    if (bound, batch) in cells:
-                        f.write(row(bound, batch * HKV, cells[(bound, batch)]))
-            top = batches[-1]
+                    if (bound, u) in cells:
+                        f.write(row(bound, u, cells[(bound, u)]))
+            top = units[-1]
             for bound in bounds:
                 if (bound, top) in cells:
                     f.write(row(bound, "1 << 30", cells[(bound, top)]))
-            f.write(row("1 << 30", "1 << 30", cells[max(b for b, bt in cells if bt == top), top]))
+            f.write(row("1 << 30", "1 << 30", cells[max(b for b, u in cells if u == top), top]))
         f.write("};\n")
 
 

@@ -33,12 +33,14 @@ def test_every_head_dim_ends_with_a_catch_all():
 
 def test_merge_replaces_one_cell():
     cells = S.read_table(TABLE)
-    key = (128, 4096, 1)
+    key = (128, 4096, 8)  # (head dim, bound, decode units)
+    new = (48, 4, 4, 1) if cells[key] != (48, 4, 4, 1) else (64, 4, 4, 1)
     merged = dict(cells)
-    merged[key] = (0, 2, 8, 12)
+    merged[key] = new
     with tempfile.TemporaryDirectory() as d:
         out = os.path.join(d, "t.inc")
         S.write_table(out, merged, "test", "today")
         a, b = _rows(TABLE), _rows(out)
         diff = [(x, y) for x, y in zip(a, b) if x != y]
-        assert len(a) == len(b) and len(diff) == 1 and diff[0][1].strip() == "{128, 4096, 8, 16, 2, 8, 12},"
+        assert len(a) == len(b) and len(diff) == 1
+        assert diff[0][1].strip() == f"{{128, 4096, 8, {new[0]}, 4, 4, 1}},"
