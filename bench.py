@@ -74,7 +74,8 @@ DESCRIPTIONS = {
     "mixed": "4 prefill x 512 + 60 decode ctx U[1024, 16384] + 1 decode ctx 131072, Hq 32 / Hkv 8, D 128",
     "spec_decode": "batch 16 x 4 new tokens (speculative decoding), ctx U[2048, 8192], Hq 32 / Hkv 8, D 128",
 }
-KERNEL_RUN = 16            # consecutive launches per timed run of the dominant kernel
+KERNEL_RUN = 16            # consecutive launches per timed run of the dominant kernel (at least)
+KERNEL_RUN_MAX = 128
 KERNEL_MIN_RUNS = 100
 KERNEL_MIN_S = 0.25
 E2E_MIN_S = 0.2
@@ -97,6 +98,8 @@ def parse_args(argv=None):
     ap.add_argument("--layers", type=int, default=0,
                     help="model-step mode: L layers, each with its own KV cache, one pa_forward per layer; "
                          "times one CUDA graph of all L layers against L one-layer graphs and eager calls")
+    ap.add_argument("--kernel-runs", type=int, default=KERNEL_MIN_RUNS,
+                    help="timed runs of the dominant kernel alone (profiling runs use fewer)")
     ap.add_argument("--settle-ms", type=float, default=SETTLE_MS,
                     help="graph replays before the timed region so that clocks settle; 0 for profiling runs")
     return ap.parse_args(argv)
@@ -422,7 +425,20 @@ class Workload:
         return g
 
 
-def time_kernel(wl, world):
+def timing_events(external: bool):
+    """A pair of timing events; external ones are recorded as nodes of a graph
+    captured around them (None, None if this torch has no external events)."""
+    import torch
+    if not external:
+        return torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    try:
+        return (torch.cuda.Event(enable_timing=True, external=True),
+                torch.cuda.Event(enable_timing=True, external=True))
+    except TypeError:
+        return None, None
+
+
+def time_kernel(wl, world, est_ms, min_runs=KERNEL_MIN_RUNS):
     """Mean, median, p10, p90 launch duration (ms) of the dominant kernel alone:
     a graph of KERNEL_RUN consecutive launches (the pool copies in rotation)
     bracketed by CUDA events recorded on the launching stream, replayed at least
@@ -430,7 +446,10 @@ def time_kernel(wl, world):
     torch = wl.torch
     key = "prefill" if wl.dominant == "prefill" else "decode"
     only = (2 if key == "prefill" else 1) if wl.plan["launches"] > 1 else 0
-    run = max(KERNEL_RUN, wl.R) // wl.R * wl.R if wl.R <= KERNEL_RUN else wl.R
+    # a run lasts about a millisecond (16 to 128 launches): the two event nodes
+    # and the graph's own start cost stay small against it
+    want = int(min(KERNEL_RUN_MAX, max(KERNEL_RUN, math.ceil(1.0 / max(est_ms, 1e-3)))))
+    run = max(wl.R, want // wl.R * wl.R)
     e_a, e_b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     # torch creates the CUDA event on its first record(); do that outside the
     # capture so that the library receives real handles to re-record.
@@ -451,7 +470,8 @@ def time_kernel(wl, world):
         g.replay()
     wl.stream.synchronize()
     first = e_a.elapsed_time(e_b) / run
-    n_runs = max(KERNEL_MIN_RUNS, int(math.ceil(KERNEL_MIN_S / max(first * run / 1e3, 1e-6))))
+    n_runs = max(min_runs, int(math.ceil(KERNEL_MIN_S / max(first * run / 1e3, 1e-6)))) if min_runs >= \
+        KERNEL_MIN_RUNS else max(1, min_runs)
     per = []
     for _ in range(n_runs):
         with torch.cuda.stream(wl.stream):
@@ -640,24 +660,48 @@ def measure(config, args, dev, rank, world, local, steps=None, warmup=None, with
             g_main.replay()
     stream.synchronize()
 
-    start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    # When the K steps fit one graph, the region's two events are recorded by
+    # nodes of that graph, first and last, so the region holds exactly the K
+    # steps (not the graph's launch latency); otherwise they bracket the replays.
+    start, stop = timing_events(external=True)
+    g_timed = None
+    if full == 1 and g_rem is None and start is not None:
+        # (torch creates the CUDA event on its first record: outside the capture)
+        start.record(stream)
+        stop.record(stream)
+        stream.synchronize()
+
+        def timed_steps(i):
+            if i == 0:
+                start.record(stream)
+            wl.call(i)
+            if i == M - 1:
+                stop.record(stream)
+        g_timed = wl.graph(M, timed_steps)
+    else:
+        start, stop = timing_events(external=False)
     barrier(world)
     torch.cuda.synchronize(dev)
     with torch.cuda.stream(stream):
-        start.record()
-        for _ in range(full):
-            g_main.replay()
-        if g_rem is not None:
-            g_rem.replay()
-        stop.record()
+        if g_timed is not None:
+            g_timed.replay()
+        else:
+            start.record()
+            for _ in range(full):
+                g_main.replay()
+            if g_rem is not None:
+                g_rem.replay()
+            stop.record()
     stream.synchronize()
     torch.cuda.synchronize(dev)
     barrier(world)
     region_ms = start.elapsed_time(stop)
     assert pa.device_error(stream) == 0
-    del g_main, g_rem
+    region_how = ("CUDA events recorded by the first and last nodes of one graph of the K steps" if g_timed is not None
+                  else f"CUDA events around {full} replay(s) of a {M}-step graph" + (" and one of the rest" if rem else ""))
+    del g_main, g_rem, g_timed
 
-    kern = time_kernel(wl, world)
+    kern = time_kernel(wl, world, est_ms, args.kernel_runs)
     t_load1 = time.time()
     sampler.stop()
     assert pa.device_error(stream) == 0
@@ -711,7 +755,8 @@ def measure(config, args, dev, rank, world, local, steps=None, warmup=None, with
             "kv_bytes_per_step": int(total_kv), "causal_flops_per_step": int(total_flops),
             "l2": (f"inputs rotate over {R} KV pool copies ({R} x {work['kv_bytes'] / 2**20:.0f} MiB "
                    f"> 3 x L2 {wl.l2 / 2**20:.0f} MiB)") if R > 1 else "KV bytes per step > 3 x L2",
-            "graph": f"CUDA graphs of {M} steps", "settle_ms": round(settle_reps * M * est_ms, 1),
+            "graph": f"CUDA graphs of {M} steps", "timed_region": region_how,
+            "settle_ms": round(settle_reps * M * est_ms, 1),
             "kv_chunk": wl.plan["kv_chunk"], "splits": wl.plan["splits"],
             "decode_variant": f"{wl.plan['decode_warps']} warps x {wl.plan['decode_stages']} stages, "
                               f"cluster {wl.plan['decode_cluster']}",

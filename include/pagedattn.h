@@ -34,8 +34,8 @@
  *   query_start_loc [B + 1]           int32   0 = qsl[0] <= qsl[1] <= ... = T
  *   out             [T, Hq, D]        bf16    written for every query row
  * Logical position j of sequence b is slot j % P of physical page
- * block_table[b][j / P].  Entries of block_table past a sequence's last page are
- * never read.
+ * block_table[b][j / P].  Entries of block_table past a sequence's last page may
+ * be loaded but are never used: they need not be valid block ids.
  *
  * Pointers.  Every data pointer is a DEVICE pointer on the current CUDA device
  * (the one the stream belongs to).  q, k_cache, v_cache and out must be 16-byte

@@ -91,10 +91,12 @@ __device__ __forceinline__ int64_t partial_row(const Args& a, int b, int s, int 
 // Softmax"): M = max_s m_s, w_s = 2^(m_s - M), out = sum_s w_s O_s / sum_s w_s l_s.
 // A split that saw no visible key of a row has m_s = -inf and weight 0.  The
 // partials were written by other CTAs, so they are read with L2-coherent loads.
-// One thread per (row, 4 columns) reads the (m, l) and O of kBatch splits per
-// batch into one of two register buffers, the next batch's loads in flight
-// while the current one is combined: 2 * kBatch splits take one round trip to
-// L2, and a long run of splits streams instead of waiting batch by batch.
+// A work item is (row, 4 columns).  When the CTA has at least two threads per
+// item, lanes l and l + 16 of a warp share one item and take the even and the
+// odd splits, then combine by a shuffle, so each thread waits for half as many
+// loads.  A thread reads the (m, l) and O of kBatch of its splits per batch into
+// one of two register buffers, the next batch's loads in flight while the
+// current one is combined.
 template <int D, int kBatch>
 __device__ __forceinline__ void merge_splits(const Args& a, int b, const int* tok, const int* head, int rows,
                                              int nsplits, int q0) {
@@ -102,63 +104,95 @@ __device__ __forceinline__ void merge_splits(const Args& a, int b, const int* to
     const int64_t split_o = split_rows * D;
     __nv_bfloat16* out = reinterpret_cast<__nv_bfloat16*>(a.out);
     constexpr int kGroups = D / 4;  // 4 consecutive columns per work item
-    for (int it = threadIdx.x; it < rows * kGroups; it += blockDim.x) {
-        const int r = it / kGroups;
-        const int d4 = (it % kGroups) * 4;
-        const int64_t row = partial_row(a, b, 0, tok[r], head[r]);
-        const float2* ml = reinterpret_cast<const float2*>(a.ws_ml) + row;  // (m, l) of split 0
-        const float* os = a.ws_o + row * D + d4;
+    const int total = rows * kGroups;
+    const bool two = static_cast<int>(blockDim.x) >= 2 * total;
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int per_warp = two ? 16 : 32;
+    const int part = two ? lane >> 4 : 0;
+    const int stride = two ? 2 : 1;
+    const int nloc = (nsplits - part + stride - 1) / stride;  // splits part, part + stride, ...
+    for (int base = warp * per_warp; base < total; base += (blockDim.x >> 5) * per_warp) {
+        const int it = base + (two ? (lane & 15) : lane);
+        const bool active = it < total;
+        const int r = active ? it / kGroups : 0;
+        const int d4 = active ? (it % kGroups) * 4 : 0;
         float M = -INFINITY, den = 0.f;
         float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-        auto load = [&](int s0, float2 (&mlv)[kBatch], float4 (&ov)[kBatch]) {
+        if (active) {
+            const int64_t row = partial_row(a, b, 0, tok[r], head[r]);
+            const float2* ml = reinterpret_cast<const float2*>(a.ws_ml) + row;  // (m, l) of split 0
+            const float* os = a.ws_o + row * D + d4;
+            auto load = [&](int j0, float2 (&mlv)[kBatch], float4 (&ov)[kBatch]) {
 #pragma unroll
-            for (int k = 0; k < kBatch; ++k) {
-                if (s0 + k < nsplits) {
-                    mlv[k] = __ldcg(ml + (s0 + k) * split_rows);
-                    ov[k] = __ldcg(reinterpret_cast<const float4*>(os + (s0 + k) * split_o));
-                } else {
-                    mlv[k] = make_float2(-INFINITY, 0.f);
-                    ov[k] = make_float4(0.f, 0.f, 0.f, 0.f);
+                for (int k = 0; k < kBatch; ++k) {
+                    if (j0 + k < nloc) {
+                        const int sp = part + stride * (j0 + k);
+                        mlv[k] = __ldcg(ml + sp * split_rows);
+                        ov[k] = __ldcg(reinterpret_cast<const float4*>(os + sp * split_o));
+                    } else {
+                        mlv[k] = make_float2(-INFINITY, 0.f);
+                        ov[k] = make_float4(0.f, 0.f, 0.f, 0.f);
+                    }
                 }
-            }
-        };
-        auto combine = [&](const float2 (&mlv)[kBatch], const float4 (&ov)[kBatch]) {
-            float Mn = M;
+            };
+            auto combine = [&](const float2 (&mlv)[kBatch], const float4 (&ov)[kBatch]) {
+                float Mn = M;
 #pragma unroll
-            for (int k = 0; k < kBatch; ++k) Mn = fmaxf(Mn, mlv[k].x);
-            const float sc = M == -INFINITY ? 0.f : fast_exp2(M - Mn);  // earlier batches, rebased
-            den *= sc;
-            acc.x *= sc;
-            acc.y *= sc;
-            acc.z *= sc;
-            acc.w *= sc;
+                for (int k = 0; k < kBatch; ++k) Mn = fmaxf(Mn, mlv[k].x);
+                const float sc = M == -INFINITY ? 0.f : fast_exp2(M - Mn);  // earlier batches, rebased
+                den *= sc;
+                acc.x *= sc;
+                acc.y *= sc;
+                acc.z *= sc;
+                acc.w *= sc;
 #pragma unroll
-            for (int k = 0; k < kBatch; ++k) {
-                const float w = mlv[k].x == -INFINITY ? 0.f : fast_exp2(mlv[k].x - Mn);
-                den += w * mlv[k].y;
-                acc.x += w * ov[k].x;
-                acc.y += w * ov[k].y;
-                acc.z += w * ov[k].z;
-                acc.w += w * ov[k].w;
+                for (int k = 0; k < kBatch; ++k) {
+                    const float w = mlv[k].x == -INFINITY ? 0.f : fast_exp2(mlv[k].x - Mn);
+                    den += w * mlv[k].y;
+                    acc.x += w * ov[k].x;
+                    acc.y += w * ov[k].y;
+                    acc.z += w * ov[k].z;
+                    acc.w += w * ov[k].w;
+                }
+                M = Mn;
+            };
+            float2 mla[kBatch], mlb[kBatch];
+            float4 oa[kBatch], ob[kBatch];
+            load(0, mla, oa);
+            for (int j0 = 0; j0 < nloc; j0 += 2 * kBatch) {
+                const bool second = j0 + kBatch < nloc;
+                if (second) load(j0 + kBatch, mlb, ob);
+                combine(mla, oa);
+                if (j0 + 2 * kBatch < nloc) load(j0 + 2 * kBatch, mla, oa);
+                if (second) combine(mlb, ob);
             }
-            M = Mn;
-        };
-        float2 mla[kBatch], mlb[kBatch];
-        float4 oa[kBatch], ob[kBatch];
-        load(0, mla, oa);
-        for (int s0 = 0; s0 < nsplits; s0 += 2 * kBatch) {
-            const bool second = s0 + kBatch < nsplits;
-            if (second) load(s0 + kBatch, mlb, ob);
-            combine(mla, oa);
-            if (s0 + 2 * kBatch < nsplits) load(s0 + 2 * kBatch, mla, oa);
-            if (second) combine(mlb, ob);
         }
-        const float inv = 1.f / den;
-        uint2 packed;
-        packed.x = pack_bf16(acc.x * inv, acc.y * inv);
-        packed.y = pack_bf16(acc.z * inv, acc.w * inv);
-        *reinterpret_cast<uint2*>(out + (static_cast<int64_t>(q0 + tok[r]) * a.num_q_heads + head[r]) * D + d4) =
-            packed;
+        if (two) {
+            // the other half of the splits, from lane ^ 16 (every lane takes part)
+            const float Mo = __shfl_xor_sync(0xffffffffu, M, 16);
+            const float deno = __shfl_xor_sync(0xffffffffu, den, 16);
+            float4 acco;
+            acco.x = __shfl_xor_sync(0xffffffffu, acc.x, 16);
+            acco.y = __shfl_xor_sync(0xffffffffu, acc.y, 16);
+            acco.z = __shfl_xor_sync(0xffffffffu, acc.z, 16);
+            acco.w = __shfl_xor_sync(0xffffffffu, acc.w, 16);
+            const float Mn = fmaxf(M, Mo);
+            const float w = M == -INFINITY ? 0.f : fast_exp2(M - Mn);
+            const float wo = Mo == -INFINITY ? 0.f : fast_exp2(Mo - Mn);
+            den = w * den + wo * deno;
+            acc.x = w * acc.x + wo * acco.x;
+            acc.y = w * acc.y + wo * acco.y;
+            acc.z = w * acc.z + wo * acco.z;
+            acc.w = w * acc.w + wo * acco.w;
+        }
+        if (active && part == 0) {
+            const float inv = 1.f / den;
+            uint2 packed;
+            packed.x = pack_bf16(acc.x * inv, acc.y * inv);
+            packed.y = pack_bf16(acc.z * inv, acc.w * inv);
+            *reinterpret_cast<uint2*>(out + (static_cast<int64_t>(q0 + tok[r]) * a.num_q_heads + head[r]) * D + d4) =
+                packed;
+        }
     }
 }
 
