@@ -49,7 +49,7 @@ cudaError_t launch_cache_write(const void* k_new, const void* v_new, const int64
                                int32_t num_kv_heads, int32_t head_dim, int32_t* err, cudaStream_t stream) {
     if (num_tokens == 0) return cudaSuccess;
     const int row_chunks = num_kv_heads * head_dim / 8;
-    return launch_kernel(cache_write_kernel, static_cast<unsigned>(num_tokens), kThreads, 0, stream, 1,
+    return launch_kernel(cache_write_kernel, static_cast<unsigned>(num_tokens), kThreads, 0, stream, 1, false,
                          static_cast<const uint4*>(k_new), static_cast<const uint4*>(v_new), slot_mapping,
                          static_cast<uint4*>(k_cache), static_cast<uint4*>(v_cache), num_blocks * page_size,
                          row_chunks, err);

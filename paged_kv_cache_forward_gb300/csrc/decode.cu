@@ -236,6 +236,7 @@ __global__ void __launch_bounds__(kWarps * 32, (kWarps == 4 && D <= 128) ? 3 : 1
     decode_splitkv_kernel(const Args a) {
     using Tile = DecodeTile<D, kWarps, kStages>;
     extern __shared__ __align__(128) uint8_t smem[];
+    grid_dependency_sync();  // (no memory access before this point)
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
     const int g = lane >> 2;   // MMA group id: row g and g + 8
@@ -600,21 +601,28 @@ cudaError_t launch_decode_d(const Args& a, cudaStream_t stream) {
     using Tile = DecodeTile<D, kWarps, kStages>;
     auto kernel = decode_splitkv_kernel<D, kWarps, kStages>;
     // The attributes are set once per device.  Host threads may race here; both
-    // then set the same values, which is harmless, and the flag is atomic.
+    // then set the same values, which is harmless, and the flags are atomic.
     static std::atomic<bool> configured[64];
+    static std::atomic<int> sms[64];
     int dev = 0;
     cudaGetDevice(&dev);
     if (!configured[dev & 63].load(std::memory_order_acquire)) {
         cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                              Tile::kSmemBytes + Tile::kRecvBytes);
         if (e == cudaSuccess) e = cudaFuncSetAttribute(kernel, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+        int n = 0;
+        if (e == cudaSuccess) e = cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
         if (e != cudaSuccess) return e;
+        sms[dev & 63].store(n, std::memory_order_relaxed);
         configured[dev & 63].store(true, std::memory_order_release);
     }
     const int64_t ctas = decode_ctas(a);
     if (ctas == 0) return cudaSuccess;
     const size_t smem = Tile::kSmemBytes + (a.decode_cluster > 1 ? Tile::kRecvBytes : 0);
-    return launch_kernel(kernel, static_cast<unsigned>(ctas), kWarps * 32, smem, stream, a.decode_cluster, a);
+    // programmatic dependent launch for grids of at most one CTA per SM (larger
+    // grids would land unevenly on SMs still busy with the previous kernel)
+    const bool pdl = ctas <= sms[dev & 63].load(std::memory_order_relaxed);
+    return launch_kernel(kernel, static_cast<unsigned>(ctas), kWarps * 32, smem, stream, a.decode_cluster, pdl, a);
 }
 
 template <int D>

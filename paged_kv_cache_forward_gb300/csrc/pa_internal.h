@@ -94,28 +94,45 @@ inline WorkspaceLayout workspace_layout(int64_t num_seqs, int32_t num_q_heads, i
 }
 
 // Launches a kernel of this library, as 1-D thread-block clusters of `cluster`
-// CTAs if cluster > 1.  (Programmatic dependent launch was measured and left
-// out: early-resident CTAs of the next step land unevenly on the SMs.)
+// CTAs if cluster > 1.  With `pdl`, the launch allows programmatic dependent
+// launch: the grid may be scheduled while the previous kernel on the stream is
+// still finishing (once all of that kernel's CTAs have started and signalled),
+// and the kernel's griddepcontrol.wait, before its first memory access, holds
+// it until that kernel has completed and its writes are visible.  That hides
+// the launch latency of back-to-back calls and changes no result.  Used only
+// for grids that fit on the GPU in one wave, whose CTAs then land one per SM.
 template <typename... KArgs, typename... Args>
 cudaError_t launch_kernel(void (*kernel)(KArgs...), unsigned grid, unsigned block, size_t smem,
-                          cudaStream_t stream, int cluster, Args&&... args) {
+                          cudaStream_t stream, int cluster, bool pdl, Args&&... args) {
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(grid, 1, 1);
     cfg.blockDim = dim3(block, 1, 1);
     cfg.dynamicSmemBytes = smem;
     cfg.stream = stream;
-    cudaLaunchAttribute attr[1];
+    cudaLaunchAttribute attr[2];
     int n = 0;
     if (cluster > 1) {
-        attr[0].id = cudaLaunchAttributeClusterDimension;
-        attr[0].val.clusterDim.x = static_cast<unsigned>(cluster);
-        attr[0].val.clusterDim.y = 1;
-        attr[0].val.clusterDim.z = 1;
-        n = 1;
+        attr[n].id = cudaLaunchAttributeClusterDimension;
+        attr[n].val.clusterDim.x = static_cast<unsigned>(cluster);
+        attr[n].val.clusterDim.y = 1;
+        attr[n].val.clusterDim.z = 1;
+        ++n;
+    }
+    if (pdl) {
+        attr[n].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[n].val.programmaticStreamSerializationAllowed = 1;
+        ++n;
     }
     cfg.attrs = attr;
     cfg.numAttrs = n;
     return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+}
+
+// The first statements of a kernel launched with pdl: let the next kernel on
+// the stream be scheduled, then wait until the previous one has completed.
+__device__ __forceinline__ void grid_dependency_sync() {
+    asm volatile("griddepcontrol.launch_dependents;\n" ::: "memory");
+    asm volatile("griddepcontrol.wait;\n" ::: "memory");
 }
 
 // Sets the calling thread's pa_last_error() text.

@@ -930,7 +930,10 @@ cudaError_t launch_d(const Args& a, cudaStream_t stream) {
         !encode_cache_map(&tk_map, a.k_cache, D, a.num_kv_heads, a.num_blocks) ||
         !encode_cache_map(&tv_map, a.v_cache, D, a.num_kv_heads, a.num_blocks))
         return cudaErrorInvalidValue;
-    return launch_kernel(prefill_tc_kernel<D>, static_cast<unsigned>(ctas), Cfg<D>::kThreads, S::kAlloc, stream, 1, tq_map,
+    // (no programmatic dependent launch: back-to-back prefill calls gained
+    // nothing measurable from it, and mixed batches, whose prefill kernel runs
+    // beside the decode kernel, lost 2 %)
+    return launch_kernel(prefill_tc_kernel<D>, static_cast<unsigned>(ctas), Cfg<D>::kThreads, S::kAlloc, stream, 1, false, tq_map,
                          tk_map, tv_map, a, tq);
 }
 

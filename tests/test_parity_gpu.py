@@ -490,3 +490,26 @@ def test_workspace_reuse_across_growing_batches():
         s.synchronize()
         assert pa.device_error(s) == 0
         assert_close(out.cpu(), oracle.batch_attention(b), f"B {B}")
+
+
+def test_launch_only_writes_one_kernels_rows():
+    """pa_options.launch_only (timing and tests): 1 launches only the decode
+    kernel, 2 only the prefill kernel; each writes exactly its own rows, equal
+    bit for bit to the rows of a full call."""
+    b = W.make_batch([300, 1, 3, 150, 1], [800, 2000, 40, 150, 9000], 32, 8, 128, seed=81)
+    full = run(b)
+    qsl = b.query_start_loc.tolist()
+    decode_rows = torch.zeros(b.num_tokens, dtype=torch.bool)
+    for s, n in enumerate(b.q_lens()):
+        if 1 <= n <= 4:  # G = 4: up to 4 new tokens take the decode kernel
+            decode_rows[qsl[s]:qsl[s + 1]] = True
+    d = b.to("cuda")
+    for only, mine in ((1, decode_rows), (2, ~decode_rows)):
+        out = torch.full_like(d.q, float("nan"))
+        pa.forward(d.q, d.k_cache, d.v_cache, d.block_table, d.seq_lens, d.query_start_loc, out, scale=b.scale,
+                   launch_only=only)
+        torch.cuda.synchronize()
+        assert pa.device_error() == 0
+        got = out.cpu()
+        assert torch.equal(got[mine].view(torch.int16), full[mine].view(torch.int16)), only
+        assert torch.isnan(got[~mine].float()).all(), only
