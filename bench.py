@@ -9,9 +9,10 @@ headline workload is the Llama-3.1-8B-shaped single-stream decode at context
 scattered in a pool 1.5x the need); --config picks another.  At N = 1 the same
 process also measures every other workload of the metric (single-stream decode
 at 1024 and 8192, the 64-sequence batched decode, the causal varlen prefill, the
-mixed batch) and a 32-layer full-graph decoder step, each as a record under
-"sub_records" with its own timing, kernel roofline, end-to-end figure and clock
-summary.
+mixed batch), speculative multi-token decode, the paged KV-cache write of the
+prefill's new tokens and a 32-layer full-graph decoder step, each as a record
+under "sub_records" with its own timing, kernel roofline and clock summary (and
+an end-to-end figure for the attention workloads).
 
 Per workload:
   * timed region: `steps` steps replayed from CUDA graphs, after W untimed
@@ -54,7 +55,7 @@ sys.path.insert(0, ROOT)
 
 HEADLINE = "llama_decode_32768"
 SUB_CONFIGS = ["llama_decode_1024", "llama_decode_8192", "llama_decode_32768", "batched_decode", "varlen_prefill",
-               "mixed"]
+               "mixed", "spec_decode"]
 LAYERS_SUB = ("llama_decode_32768", 32)  # the full-graph decoder step of the sub-records
 FALLBACK_HBM_GBS = 6800.0      # profiling recipe's fallback, one earlier GB300 measurement
 FALLBACK_BF16_TFLOPS = 1900.0
@@ -906,6 +907,122 @@ def measure_layers(config, L, args, dev, rank, world, local, steps=50):
     return rec, identical
 
 
+def measure_cache_write(args, dev, rank, world, local, steps=None):
+    """The paged KV-cache write (pa_cache_write) of the varlen prefill's new
+    tokens (Llama shape: 8 KV heads, head_dim 128): each token's K and V rows
+    scattered to its page slot, 16 consecutive tokens to a page, pages drawn at
+    random from a pool.  Algorithmic bytes per launch = read and write of K and V
+    (4 x tokens x 2 KiB) + the 8-byte slot of every token; rotating over R sets of
+    buffers larger than 3 x L2 together."""
+    import torch
+    import paged_kv_cache_forward_gb300 as pa
+    from paged_kv_cache_forward_gb300 import workloads as W
+    b = W.varlen_prefill(seed=rank_seed(args.seed, rank))
+    T, Hkv, D, P = b.num_tokens, b.num_kv_heads, b.head_dim, b.page_size
+    row = Hkv * D * 2
+    nbytes = 4 * T * row + 8 * T
+    props = torch.cuda.get_device_properties(dev)
+    l2 = getattr(props, "L2_cache_size", 128 << 20) or (128 << 20)
+    R = 1 if nbytes > 3 * l2 else int(math.ceil(3 * l2 / nbytes)) + 1
+    gen = torch.Generator(device=dev).manual_seed(rank_seed(args.seed, rank) + 7)
+    pages = (T + P - 1) // P + 1
+    sets = []
+    for _ in range(R):
+        perm = torch.randperm(pages, device=dev, generator=gen)
+        t = torch.arange(T, device=dev)
+        slots = (perm[t // P] * P + t % P).to(torch.int64)
+        sets.append((torch.randn(T, Hkv, D, device=dev, generator=gen).to(torch.bfloat16),
+                     torch.randn(T, Hkv, D, device=dev, generator=gen).to(torch.bfloat16), slots,
+                     torch.zeros(pages, P, Hkv, D, device=dev, dtype=torch.bfloat16),
+                     torch.zeros(pages, P, Hkv, D, device=dev, dtype=torch.bfloat16)))
+    stream = torch.cuda.Stream(device=dev)
+    torch.cuda.synchronize(dev)
+
+    def call(i):
+        kn, vn, sl, kc, vc = sets[i % R]
+        pa.cache_write(kn, vn, sl, kc, vc, stream=stream)
+
+    with torch.cuda.stream(stream):
+        for i in range(max(1, args.warmup)):
+            call(i)
+    stream.synchronize()
+    assert pa.device_error(stream) == 0
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        e0.record()
+        for i in range(10):
+            call(i)
+        e1.record()
+    stream.synchronize()
+    est_ms = e0.elapsed_time(e1) / 10
+    steps = steps or max(R, int(min(256, max(16, 0.05e3 / max(est_ms, 1e-3)))) // R * R)
+    start, stop = timing_events(external=True)
+    external = start is not None
+    if not external:
+        start, stop = timing_events(external=False)
+    start.record(stream)
+    stop.record(stream)
+    stream.synchronize()
+
+    def steps_fn(i):
+        if external and i == 0:
+            start.record(stream)
+        call(i)
+        if external and i == steps - 1:
+            stop.record(stream)
+
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=stream):
+        for i in range(steps):
+            steps_fn(i)
+    sampler = ClockSampler(local).start()
+    t0 = time.time()
+    with torch.cuda.stream(stream):
+        for _ in range(int(math.ceil(args.settle_ms / max(est_ms * steps, 1e-3)))):
+            g.replay()
+    stream.synchronize()
+    times = []
+    for _ in range(20):
+        barrier(world)
+        torch.cuda.synchronize(dev)
+        with torch.cuda.stream(stream):
+            torch.cuda._sleep(int(30e-6 * SM_HZ_NOMINAL))
+            if not external:
+                start.record()
+            g.replay()
+            if not external:
+                stop.record()
+        stream.synchronize()
+        times.append(reduce_max(start.elapsed_time(stop), world, dev) / steps)
+    t1 = time.time()
+    sampler.stop()
+    assert pa.device_error(stream) == 0
+    st = stats_ms(times)
+    peak, src = measured_peaks()["hbm"]
+    total = reduce_sum(nbytes, world, dev)
+    achieved = nbytes / (st["mean"] / 1e3) / 1e9
+    rec = {
+        "metric": "paged KV-cache write GB/s", "value": total / (st["median"] / 1e3) / 1e9, "unit": "GB/s",
+        "n_gpus": world, "steps": steps, "warmup": args.warmup, "ms_per_step": st["median"],
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": f"cache write of the varlen prefill's {T} new tokens, Hkv {Hkv}, D {D}, page {P}",
+                   "bytes_per_step": nbytes,
+                   "l2": f"rotating over {R} buffer sets ({R} x {nbytes / 2**20:.0f} MiB > 3 x L2)" if R > 1
+                   else "bytes per step > 3 x L2",
+                   "timed_region": f"median of 20 replays of one {steps}-step graph, events as its first and last "
+                                   "nodes" if external else f"median of 20 replays of one {steps}-step graph"},
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
+                     "peak_source": f"{src} (copy bandwidth)", "kernel": "cache_write", "kernel_ms_mean": st["mean"],
+                     "kernel_ms_median": st["median"], "kernel_ms_p10": st["p10"], "kernel_ms_p90": st["p90"],
+                     "algorithmic_per_launch": nbytes, "traffic": None},
+        "gpu_launches": steps * 20,
+        "clocks": sampler.summary(t0, t1, "the timed replays"),
+    }
+    del sets, g
+    torch.cuda.empty_cache()
+    return rec
+
+
 def _brief(rec):
     """The figures of a sub-record that a reader compares across workloads."""
     keep = ("metric", "value", "unit", "steps", "warmup", "ms_per_step", "hbm_frac_step", "tensor_frac_step",
@@ -946,6 +1063,7 @@ def run_ours(args):
                 continue
             rec, _ = measure(cfg, args, dev, rank, world, local, warmup=args.warmup, region_s=0.5)
             subs[cfg] = _brief(rec)
+        subs["cache_write"] = _brief(measure_cache_write(args, dev, rank, world, local))
         cfg, L = LAYERS_SUB
         rec, identical = measure_layers(cfg, L, args, dev, rank, world, local)
         ok = ok and identical

@@ -15,15 +15,16 @@
 // mask bottom-right aligned ("Flash Attention in Triton"), online softmax,
 // O += P V, out = O / l.
 //
-// Warp roles (384 threads, three warpgroups), each looping over the CTA's items:
+// Warp roles (640 threads at D <= 128, 384 at D = 256), each looping over the
+// CTA's items:
 //   warps 0, 2  TMA producers: warp 0 resolves the items and per item loads
 //               both Q tiles and the K page boxes (64 columns x 16 slots of one
-//               page and head, 128-byte swizzle) into a 3-stage K ring; warp 2
-//               the V page boxes into a 2-stage V ring, each running ahead on
-//               its own.  Block-table entries are fetched one group of 4 tiles
-//               ahead.  The one page of V that holds the sequence end is copied
-//               by plain loads with zero fill, so no slot past seq_len reaches
-//               the MMA.
+//               page and head, 128-byte swizzle) into the K ring; warp 2 the V
+//               page boxes into the V ring, each running ahead on its own.
+//               Block-table entries are fetched one group of 4 tiles ahead.
+//               The one page of V that holds the sequence end is copied by
+//               plain loads with zero fill, so no slot past seq_len reaches the
+//               MMA.
 //   warp 1      allocates all 512 TMEM columns (S and O of each tile); its lane 0
 //               issues the MMAs in the order
 //                   O_A += P_A(j) V(j),  S_A(j+1) = Q_A K(j+1)^T,
@@ -33,14 +34,18 @@
 //               last 64 columns of its tile's S; the MMA that next overwrites S
 //               is issued after the P V that reads it, and tcgen05 operations of
 //               one thread execute in issue order.
-//   (warp 3 idle; warpgroup 0 gives registers to the softmax warpgroups)
-//   warps 4-7   softmax of tile A, warps 8-11 softmax of tile B: one thread per
-//               row (TMEM lane).  The whole S row is loaded from TMEM at once,
-//               masked, its max taken in log2 units, and P = 2^(x - m) stored
-//               straight into TMEM as bf16 in four stores of 32 keys with one
-//               wait; the normaliser l sums those same bf16 values.  The
-//               running max is only moved (and O in TMEM rescaled) when the row
-//               max grows by more than 2^8; the final O / l is exact either way.
+//   (warp 3 idle)
+//   softmax     one thread per row (TMEM lane).  At D <= 128 each tile's rows are
+//               shared by two warps per lane quarter, 64 key columns each (warps
+//               4-7 / 8-11: columns 0-63 of tile A / B, warps 12-15 / 16-19:
+//               columns 64-127), which exchange their row maxima through shared
+//               memory; at D = 256 warps 4-7 hold whole 128-column rows of the
+//               single tile.  S is loaded from TMEM at once, masked, its max taken
+//               in log2 units, and P = 2^(x - m) stored straight into TMEM as
+//               bf16 with one wait; the normaliser l sums those same bf16
+//               values.  The running max is only moved (and O in TMEM rescaled)
+//               when the row max grows by more than 2^8; the final O / l is
+//               exact either way.
 // Every wait on an mbarrier is bounded (2 s); on timeout the CTA records
 // kDevWaitTimeout, stops all roles, drains the MMAs it issued, frees TMEM and
 // exits.

@@ -513,3 +513,48 @@ def test_launch_only_writes_one_kernels_rows():
         got = out.cpu()
         assert torch.equal(got[mine].view(torch.int16), full[mine].view(torch.int16)), only
         assert torch.isnan(got[~mine].float()).all(), only
+
+
+def test_back_to_back_calls_see_the_previous_output():
+    """Two decode calls in a row on one stream, the second reading the first's
+    output as its queries: the second call (scheduled early by programmatic
+    dependent launch) must not read q before the first call has written it.
+    Eager and in a CUDA graph, against the same two calls with a device
+    synchronisation between them."""
+    b = W.llama_decode(8192, seed=82)
+    d = b.to("cuda")
+    pl = pa.plan_for(d.q, d.k_cache, d.block_table, d.seq_lens)
+    assert pl["decode_ctas"] <= torch.cuda.get_device_properties(0).multi_processor_count
+    mid = torch.empty_like(d.q)
+    ref = torch.empty_like(d.q)
+    pa.forward(d.q, d.k_cache, d.v_cache, d.block_table, d.seq_lens, d.query_start_loc, mid, scale=b.scale)
+    torch.cuda.synchronize()
+    pa.forward(mid, d.k_cache, d.v_cache, d.block_table, d.seq_lens, d.query_start_loc, ref, scale=b.scale)
+    torch.cuda.synchronize()
+    s = torch.cuda.Stream()
+    pa.prepare(d.q, d.k_cache, d.block_table, d.seq_lens, stream=s)
+    torch.cuda.synchronize()
+    for mode in ("eager", "graph"):
+        mid.fill_(float("nan"))
+        out = torch.full_like(d.q, float("nan"))
+
+        def two_calls():
+            pa.forward(d.q, d.k_cache, d.v_cache, d.block_table, d.seq_lens, d.query_start_loc, mid, scale=b.scale,
+                       stream=s)
+            pa.forward(mid, d.k_cache, d.v_cache, d.block_table, d.seq_lens, d.query_start_loc, out, scale=b.scale,
+                       stream=s)
+
+        if mode == "eager":
+            with torch.cuda.stream(s):
+                two_calls()
+        else:
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=s):
+                two_calls()
+            mid.fill_(float("nan"))
+            torch.cuda.synchronize()
+            with torch.cuda.stream(s):
+                g.replay()
+        s.synchronize()
+        assert pa.device_error(s) == 0
+        assert torch.equal(out.view(torch.int16), ref.view(torch.int16)), mode
