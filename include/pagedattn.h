@@ -54,7 +54,11 @@
  * stream before the call happens before both kernels, work enqueued after it
  * after both, and a capture records the fork and the join (pa_prepare creates
  * that stream; a call captured without it launches both kernels on the given
- * stream, one after the other).
+ * stream, one after the other).  A decode grid of at most one CTA per SM is
+ * launched with programmatic dependent launch: its CTAs may be scheduled while
+ * the previous kernel on the stream finishes, but they wait for that kernel to
+ * complete (griddepcontrol.wait) before any memory access, so the ordering
+ * above holds.
  *
  * Scratch memory.  Splitting a long key range needs a workspace of
  * pa_plan(...).workspace_bytes bytes, which the library allocates and caches per
