@@ -57,7 +57,7 @@ def draw_case(seed):
     return q_lens, seq_lens, Hq, Hkv, D, opts
 
 
-@pytest.mark.parametrize("seed", range(256))
+@pytest.mark.parametrize("seed", range(1024))
 def test_random_case(seed):
     q_lens, seq_lens, Hq, Hkv, D, opts = draw_case(1000 + seed)
     b = W.make_batch(q_lens, seq_lens, Hq, Hkv, D, seed=2000 + seed, max_pages=(max(seq_lens) + 15) // 16 + 3)
