@@ -478,29 +478,54 @@ __global__ void __launch_bounds__(kWarps * 32, (kWarps == 4 && D <= 128) ? 3 : 1
     cp_async_wait<0>();
     __syncthreads();
 
-    // Merge the warps' partial softmax states in shared memory.
+    // Merge the warps' partial softmax states in shared memory into this CTA's
+    // (O, m, l) for each row r: M = max over the warps of m_w; each warp scales
+    // its O_w and l_w by 2^(m_w - M) in registers (one exponential per row and
+    // thread); O and l are the sums of the scaled partials.
     constexpr int kMS = Tile::kMS;
-    constexpr int kM0 = kRows * kMS;  // m[16], then l[16], after the O rows
+    constexpr int kM0 = kRows * kMS;  // m[16], then the scaled l[16], after the O rows
     float* mw = reinterpret_cast<float*>(smem) + warp * Tile::kMergeWarpFloats;
-#pragma unroll
-    for (int i = 0; i < D / 8; ++i) {
-        const int c = i * 8 + 2 * tq;
-        *reinterpret_cast<float2*>(mw + g * kMS + c) = make_float2(o[i][0], o[i][1]);
-        *reinterpret_cast<float2*>(mw + (g + 8) * kMS + c) = make_float2(o[i][2], o[i][3]);
-    }
+    const float* ms = reinterpret_cast<const float*>(smem);
     l_lo = quad_sum(l_lo);
     l_hi = quad_sum(l_hi);
     if (tq == 0) {
         mw[kM0 + g] = m_lo;
         mw[kM0 + g + 8] = m_hi;
-        mw[kM0 + kRows + g] = l_lo;
-        mw[kM0 + kRows + g + 8] = l_hi;
     }
     __syncthreads();
-
-    // This CTA's (O, m, l) for row r: over the warps, M = max m_w, then
-    // O = sum 2^(m_w - M) O_w and l likewise.
-    const float* ms = reinterpret_cast<const float*>(smem);
+    auto row_max = [&](int r) {
+        float M = -INFINITY;
+#pragma unroll
+        for (int w = 0; w < kWarps; ++w) M = fmaxf(M, ms[w * Tile::kMergeWarpFloats + kM0 + r]);
+        return M;
+    };
+    {
+        const float sc_lo = m_lo == -INFINITY ? 0.f : fast_exp2(m_lo - row_max(g));
+        const float sc_hi = m_hi == -INFINITY ? 0.f : fast_exp2(m_hi - row_max(g + 8));
+        if (row_lo) {
+#pragma unroll
+            for (int i = 0; i < D / 8; ++i)
+                *reinterpret_cast<float2*>(mw + g * kMS + i * 8 + 2 * tq) =
+                    make_float2(o[i][0] * sc_lo, o[i][1] * sc_lo);
+        }
+        if (row_hi) {  // (no lane of the CTA has one when rows <= 8)
+#pragma unroll
+            for (int i = 0; i < D / 8; ++i)
+                *reinterpret_cast<float2*>(mw + (g + 8) * kMS + i * 8 + 2 * tq) =
+                    make_float2(o[i][2] * sc_hi, o[i][3] * sc_hi);
+        }
+        if (tq == 0) {
+            mw[kM0 + kRows + g] = l_lo * sc_lo;
+            mw[kM0 + kRows + g + 8] = l_hi * sc_hi;
+        }
+    }
+    __syncthreads();
+    auto row_sum = [&](int r) {
+        float l = 0.f;
+#pragma unroll
+        for (int w = 0; w < kWarps; ++w) l += ms[w * Tile::kMergeWarpFloats + kM0 + kRows + r];
+        return l;
+    };
     // Cluster mode: CTA c of the cluster owns columns [c * cols, (c + 1) * cols)
     // and receives every CTA's partial of them.
     const int C = a.splits;
@@ -508,35 +533,40 @@ __global__ void __launch_bounds__(kWarps * 32, (kWarps == 4 && D <= 128) ? 3 : 1
     float* recv_o = reinterpret_cast<float*>(smem + Tile::kSmemBytes);  // [src][16][ccols]
     float* recv_ml = recv_o + Tile::kRecvOFloats;                        // [src][16][2]
     if (clustered) cluster_wait();  // every peer has started: its receive area exists
-    for (int i = threadIdx.x; i < rows * D; i += blockDim.x) {
-        const int r = i / D, d = i % D;
-        float M = -INFINITY;
-#pragma unroll
-        for (int w = 0; w < kWarps; ++w) M = fmaxf(M, ms[w * Tile::kMergeWarpFloats + kM0 + r]);
-        float acc = 0.f, l = 0.f;
+    // One item: row r, columns d .. d + 3.
+    for (int i = threadIdx.x; i < rows * (D / 4); i += blockDim.x) {
+        const int r = i / (D / 4), d = (i % (D / 4)) * 4;
+        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
         for (int w = 0; w < kWarps; ++w) {
-            const float* mwr = ms + w * Tile::kMergeWarpFloats;
-            const float mwv = mwr[kM0 + r];
-            const float sc = mwv == -INFINITY ? 0.f : fast_exp2(mwv - M);
-            acc += sc * mwr[r * kMS + d];
-            l += sc * mwr[kM0 + kRows + r];
+            const float4 v = *reinterpret_cast<const float4*>(ms + w * Tile::kMergeWarpFloats + r * kMS + d);
+            acc.x += v.x;
+            acc.y += v.y;
+            acc.z += v.z;
+            acc.w += v.w;
         }
+        const float av[4] = {acc.x, acc.y, acc.z, acc.w};
         if (clustered) {
-            const int own = d / ccols;
-            st_peer(recv_o + (s * kRows + r) * ccols + (d - own * ccols), own, acc);
-            if (d == 0)
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                const int own = (d + j) / ccols;
+                st_peer(recv_o + (s * kRows + r) * ccols + (d + j - own * ccols), own, av[j]);
+            }
+            if (d == 0) {
+                const float M = row_max(r), l = row_sum(r);
                 for (int c = 0; c < C; ++c) st_peer2(recv_ml + (s * kRows + r) * 2, c, M, l);
+            }
         } else if (nsplits == 1) {
-            out[(static_cast<int64_t>(q0 + tok_of(r)) * a.num_q_heads + head_of(r)) * D + d] =
-                __float2bfloat16(acc / l);
+            const float inv = 1.f / row_sum(r);
+            uint2 packed;
+            packed.x = pack_bf16(av[0] * inv, av[1] * inv);
+            packed.y = pack_bf16(av[2] * inv, av[3] * inv);
+            *reinterpret_cast<uint2*>(out + (static_cast<int64_t>(q0 + tok_of(r)) * a.num_q_heads + head_of(r)) * D +
+                                      d) = packed;
         } else {
             const int64_t slot = partial_row(a, b, s, tok_of(r), head_of(r));
-            a.ws_o[slot * D + d] = acc;
-            if (d == 0) {
-                a.ws_ml[slot * 2] = M;
-                a.ws_ml[slot * 2 + 1] = l;
-            }
+            *reinterpret_cast<float4*>(a.ws_o + slot * D + d) = acc;
+            if (d == 0) *reinterpret_cast<float2*>(a.ws_ml + slot * 2) = make_float2(row_max(r), row_sum(r));
         }
     }
 
