@@ -95,6 +95,8 @@ def parse_args(argv=None):
     ap.add_argument("--seed", type=int, default=0)
     ap.add_argument("--kv-chunk", type=int, default=0, help="override the tuned split size (sweeps)")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-early-metadata", action="store_true",
+                    help="every call waits for the previous kernel before reading its metadata (pa_options)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-sub-records", action="store_true", help="headline workload only")
     ap.add_argument("--cpu-seconds", type=float, default=10.0, help="target CPU time of the oracle leg")
@@ -388,11 +390,12 @@ class Workload:
     """One workload on the device: the batch, R rotating KV pool copies, the
     output, a stream, the launch plan and the forward call."""
 
-    def __init__(self, config, seed, dev, kv_chunk=0):
+    def __init__(self, config, seed, dev, kv_chunk=0, early=1):
         import torch
         import paged_kv_cache_forward_gb300 as pa
         from paged_kv_cache_forward_gb300 import workloads as W
         self.pa, self.torch, self.config, self.dev, self.kv_chunk = pa, torch, config, dev, kv_chunk
+        self.early = early  # pa_options.early_metadata: the metadata is the same for every call
         self.batch = W.CONFIGS[config](seed=seed)
         self.work = work_of(self.batch)
         props = torch.cuda.get_device_properties(dev)
@@ -418,7 +421,7 @@ class Workload:
         d = self.d
         self.pa.forward(d.q, self.ks[i % self.R], self.vs[i % self.R], d.block_table, d.seq_lens, d.query_start_loc,
                         self.out if out is None else out, scale=self.batch.scale, kv_chunk=self.kv_chunk,
-                        events=events, stream=self.stream, launch_only=launch_only)
+                        events=events, stream=self.stream, launch_only=launch_only, early_metadata=self.early)
 
     def graph(self, n, fn):
         g = self.torch.cuda.CUDAGraph()
@@ -524,7 +527,8 @@ def time_e2e(wl, world, est_ms):
 
     def e2e_step(i):
         dbuf.copy_(hbuf, non_blocking=True)
-        pa.forward(eq, ks[i % R], vs[i % R], ebt, esl, eqsl, out, scale=b.scale, kv_chunk=wl.kv_chunk, stream=stream)
+        pa.forward(eq, ks[i % R], vs[i % R], ebt, esl, eqsl, out, scale=b.scale, kv_chunk=wl.kv_chunk, stream=stream,
+                   early_metadata=wl.early)
         hout.copy_(out, non_blocking=True)
 
     def timed(fn, reps):
@@ -587,7 +591,7 @@ def time_e2e(wl, world, est_ms):
                 stream.wait_event(ev_out[k])  # out k copied out by step i-2
             qv, btv, slv, qslv = arenas[k]
             pa.forward(qv, ks[i % R], vs[i % R], btv, slv, qslv, outs2[k], scale=b.scale,
-                       kv_chunk=wl.kv_chunk, stream=stream)
+                       kv_chunk=wl.kv_chunk, stream=stream, early_metadata=wl.early)
             ev_fwd[k] = torch.cuda.Event()
             ev_fwd[k].record(stream)
             with torch.cuda.stream(cs_out):
@@ -626,7 +630,7 @@ def measure(config, args, dev, rank, world, local, steps=None, warmup=None, with
     """One workload's record: timed region, kernel roofline, e2e, clocks."""
     import torch
     torch.cuda.synchronize(dev)
-    wl = Workload(config, rank_seed(args.seed, rank), dev, args.kv_chunk)
+    wl = Workload(config, rank_seed(args.seed, rank), dev, args.kv_chunk, early=0 if args.no_early_metadata else 1)
     work, pa, stream = wl.work, wl.pa, wl.stream
     metric, unit, _ = metric_of(config)
     W_req = args.warmup if warmup is None else warmup
@@ -771,6 +775,7 @@ def measure(config, args, dev, rank, world, local, steps=None, warmup=None, with
             "kv_chunk": wl.plan["kv_chunk"], "splits": wl.plan["splits"],
             "decode_variant": f"{wl.plan['decode_warps']} warps x {wl.plan['decode_stages']} stages, "
                               f"cluster {wl.plan['decode_cluster']}",
+            "early_metadata": bool(wl.early),
             "parallelism": f"dp{world}" if world > 1 else "single GPU",
         },
         "tok_s": total_tokens * steps / (region_ms_max / 1e3),
@@ -823,7 +828,8 @@ def measure_layers(config, L, args, dev, rank, world, local, steps=50):
 
     def layer(i):
         pa.forward(qs[i], ks[i], vs[i], d.block_table, d.seq_lens, d.query_start_loc, outs[i],
-                   scale=batch.scale, kv_chunk=args.kv_chunk, stream=stream)
+                   scale=batch.scale, kv_chunk=args.kv_chunk, stream=stream,
+                   early_metadata=0 if args.no_early_metadata else 1)
 
     def model_step():
         for i in range(L):
@@ -888,7 +894,7 @@ def measure_layers(config, L, args, dev, rank, world, local, steps=50):
         "config": {
             "workload": f"{L} layers x {config}: {DESCRIPTIONS.get(config, '')}",
             "layers": L, "kv_bytes_per_step": int(total_kv), "kv_chunk": plan["kv_chunk"],
-            "splits": plan["splits"],
+            "splits": plan["splits"], "early_metadata": not args.no_early_metadata,
             "l2": f"KV bytes per step {total_kv / 2**20:.0f} MiB (> 3 x L2)" if total_kv > 3 * (128 << 20)
             else f"KV bytes per step {total_kv / 2**20:.0f} MiB (<= 3 x L2)",
             "parallelism": f"dp{world}" if world > 1 else "single GPU",

@@ -58,7 +58,11 @@
  * launched with programmatic dependent launch: its CTAs may be scheduled while
  * the previous kernel on the stream finishes, but they wait for that kernel to
  * complete (griddepcontrol.wait) before any memory access, so the ordering
- * above holds.
+ * above holds.  Only after that wait does the decode kernel let the next kernel
+ * on the stream be scheduled early, so a kernel that starts early never runs
+ * beside anything but the one kernel immediately before it.  The one exception
+ * is opt-in: with pa_options.early_metadata the decode kernel reads the
+ * metadata (and prefetches its first KV pages into L2) before that wait.
  *
  * Scratch memory.  Splitting a long key range needs a workspace of
  * pa_plan(...).workspace_bytes bytes, which the library allocates and caches per
@@ -139,6 +143,21 @@ typedef struct {
        decode kernel, 2 only the prefill kernel (rows of the other kind are then
        not written).  Other values are PA_ERR_INVALID_ARG. */
     int32_t launch_only;
+    /* 1: the caller guarantees that block_table, seq_lens and query_start_loc
+       are not written by the kernel immediately before this call on the stream
+       (as in the attention layers of one decode step, which share the
+       metadata; work enqueued earlier than that kernel, host copies included,
+       is always finished by then).  A decode kernel launched with programmatic
+       dependent launch (see "Streams and graphs") then loads its metadata and
+       block-table entries, and prefetches the first KV pages of each warp into
+       L2, while that kernel is still finishing; q, the KV values it computes
+       with, and every write still wait for it.  A prefetch only warms L2, so a
+       KV page that kernel writes is still read after the write.  Breaking the
+       guarantee gives wrong rows (a stale length or page id), never an access
+       outside the buffers: page ids and lengths are bounds-checked as always.
+       0: every access waits (the default).  Other values are
+       PA_ERR_INVALID_ARG. */
+    int32_t early_metadata;
 } pa_options;
 
 /* What a call with these dims launches (host-only; no device work). */

@@ -69,6 +69,7 @@ class Options(ctypes.Structure):
         ("prefill_stop_event", ctypes.c_void_p),
         ("test_stall_prefill", ctypes.c_int32),
         ("launch_only", ctypes.c_int32),
+        ("early_metadata", ctypes.c_int32),
     ]
 
 
@@ -184,9 +185,11 @@ def _check_tensors(q, k_cache, v_cache, block_table, seq_lens, query_start_loc, 
 
 
 def options(kv_chunk: int = 0, events=None, decode_stages: int = 0, decode_warps: int = 0,
-            decode_cluster: int = 0, test_stall_prefill: int = 0, launch_only: int = 0) -> Options:
+            decode_cluster: int = 0, test_stall_prefill: int = 0, launch_only: int = 0,
+            early_metadata: int = 0) -> Options:
     o = Options()
     o.launch_only = launch_only
+    o.early_metadata = early_metadata
     o.kv_chunk = kv_chunk
     o.decode_stages = decode_stages
     o.decode_warps = decode_warps
@@ -204,15 +207,16 @@ def options(kv_chunk: int = 0, events=None, decode_stages: int = 0, decode_warps
 def forward(q, k_cache, v_cache, block_table, seq_lens, query_start_loc, out=None,
             scale: Optional[float] = None, kv_chunk: int = 0, events=None, stream=None,
             decode_stages: int = 0, decode_warps: int = 0, decode_cluster: int = 0,
-            test_stall_prefill: int = 0, launch_only: int = 0) -> torch.Tensor:
+            test_stall_prefill: int = 0, launch_only: int = 0, early_metadata: int = 0) -> torch.Tensor:
     """Paged attention forward (pa_forward).  Returns ``out`` ([T, Hq, D] bf16).
 
     ``events`` (optional) maps decode_start_event / decode_stop_event /
     prefill_start_event / prefill_stop_event to torch.cuda.Event objects, recorded
     around the corresponding kernels on the stream.  ``test_stall_prefill``
     (tests only) makes a wait of the prefill kernel run out; ``launch_only``
-    (timing and tests) launches only the decode (1) or the prefill (2) kernel
-    (pa_options).
+    (timing and tests) launches only the decode (1) or the prefill (2) kernel;
+    ``early_metadata`` promises that the metadata is not written by the kernel
+    just before the call (pa_options).
     """
     if out is None:
         out = torch.empty_like(q)
@@ -224,9 +228,10 @@ def forward(q, k_cache, v_cache, block_table, seq_lens, query_start_loc, out=Non
     s = _stream_handle(stream)
     args = (_ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(block_table), _ptr(seq_lens), _ptr(query_start_loc),
             _ptr(out), ctypes.c_float(scale), ctypes.byref(dims))
-    if kv_chunk or events or decode_stages or decode_warps or decode_cluster or test_stall_prefill or launch_only:
+    if (kv_chunk or events or decode_stages or decode_warps or decode_cluster or test_stall_prefill or launch_only
+            or early_metadata):
         opts = options(kv_chunk, events, decode_stages, decode_warps, decode_cluster, test_stall_prefill,
-                       launch_only)
+                       launch_only, early_metadata)
         _check(lib.pa_forward_ex(*args, ctypes.byref(opts), s))
     else:
         _check(lib.pa_forward(*args, s))

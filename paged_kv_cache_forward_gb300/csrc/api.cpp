@@ -129,6 +129,8 @@ pa_status make_plan(const pa_dims* d, const pa_options* o, Plan* p) {
     if (o && (o->kv_chunk || o->decode_cluster)) cluster = o->decode_cluster > 1 ? o->decode_cluster : 1;
     if (o && o->kv_chunk && o->decode_cluster > 1)
         return fail(PA_ERR_INVALID_ARG, "kv_chunk and decode_cluster > 1 are exclusive (a cluster deals the pages round-robin)");
+    if (o && (o->early_metadata < 0 || o->early_metadata > 1))
+        return fail(PA_ERR_INVALID_ARG, "early_metadata %d is not 0 or 1", o->early_metadata);
     if (o && (o->launch_only < 0 || o->launch_only > 2))
         return fail(PA_ERR_INVALID_ARG, "launch_only %d is not 0, 1 or 2", o->launch_only);
     if (o && (o->decode_cluster < 0 || o->decode_cluster > kMaxDecodeCluster))
@@ -159,6 +161,7 @@ pa_status make_plan(const pa_dims* d, const pa_options* o, Plan* p) {
     a.decode_stages = stages;
     a.decode_warps = warps;
     a.test_stall_prefill = o ? o->test_stall_prefill : 0;
+    a.early_metadata = o ? o->early_metadata : 0;
     p->kv_chunk = a.kv_chunk;
     p->splits = a.splits;
     p->row_groups = a.row_groups;

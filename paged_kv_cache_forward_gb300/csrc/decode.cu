@@ -229,6 +229,24 @@ __device__ __forceinline__ void st_peer2(float* local, uint32_t peer, float x, f
     asm volatile("st.shared::cluster.v2.f32 [%0], {%1, %2};\n" ::"r"(remote), "f"(x), "f"(y) : "memory");
 }
 
+// The keys of CTA split s of a sequence of L keys: its npages pages (the CTA's
+// k-th page is p0 + pstep * k) hold keys below `end`; npages = 0: none.
+__device__ __forceinline__ void split_pages(const Args& a, int s, int L, bool clustered, int& end, int& npages) {
+    if (clustered) {
+        const int pages_b = (L + kPage - 1) / kPage;
+        end = L;
+        npages = pages_b > s ? (pages_b - s + a.splits - 1) / a.splits : 0;  // 0: an empty CTA of the cluster
+    } else {
+        const int start = s * a.kv_chunk;
+        end = min(L, start + a.kv_chunk);
+        npages = start < L ? (end - start + kPage - 1) / kPage : 0;
+    }
+}
+
+__device__ __forceinline__ void prefetch_l2(const void* p) {
+    asm volatile("prefetch.global.L2 [%0];\n" ::"l"(p));
+}
+
 // 4-warp CTAs are sized to share an SM three at a time (at most 170 registers),
 // except at D = 256, whose O fragments alone take 128 registers a thread.
 template <int D, int kWarps, int kStages>
@@ -236,7 +254,11 @@ __global__ void __launch_bounds__(kWarps * 32, (kWarps == 4 && D <= 128) ? 3 : 1
     decode_splitkv_kernel(const Args a) {
     using Tile = DecodeTile<D, kWarps, kStages>;
     extern __shared__ __align__(128) uint8_t smem[];
-    grid_dependency_sync();  // (no memory access before this point)
+    // Without early_metadata no memory is accessed before the previous kernel
+    // on the stream has completed; with it, only the metadata loads and the L2
+    // prefetches below come first (see pa_options.early_metadata).
+    const bool early = a.early_metadata != 0;
+    if (!early) grid_dependency_wait();
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
     const int g = lane >> 2;   // MMA group id: row g and g + 8
@@ -274,6 +296,34 @@ __global__ void __launch_bounds__(kWarps * 32, (kWarps == 4 && D <= 128) ? 3 : 1
     const int q0 = ldg_s32(a.query_start_loc + b);
     const int q1 = ldg_s32(a.query_start_loc + b + 1);
     int L = ldg_s32(a.seq_lens + b);
+    const __nv_bfloat16* kc = reinterpret_cast<const __nv_bfloat16*>(a.k_cache);
+    const __nv_bfloat16* vc = reinterpret_cast<const __nv_bfloat16*>(a.v_cache);
+    if (early) {
+        // While the previous kernel finishes: warm L2 with the K and V rows of
+        // this warp's first kStages pages (reads only; every check that may
+        // write or leave comes after the wait).
+        const int n0 = q1 - q0, Lp = min(L, a.max_pages * kPage);
+        if (n0 >= 1 && n0 <= a.decode_max_q && Lp >= n0) {
+            int end0, np0;
+            split_pages(a, s, Lp, clustered, end0, np0);
+            const int mine = warp < np0 ? (np0 - warp + kWarps - 1) / kWarps : 0;
+            constexpr int kLines = D / 64;  // 128-byte lines per row of one KV head
+            for (int k = 0; k < kStages && k < mine; ++k) {
+                const int page = __shfl_sync(0xffffffffu, bt_cur, k);
+                const int valid = min(kPage, end0 - (p0 + pstep * (warp + kWarps * k)) * kPage);
+                if (static_cast<uint32_t>(page) < static_cast<uint64_t>(a.num_blocks)) {
+                    for (int i = lane; i < valid * kLines; i += 32) {
+                        const int64_t off =
+                            ((static_cast<int64_t>(page) * kPage + i / kLines) * a.num_kv_heads + h) * D + (i % kLines) * 64;
+                        prefetch_l2(kc + off);
+                        prefetch_l2(vc + off);
+                    }
+                }
+            }
+        }
+        grid_dependency_wait();
+    }
+    grid_launch_dependents();
     const int n = q1 - q0;
     if (n < 1 || n > a.decode_max_q) return;  // empty, or the prefill kernel's
     if (q0 < 0 || static_cast<int64_t>(q0) + n > a.num_tokens) {
@@ -308,19 +358,10 @@ __global__ void __launch_bounds__(kWarps * 32, (kWarps == 4 && D <= 128) ? 3 : 1
     }
     // This CTA's pages (npages of them, page p0 + pstep * k for k < npages) hold
     // keys below `end`.
-    int end, nsplits, npages;
-    if (clustered) {
-        const int pages_b = (L + kPage - 1) / kPage;
-        end = L;
-        npages = pages_b > s ? (pages_b - s + a.splits - 1) / a.splits : 0;  // 0: an empty CTA of the cluster
-        nsplits = a.splits;
-    } else {
-        const int start = s * a.kv_chunk;
-        if (start >= L) return;
-        end = min(L, start + a.kv_chunk);
-        npages = (end - start + kPage - 1) / kPage;
-        nsplits = (L + a.kv_chunk - 1) / a.kv_chunk;
-    }
+    int end, npages;
+    split_pages(a, s, L, clustered, end, npages);
+    if (!clustered && npages == 0) return;  // past the end of the sequence
+    const int nsplits = clustered ? a.splits : (L + a.kv_chunk - 1) / a.kv_chunk;
     const int my_pages = warp < npages ? (npages - warp + kWarps - 1) / kWarps : 0;
     if (clustered) cluster_arrive_relaxed();  // waited for before the first push to a peer
 
@@ -341,8 +382,6 @@ __global__ void __launch_bounds__(kWarps * 32, (kWarps == 4 && D <= 128) ? 3 : 1
     const int lim_lo = L - n + (row_lo ? tok_of(g) : 0);      // last key row g may see
     const int lim_hi = L - n + (row_hi ? tok_of(g + 8) : 0);
 
-    const __nv_bfloat16* kc = reinterpret_cast<const __nv_bfloat16*>(a.k_cache);
-    const __nv_bfloat16* vc = reinterpret_cast<const __nv_bfloat16*>(a.v_cache);
     const uint32_t wbase = smem_u32(smem) + warp * Tile::kWarpBytes;
     const uint64_t policy = policy_evict_first();
 

@@ -45,6 +45,7 @@ struct Args {
                              // thread-block cluster of this many CTAs (== splits), merged
                              // through distributed shared memory; 1: merged through ws
     int32_t test_stall_prefill;  // tests only: see pa_options
+    int32_t early_metadata;      // decode: metadata loads and KV prefetch before the PDL wait
     float scale;         // softmax scale
     float scale_log2;    // scale * log2(e)
 };
@@ -128,11 +129,15 @@ cudaError_t launch_kernel(void (*kernel)(KArgs...), unsigned grid, unsigned bloc
     return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
 }
 
-// The first statements of a kernel launched with pdl: let the next kernel on
-// the stream be scheduled, then wait until the previous one has completed.
-__device__ __forceinline__ void grid_dependency_sync() {
+// Programmatic dependent launch, device side.  grid_dependency_wait returns
+// once the previous kernel on the stream has completed and its writes are
+// visible (at once when the kernel was not launched with pdl).
+// grid_launch_dependents lets the next kernel on the stream be scheduled; a
+// kernel calls it only after its own wait, so that a kernel scheduled early
+// runs beside its immediate predecessor alone, never beside an older one.
+__device__ __forceinline__ void grid_dependency_wait() { asm volatile("griddepcontrol.wait;\n" ::: "memory"); }
+__device__ __forceinline__ void grid_launch_dependents() {
     asm volatile("griddepcontrol.launch_dependents;\n" ::: "memory");
-    asm volatile("griddepcontrol.wait;\n" ::: "memory");
 }
 
 // Sets the calling thread's pa_last_error() text.

@@ -180,3 +180,16 @@ def test_cache_write_rejects_before_cuda(lib):
     assert lib.pa_cache_write(None, None, None, None, None, ctypes.byref(d), None) == B.PA_OK
     d = B.CacheDims(num_tokens=4, num_blocks=8, num_kv_heads=8, head_dim=128, page_size=16)
     assert lib.pa_cache_write(None, None, None, None, None, ctypes.byref(d), None) == B.PA_ERR_INVALID_ARG
+
+
+def test_early_metadata_option(lib):
+    """pa_options.early_metadata takes 0 or 1 and does not change the plan."""
+    base = B.plan(llama_dims())
+    for v, ok in ((0, True), (1, True), (2, False), (-1, False)):
+        info = B.PlanInfo()
+        opts = B.options(early_metadata=v)
+        st = lib.pa_plan(ctypes.byref(llama_dims()), ctypes.byref(opts), ctypes.byref(info))
+        if ok:
+            assert st == B.PA_OK and info.as_dict() == base
+        else:
+            assert st == B.PA_ERR_INVALID_ARG and lib.pa_last_error().decode()

@@ -558,3 +558,98 @@ def test_back_to_back_calls_see_the_previous_output():
         s.synchronize()
         assert pa.device_error(s) == 0
         assert torch.equal(out.view(torch.int16), ref.view(torch.int16)), mode
+
+
+_EARLY_CASES = {
+    "decode_1024": lambda: W.llama_decode(1024, seed=84),
+    "decode_8192": lambda: W.llama_decode(8192, seed=85),
+    "multi_token": lambda: W.make_batch([4, 1, 2, 3], [700, 5000, 33, 1600], 32, 8, 128, seed=86),
+    "batched": lambda: W.batched_decode(seed=87),
+    "mixed": lambda: W.make_batch([300, 1, 3, 150, 1], [800, 2000, 40, 150, 9000], 32, 8, 128, seed=88),
+    "d64": lambda: W.make_batch([1, 1, 1], [3000, 17, 900], 16, 4, 64, seed=89),
+    "d256": lambda: W.make_batch([1, 2, 1], [2500, 700, 31], 16, 2, 256, seed=90),
+}
+
+
+@pytest.mark.parametrize("case", sorted(_EARLY_CASES))
+@pytest.mark.parametrize("cluster", [0, 4])
+def test_early_metadata_is_bit_identical(case, cluster):
+    """pa_options.early_metadata only moves the metadata loads (and L2 prefetches
+    of the first KV pages) ahead of the wait for the previous kernel: the output
+    equals, bit for bit, that of the same call without it, in every path (single
+    and split decode, cluster merge, multi-token decode, the mixed batch)."""
+    b = _EARLY_CASES[case]()
+    d = b.to("cuda")
+    outs = []
+    for early in (0, 1):
+        out = torch.full_like(d.q, float("nan"))
+        pa.forward(d.q, d.k_cache, d.v_cache, d.block_table, d.seq_lens, d.query_start_loc, out, scale=b.scale,
+                   decode_cluster=cluster, early_metadata=early)
+        torch.cuda.synchronize()
+        assert pa.device_error() == 0
+        outs.append(out.cpu())
+    assert torch.equal(outs[0].view(torch.int16), outs[1].view(torch.int16)), case
+    assert_close(outs[1], oracle.batch_attention(b), f"{case} cluster {cluster}")
+
+
+def test_early_metadata_still_waits_for_q_and_kv_written_just_before():
+    """With early_metadata the second of two back-to-back decode calls reads its
+    metadata while the first may still run, but q and KV values still wait:
+    here the first call's output is the second call's q and also overwrites the
+    first four rows of a KV page that the second call reads (one of the pages it
+    prefetches).  Eager and in a CUDA graph, the result equals the two calls with
+    a device synchronisation between them."""
+    b = W.llama_decode(8192, seed=91)
+    d = b.to("cuda")
+    pl = pa.plan_for(d.q, d.k_cache, d.block_table, d.seq_lens)
+    assert pl["decode_ctas"] <= torch.cuda.get_device_properties(0).multi_processor_count
+    X = int(b.block_table[0, 0])  # the first page of split 0's first warp
+    orig = d.k_cache[X].clone()
+    mid = torch.empty_like(d.q)
+    spill = d.k_cache[X, 0:4].view(1, b.num_q_heads, b.head_dim)  # 4 tokens x Hkv x D = Hq x D
+
+    def two_calls(early, stream=None):
+        pa.forward(d.q, d.k_cache, d.v_cache, d.block_table, d.seq_lens, d.query_start_loc, spill, scale=b.scale,
+                   stream=stream, early_metadata=early)
+        pa.forward(d.q, d.k_cache, d.v_cache, d.block_table, d.seq_lens, d.query_start_loc, mid, scale=b.scale,
+                   stream=stream, early_metadata=early)
+
+    def reset():
+        d.k_cache[X].copy_(orig)
+        torch.cuda.synchronize()
+
+    reset()
+    pa.forward(d.q, d.k_cache, d.v_cache, d.block_table, d.seq_lens, d.query_start_loc, spill, scale=b.scale)
+    torch.cuda.synchronize()
+    ref = torch.empty_like(d.q)
+    pa.forward(d.q, d.k_cache, d.v_cache, d.block_table, d.seq_lens, d.query_start_loc, ref, scale=b.scale)
+    torch.cuda.synchronize()
+    # the first call changed a page the second one reads, so a stale read would show
+    reset()
+    unchanged = torch.empty_like(d.q)
+    pa.forward(d.q, d.k_cache, d.v_cache, d.block_table, d.seq_lens, d.query_start_loc, unchanged, scale=b.scale)
+    torch.cuda.synchronize()
+    assert not torch.equal(unchanged.view(torch.int16), ref.view(torch.int16))
+    s = torch.cuda.Stream()
+    pa.prepare(d.q, d.k_cache, d.block_table, d.seq_lens, stream=s)
+    torch.cuda.synchronize()
+    for mode in ("eager", "graph"):
+        reset()
+        mid.fill_(float("nan"))
+        torch.cuda.synchronize()
+        if mode == "eager":
+            with torch.cuda.stream(s):
+                two_calls(1, s)
+        else:
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=s):
+                two_calls(1, s)
+            reset()
+            mid.fill_(float("nan"))
+            torch.cuda.synchronize()
+            with torch.cuda.stream(s):
+                g.replay()
+        s.synchronize()
+        assert pa.device_error(s) == 0
+        assert torch.equal(mid.view(torch.int16), ref.view(torch.int16)), mode
+    reset()
