@@ -300,16 +300,16 @@ __global__ void __launch_bounds__(kWarps * 32, (kWarps == 4 && D <= 128) ? 3 : 1
     const __nv_bfloat16* vc = reinterpret_cast<const __nv_bfloat16*>(a.v_cache);
     if (early) {
         // While the previous kernel finishes: warm L2 with the K and V rows of
-        // this warp's first kStages pages (reads only; every check that may
-        // write or leave comes after the wait).
+        // this warp's first a.prefetch_pages pages (reads only; every check
+        // that may write or leave comes after the wait).
         const int n0 = q1 - q0, Lp = min(L, a.max_pages * kPage);
         if (n0 >= 1 && n0 <= a.decode_max_q && Lp >= n0) {
             int end0, np0;
             split_pages(a, s, Lp, clustered, end0, np0);
             const int mine = warp < np0 ? (np0 - warp + kWarps - 1) / kWarps : 0;
             constexpr int kLines = D / 64;  // 128-byte lines per row of one KV head
-            for (int k = 0; k < kStages && k < mine; ++k) {
-                const int page = __shfl_sync(0xffffffffu, bt_cur, k);
+            for (int k = 0; k < a.prefetch_pages && k < mine; ++k) {  // (prefetch_pages <= 64)
+                const int page = __shfl_sync(0xffffffffu, k < 32 ? bt_cur : bt_nxt, k & 31);
                 const int valid = min(kPage, end0 - (p0 + pstep * (warp + kWarps * k)) * kPage);
                 if (static_cast<uint32_t>(page) < static_cast<uint64_t>(a.num_blocks)) {
                     for (int i = lane; i < valid * kLines; i += 32) {
@@ -691,7 +691,16 @@ cudaError_t launch_decode_d(const Args& a, cudaStream_t stream) {
     // programmatic dependent launch for grids of at most one CTA per SM (larger
     // grids would land unevenly on SMs still busy with the previous kernel)
     const bool pdl = ctas <= sms[dev & 63].load(std::memory_order_relaxed);
-    return launch_kernel(kernel, static_cast<unsigned>(ctas), kWarps * 32, smem, stream, a.decode_cluster, pdl, a);
+    // With early_metadata, a grid launched early prefetches about 256 KiB of
+    // pages per CTA while the previous kernel finishes (on the 32k-key single
+    // stream, 8 warps x 2 stages: 128 KiB 23.8 us a step, 256 KiB 22.8 us,
+    // 512 KiB 23.7 us, every page 24.4 us).  A grid launched normally starts
+    // at once, so there is nothing to overlap and it prefetches nothing.
+    Args la = a;
+    constexpr int kPrefetchPages = (256 << 10) / (kWarps * Tile::kStageBytes);
+    static_assert(kPrefetchPages >= 1 && kPrefetchPages <= 64, "prefetch depth");
+    la.prefetch_pages = (a.early_metadata && pdl) ? kPrefetchPages : 0;
+    return launch_kernel(kernel, static_cast<unsigned>(ctas), kWarps * 32, smem, stream, a.decode_cluster, pdl, la);
 }
 
 template <int D>

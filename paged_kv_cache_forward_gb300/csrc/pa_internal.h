@@ -45,7 +45,8 @@ struct Args {
                              // thread-block cluster of this many CTAs (== splits), merged
                              // through distributed shared memory; 1: merged through ws
     int32_t test_stall_prefill;  // tests only: see pa_options
-    int32_t early_metadata;      // decode: metadata loads and KV prefetch before the PDL wait
+    int32_t early_metadata;      // decode: metadata loads (and KV prefetch) before the PDL wait
+    int32_t prefetch_pages;      // decode, set at launch: pages per warp prefetched before that wait
     float scale;         // softmax scale
     float scale_log2;    // scale * log2(e)
 };

@@ -59,6 +59,7 @@ REGS_PER_SM = 65536
 REGS_PER_THREAD = 168
 VARIANTS = {64: "4x2,4x3,4x4,8x2,8x3,12x2", 128: "4x2,4x3,4x4,8x2,8x3,12x2", 256: "4x2,4x3"}
 CLUSTERS = "2,4,8,12,16"
+EARLY = 1        # pa_options.early_metadata in the timed calls (--no-early-metadata: 0)
 GROUP_CELLS = [(1, 2048), (1, 8192), (1, 32768), (8, 8192), (64, 4096)]  # (batch, bound) for --validate-groups
 GROUP_SHAPES = [(8, 8), (64, 8), (32, 1)]  # (Hq, Hkv): 1, 8 and 32 query heads per KV head
 
@@ -90,7 +91,7 @@ def time_shape(pools, stream, chunk=0, warps=0, stages=0, cluster=0, steps_per_g
     with torch.cuda.stream(stream):
         for i in range(2):
             pa.forward(q, ks[i % R], vs[i % R], bt, sl, qsl, out, kv_chunk=chunk, stream=stream,
-                       decode_stages=stages, decode_warps=warps, decode_cluster=cluster)
+                       decode_stages=stages, decode_warps=warps, decode_cluster=cluster, early_metadata=EARLY)
     stream.synchronize()
     M = max(R, (steps_per_graph // R) * R)
     # (captured directly: the torch.cuda.graph context manager also runs a
@@ -101,7 +102,7 @@ def time_shape(pools, stream, chunk=0, warps=0, stages=0, cluster=0, steps_per_g
         try:
             for i in range(M):
                 pa.forward(q, ks[i % R], vs[i % R], bt, sl, qsl, out, kv_chunk=chunk, stream=stream,
-                           decode_stages=stages, decode_warps=warps, decode_cluster=cluster)
+                           decode_stages=stages, decode_warps=warps, decode_cluster=cluster, early_metadata=EARLY)
         finally:
             g.capture_end()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
@@ -240,7 +241,11 @@ def main(argv=None):
                     help="sweep only the batch-1 cells with 1, 2 and 4 KV heads (fewer than 8 decode units)")
     ap.add_argument("--merge", action="store_true",
                     help="replace only the swept cells of the existing table and log")
+    ap.add_argument("--no-early-metadata", action="store_true",
+                    help="time calls without pa_options.early_metadata (the table is swept with it by default)")
     args = ap.parse_args(argv)
+    global EARLY
+    EARLY = 0 if args.no_early_metadata else 1
     dims = [int(x) for x in args.dims.split(",") if x]
     bounds = [int(x) for x in args.bounds.split(",")]
     clusters = [int(c) for c in args.clusters.split(",") if c]
@@ -305,7 +310,8 @@ def main(argv=None):
                 "Decode batches with 4 query heads per KV head: one sequence with 1, 2, 4 or 8 KV heads at\n"
                 "the bound, larger batches (8 KV heads) with lengths uniform in [bound/16, bound] (seeded\n"
                 "per cell); units = sequences x KV heads, the table's key,\n"
-                "graph-replayed pa_forward steps rotating over KV pool copies larger than 3 x L2.\n"
+                "graph-replayed pa_forward steps rotating over KV pool copies larger than 3 x L2,\n"
+                f"early_metadata {EARLY} (the metadata is the same for every call).\n"
                 "GB/s = KV bytes per step / step time.  Every candidate is timed once; the five fastest\n"
                 f"(marked *) {REPEATS} times, and the cell keeps the best median (its spread in brackets).\n\n"
                 "Split `cN`: the pages dealt round-robin to a thread-block cluster of N CTAs.\n\n"
