@@ -62,8 +62,8 @@ FALLBACK_BF16_TFLOPS = 1900.0
 FALLBACK_BF16_SUSTAINED = 1700.0
 CSRC = os.path.join(ROOT, "paged_kv_cache_forward_gb300", "csrc")
 KERNEL_SOURCES = {
-    "decode_splitkv": ["decode.cu", "pa_device.cuh"],
-    "prefill": ["prefill_tc.cu", "tc_device.cuh", "pa_device.cuh"],
+    "decode_splitkv": ["decode.cu", "pa_device.cuh", "pa_internal.h"],
+    "prefill": ["prefill_tc.cu", "tc_device.cuh", "pa_device.cuh", "pa_internal.h"],
 }
 DESCRIPTIONS = {
     "tiny_decode": "batch 1, 1 query token, Hq 4 / Hkv 1, head_dim 64, context 256, page 16, 16 of 64 pages",
