@@ -126,6 +126,15 @@ pa_status make_plan(const pa_dims* d, const pa_options* o, Plan* p) {
                     warps, stages, d->head_dim);
     // cluster mode: the table's, unless the caller forces a split size or a cluster
     int32_t cluster = te.decode_cluster > 1 ? te.decode_cluster : 1;
+    // The table's cells give one CTA at most 8192 * 128 / D keys of a sequence
+    // (a sequence at the bound must not leave a few CTAs streaming after the
+    // rest of the batch is done).  A bound beyond the swept ones can break that
+    // for a cluster (bound / C keys per CTA): take static splits of that size.
+    const int64_t max_keys = 8192LL * 128 / d->head_dim;
+    if (cluster > 1 && !(o && (o->kv_chunk || o->decode_cluster)) && (bound + cluster - 1) / cluster > max_keys) {
+        cluster = 1;
+        chunk = max_keys;
+    }
     if (o && (o->kv_chunk || o->decode_cluster)) cluster = o->decode_cluster > 1 ? o->decode_cluster : 1;
     if (o && o->kv_chunk && o->decode_cluster > 1)
         return fail(PA_ERR_INVALID_ARG, "kv_chunk and decode_cluster > 1 are exclusive (a cluster deals the pages round-robin)");

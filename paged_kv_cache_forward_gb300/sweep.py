@@ -71,15 +71,26 @@ def resident_ctas(warps: int, stages: int, d: int) -> int:
     return max(1, min(SMEM_PER_SM // per_cta, REGS_PER_SM // (warps * 32 * REGS_PER_THREAD)))
 
 
+def max_keys_per_cta(d: int) -> int:
+    """The most keys of one sequence a CTA may stream.  A cell's lengths cannot
+    stand for every batch with the same key: the plan only knows the bound, so a
+    sequence at the bound must not leave its few CTAs streaming long after the
+    rest of the batch is done.  8192 keys at D = 128 (4 MiB of K and V) is what
+    the GPU as a whole streams in the time one sequence at the largest bound
+    takes on its own (batch-1 cells pick 6912 keys at 131072), so a longer
+    per-CTA stream would set the step time whenever the other sequences are short."""
+    return 8192 * 128 // d
+
+
 def candidates(bound: int, units: int, sms: int, warps: int, stages: int, d: int):
     """Split sizes: powers of two, and those that give whole waves of CTAs at this
-    variant's residency."""
+    variant's residency, up to max_keys_per_cta."""
     base = {64, 128, 256, 512, 1024, 2048, 4096, 8192, 16384}
     per_sm = resident_ctas(warps, stages, d)
     for k in (1, 2, 3):
         pages = math.ceil(bound * units / (k * per_sm * sms) / PAGE)
         base.add(max(1, pages) * PAGE)
-    return sorted(c for c in base if 16 <= c <= bound)
+    return sorted(c for c in base if 16 <= c <= bound and c <= max_keys_per_cta(d))
 
 
 def time_shape(pools, stream, chunk=0, warps=0, stages=0, cluster=0, steps_per_graph=16):
@@ -126,23 +137,31 @@ def time_shape(pools, stream, chunk=0, warps=0, stages=0, cluster=0, steps_per_g
     return e0.elapsed_time(e1) * 1e3 / (reps * M)
 
 
-def seq_lengths(bound, batch):
+def seq_lengths(bound, batch, d=128, hkv=HKV):
     """One sequence at the bound; a batch has lengths uniform in [bound/16, bound]
     (as a serving batch mixes lengths; with every sequence at the bound the
-    table would favour unsplit CTAs, whose longest sequences then set the time)."""
+    table would favour unsplit CTAs, whose longest sequences then set the time).
+    Where such a batch would hold more than MAX_KV_BYTES of KV, the bound is set
+    by one long sequence and the others are a serving mix of 1024..16384 keys
+    (the shape of a mixed prefill/decode batch with one long conversation)."""
     if batch == 1:
         return [bound]
     g = torch.Generator().manual_seed(bound * 1000 + batch)
     lo = max(1, bound // 16)
-    return torch.randint(lo, bound + 1, (batch,), generator=g).tolist()
+    if batch * bound * hkv * d * 4 <= MAX_KV_BYTES:
+        return torch.randint(lo, bound + 1, (batch,), generator=g).tolist()
+    return [bound] + torch.randint(min(1024, bound), min(16384, bound) + 1, (batch - 1,), generator=g).tolist()
 
 
 def make_pools(bound, batch, d, hq, hkv, l2_bytes, gen):
+    """The inputs of one cell: a pool holding just the pages the lengths use (in
+    random order), R copies of it when one step's KV bytes fit 3 x L2."""
     pages = bound // PAGE
-    lens = seq_lengths(bound, batch)
+    lens = seq_lengths(bound, batch, d, hkv)
     kv = sum(lens) * hkv * d * 2 * 2
     R = 1 if kv > 3 * l2_bytes else int(math.ceil(3 * l2_bytes / kv)) + 1
-    nb = batch * pages + 1
+    used = [(n + PAGE - 1) // PAGE for n in lens]
+    nb = sum(used) + 1
     dev = "cuda"
     q = torch.randn(batch, hq, d, device=dev, generator=gen).to(torch.bfloat16)
     ks, vs = [], []
@@ -150,7 +169,11 @@ def make_pools(bound, batch, d, hq, hkv, l2_bytes, gen):
         ks.append(torch.randn(nb, PAGE, hkv, d, device=dev, generator=gen).to(torch.bfloat16))
         vs.append(torch.randn(nb, PAGE, hkv, d, device=dev, generator=gen).to(torch.bfloat16))
     perm = torch.randperm(nb, device=dev, generator=gen).to(torch.int32)
-    bt = perm[: batch * pages].reshape(batch, pages).contiguous()
+    bt = torch.zeros(batch, pages, dtype=torch.int32, device=dev)  # entries past a sequence are never used
+    off = 0
+    for i, u in enumerate(used):
+        bt[i, :u] = perm[off:off + u]
+        off += u
     sl = torch.tensor(lens, dtype=torch.int32, device=dev)
     qsl = torch.arange(batch + 1, dtype=torch.int32, device=dev)
     out = torch.empty_like(q)
@@ -164,7 +187,7 @@ def all_candidates(bound, units, sms, d, variants, clusters):
     out = []
     for w, st in variants:
         out += [(c, st, w, 1) for c in candidates(bound, units, sms, w, st, d)]
-        out += [(0, st, w, c) for c in clusters]
+        out += [(0, st, w, c) for c in clusters if math.ceil(bound / c) <= max_keys_per_cta(d)]
     return out
 
 
@@ -280,7 +303,7 @@ def main(argv=None):
         for batch, hkv in shapes:
             units = batch * hkv
             for bound in bounds:
-                if batch * bound * hkv * d * 4 > MAX_KV_BYTES:
+                if sum(seq_lengths(bound, batch, d, hkv)) * hkv * d * 4 > MAX_KV_BYTES:
                     continue
                 pools, kv = make_pools(bound, batch, d, 4 * hkv, hkv, l2, gen)
                 res = sweep_cell(pools, stream, all_candidates(bound, units, sms, d, variants, clusters))
@@ -309,7 +332,9 @@ def main(argv=None):
                 f"Command: `python -m paged_kv_cache_forward_gb300.sweep {' '.join(argv or sys.argv[1:])}`\n\n"
                 "Decode batches with 4 query heads per KV head: one sequence with 1, 2, 4 or 8 KV heads at\n"
                 "the bound, larger batches (8 KV heads) with lengths uniform in [bound/16, bound] (seeded\n"
-                "per cell); units = sequences x KV heads, the table's key,\n"
+                "per cell), or, where those would exceed 6 GiB of KV, one sequence at the bound and the\n"
+                "others uniform in [1024, 16384]; units = sequences x KV heads, the table's key,\n"
+                "candidates that leave at most 8192 x 128 / head_dim keys of a sequence to one CTA,\n"
                 "graph-replayed pa_forward steps rotating over KV pool copies larger than 3 x L2,\n"
                 f"early_metadata {EARLY} (the metadata is the same for every call).\n"
                 "GB/s = KV bytes per step / step time.  Every candidate is timed once; the five fastest\n"
