@@ -54,7 +54,10 @@ constexpr int32_t kMaxDecodeCluster = 16;  // largest thread-block cluster (non-
 // behaves like one Llama sequence with 8 KV heads).  Every built head dim has
 // rows ending in a catch-all; a table without the head dim would fall back to
 // its last row.
-const LutEntry& table_entry(int32_t head_dim, int64_t bound, int64_t units) {
+const LutEntry& table_entry(int32_t head_dim, int64_t bound, int64_t units, int32_t row_groups) {
+    if (row_groups > 1)  // more than 16 query heads per KV head: the wide-group cells, if swept
+        for (const LutEntry& e : kSplitTableWide)
+            if (e.head_dim == head_dim && bound <= e.max_bound && units <= e.max_units) return e;
     for (const LutEntry& e : kSplitTable)
         if (e.head_dim == head_dim && bound <= e.max_bound && units <= e.max_units) return e;
     return kSplitTable[sizeof(kSplitTable) / sizeof(kSplitTable[0]) - 1];
@@ -101,8 +104,9 @@ pa_status make_plan(const pa_dims* d, const pa_options* o, Plan* p) {
     if (st != PA_OK) return st;
     const int64_t bound = static_cast<int64_t>(d->max_pages) * d->page_size;
     const int32_t group0 = d->num_q_heads / d->num_kv_heads;
-    const LutEntry& te = table_entry(d->head_dim, bound,
-                                     static_cast<int64_t>(d->num_seqs) * d->num_kv_heads * ((group0 + 15) / 16));
+    const int32_t rgroups = (group0 + 15) / 16;
+    const LutEntry& te =
+        table_entry(d->head_dim, bound, static_cast<int64_t>(d->num_seqs) * d->num_kv_heads * rgroups, rgroups);
     int64_t chunk = (o && o->kv_chunk) ? o->kv_chunk : te.kv_chunk;
     if (chunk < d->page_size || chunk % d->page_size)
         return fail(PA_ERR_INVALID_ARG, "kv_chunk %lld must be a positive multiple of page_size",

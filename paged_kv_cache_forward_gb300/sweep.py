@@ -60,6 +60,10 @@ REGS_PER_THREAD = 168
 VARIANTS = {64: "4x2,4x3,4x4,8x2,8x3,12x2", 128: "4x2,4x3,4x4,8x2,8x3,12x2", 256: "4x2,4x3"}
 CLUSTERS = "2,4,8,12,16"
 EARLY = 1        # pa_options.early_metadata in the timed calls (--no-early-metadata: 0)
+# Wide groups (more than 16 query heads per KV head: CTAs of 16 heads, each page
+# read by every row group of its KV head) have their own cells: Hq 32 / Hkv 1.
+WIDE = {128: (32, 1, [1, 2, 4, 8, 16, 64])}  # head_dim: (Hq, Hkv, batches)
+WIDE_NAME = "kSplitTableWide"
 GROUP_CELLS = [(1, 2048), (1, 8192), (1, 32768), (8, 8192), (64, 4096)]  # (batch, bound) for --validate-groups
 GROUP_SHAPES = [(8, 8), (64, 8), (32, 1)]  # (Hq, Hkv): 1, 8 and 32 query heads per KV head
 
@@ -264,6 +268,8 @@ def main(argv=None):
                     help="sweep only the batch-1 cells with 1, 2 and 4 KV heads (fewer than 8 decode units)")
     ap.add_argument("--merge", action="store_true",
                     help="replace only the swept cells of the existing table and log")
+    ap.add_argument("--wide-only", action="store_true",
+                    help="sweep only the wide-group cells (more than 16 query heads per KV head)")
     ap.add_argument("--no-early-metadata", action="store_true",
                     help="time calls without pa_options.early_metadata (the table is swept with it by default)")
     args = ap.parse_args(argv)
@@ -289,7 +295,7 @@ def main(argv=None):
             f.write("\n".join(extra) + "\n")
         print(f"wrote {args.log}")
         return
-    best = {}
+    best, best_wide = {}, {}
     lines = {}
     for d in dims:
         batches = [int(x) for x in args.batches.split(",")] if args.batches else BATCHES[d]
@@ -300,33 +306,41 @@ def main(argv=None):
         shapes = [(1, h) for h in SUB_UNIT_KV_HEADS] if not args.batches else []
         if not args.only_sub_units:
             shapes += [(b, HKV) for b in batches]
-        for batch, hkv in shapes:
-            units = batch * hkv
+        # (batch, Hq, KV heads, wide)
+        cases = [(b, 4 * h, h, False) for b, h in shapes] if not args.wide_only else []
+        if d in WIDE and not args.only_sub_units:
+            hq_w, hkv_w, batches_w = WIDE[d]
+            cases += [(b, hq_w, hkv_w, True) for b in batches_w]
+        for batch, hq, hkv, wide in cases:
+            units = batch * hkv * ((hq // hkv + 15) // 16)
             for bound in bounds:
                 if sum(seq_lengths(bound, batch, d, hkv)) * hkv * d * 4 > MAX_KV_BYTES:
                     continue
-                pools, kv = make_pools(bound, batch, d, 4 * hkv, hkv, l2, gen)
+                pools, kv = make_pools(bound, batch, d, hq, hkv, l2, gen)
                 res = sweep_cell(pools, stream, all_candidates(bound, units, sms, d, variants, clusters))
                 us, (chunk, st, w, cl), ts = res[0]
-                best[(d, bound, units)] = (chunk, st, w, cl)
+                (best_wide if wide else best)[(d, bound, units)] = (chunk, st, w, cl)
                 row = " ".join(f"{name_of(c, k)}/{ww}x{t}:{kv / u / 1e3:.0f}" + ("*" if len(tsx) > 1 else "")
                                for u, (c, t, ww, k), tsx in sorted(res, key=lambda x: (x[1][2], x[1][1], x[1][3],
                                                                                       x[1][0])))
                 spread = f"{min(ts):.1f}-{max(ts):.1f}"
-                lines[(d, units, bound)] = (f"| {d} | {batch} x {hkv} | {units} | {bound} | {name_of(chunk, cl)} | "
-                                            f"{w}x{st} | {us:.1f} ({spread}) | {kv / us / 1e3:.0f} | {row} |")
-                print(lines[(d, units, bound)], flush=True)
+                shape = f"{batch} x {hkv}" + (f" (Hq {hq})" if wide else "")
+                key = (d, units, bound, shape)
+                lines[key] = (f"| {d} | {shape} | {units} | {bound} | {name_of(chunk, cl)} | "
+                              f"{w}x{st} | {us:.1f} ({spread}) | {kv / us / 1e3:.0f} | {row} |")
+                print(lines[key], flush=True)
                 del pools
                 torch.cuda.empty_cache()
 
     if args.merge:
-        cells, old_lines = read_table(args.out), read_log(args.log)
+        cells, cells_w, old_lines = read_table(args.out), read_table(args.out, WIDE_NAME), read_log(args.log)
         cells.update(best)
+        cells_w.update(best_wide)
         old_lines.update(lines)
-        best, lines = cells, old_lines
+        best, best_wide, lines = cells, cells_w, old_lines
     stamp = datetime.date.today().isoformat()
     if not args.no_write:
-        write_table(args.out, best, props.name, stamp)
+        write_table(args.out, best, props.name, stamp, best_wide)
     with open(args.log, "w") as f:
         f.write(f"# Split-size sweep on {props.name} ({stamp})\n\n"
                 f"Command: `python -m paged_kv_cache_forward_gb300.sweep {' '.join(argv or sys.argv[1:])}`\n\n"
@@ -335,6 +349,8 @@ def main(argv=None):
                 "per cell), or, where those would exceed 6 GiB of KV, one sequence at the bound and the\n"
                 "others uniform in [1024, 16384]; units = sequences x KV heads, the table's key,\n"
                 "candidates that leave at most 8192 x 128 / head_dim keys of a sequence to one CTA,\n"
+                "and wide-group cells (Hq 32 / Hkv 1: two row groups of 16 query heads read each page)\n"
+                "for the table's second array,\n"
                 "graph-replayed pa_forward steps rotating over KV pool copies larger than 3 x L2,\n"
                 f"early_metadata {EARLY} (the metadata is the same for every call).\n"
                 "GB/s = KV bytes per step / step time.  Every candidate is timed once; the five fastest\n"
@@ -347,33 +363,60 @@ def main(argv=None):
     print(f"wrote {args.log}" + ("" if args.no_write else f" and {args.out}"))
 
 
-def read_table(path):
-    """The cells of an existing table: {(head_dim, bound, units): (chunk, stages, warps, cluster)}
-    (the catch-all rows are dropped)."""
+def read_table(path, array="kSplitTable"):
+    """The cells of one array of an existing table: {(head_dim, bound, units):
+    (chunk, stages, warps, cluster)} (the catch-all rows and the head-dim-0 end
+    row are dropped)."""
+    m = re.search(re.escape(array) + r"\[\] = \{(.*?)\n\};", open(path).read(), re.S)
     cells = {}
-    rows = re.findall(r"\{(\d+), (\d+), (\d+), (\d+), (\d+), (\d+), (\d+)\}", open(path).read())
+    if m is None:
+        return cells
+    rows = re.findall(r"\{(\d+), (\d+), (\d+), (\d+), (\d+), (\d+), (\d+)\}", m.group(1))
     for d, bound, units, chunk, st, w, cl in rows:
-        cells[(int(d), int(bound), int(units))] = (int(chunk), int(st), int(w), int(cl))
+        if int(d):
+            cells[(int(d), int(bound), int(units))] = (int(chunk), int(st), int(w), int(cl))
     return cells
 
 
 def read_log(path):
-    """The rows of an existing sweep log: {(head_dim, units, bound): line}."""
+    """The rows of an existing sweep log: {(head_dim, units, bound, shape): line}."""
     out = {}
     if os.path.exists(path):
         for line in open(path):
-            m = re.match(r"\| (\d+) \| [^|]+ \| (\d+) \| (\d+) \|", line)
+            m = re.match(r"\| (\d+) \| ([^|]+?) \| (\d+) \| (\d+) \|", line)
             if m:
-                out[(int(m.group(1)), int(m.group(2)), int(m.group(3)))] = line.rstrip("\n")
+                out[(int(m.group(1)), int(m.group(3)), int(m.group(4)), m.group(2))] = line.rstrip("\n")
     return out
 
 
-def write_table(path, best, gpu_name, stamp):
+def _table_rows(best):
     """Rows {head_dim, max_bound, max_units, ...}: per head dim, units-major, so the
     first match is the smallest swept number of units >= the call's and, within
     it, the smallest swept bound >= the call's.  Each head dim ends with
     catch-all rows: its largest units' cells for any number of units, and that
     group's largest bound for any bound."""
+    out = []
+    for d in sorted({k[0] for k in best}):
+        cells = {k[1:]: v for k, v in best.items() if k[0] == d}
+        units = sorted({u for _, u in cells})
+        bounds = sorted({bd for bd, _ in cells})
+        row = lambda bound, mu, c: f"    {{{d}, {bound}, {mu}, {c[0] or 16}, {c[1]}, {c[2]}, {c[3]}}},\n"
+        for u in units:
+            for bound in bounds:
+                if (bound, u) in cells:
+                    out.append(row(bound, u, cells[(bound, u)]))
+        top = units[-1]
+        for bound in bounds:
+            if (bound, top) in cells:
+                out.append(row(bound, "1 << 30", cells[(bound, top)]))
+        out.append(row("1 << 30", "1 << 30", cells[max(b for b, u in cells if u == top), top]))
+    return out
+
+
+def write_table(path, best, gpu_name, stamp, best_wide=None):
+    """kSplitTable from `best`, then kSplitTableWide (calls with more than one row
+    group of 16 query heads per KV head) from `best_wide`; a head dim without wide
+    rows takes the first table (a row of head dim 0 keeps the array non-empty)."""
     with open(path, "w") as f:
         f.write("// Keys per split and decode kernel variant, keyed on the head dim, the\n"
                 "// context bound (max_pages * page_size) and the number of decode units:\n"
@@ -383,22 +426,14 @@ def write_table(path, best, gpu_name, stamp):
                 "// entry that matches wins.  Written by paged_kv_cache_forward_gb300/sweep.py on\n"
                 f"// {gpu_name} ({stamp}).\n"
                 "static const LutEntry kSplitTable[] = {\n")
-        for d in sorted({k[0] for k in best}):
-            cells = {k[1:]: v for k, v in best.items() if k[0] == d}
-            units = sorted({u for _, u in cells})
-            bounds = sorted({bd for bd, _ in cells})
-            row = lambda bound, mu, c: f"    {{{d}, {bound}, {mu}, {c[0] or 16}, {c[1]}, {c[2]}, {c[3]}}},\n"
-            for u in units:
-                for bound in bounds:
-                    if (bound, u) in cells:
-                        f.write(row(bound, u, cells[(bound, u)]))
-            top = units[-1]
-            for bound in bounds:
-                if (bound, top) in cells:
-                    f.write(row(bound, "1 << 30", cells[(bound, top)]))
-            f.write(row("1 << 30", "1 << 30", cells[max(b for b, u in cells if u == top), top]))
-        f.write("};\n")
-
+        f.writelines(_table_rows(best))
+        f.write("};\n\n"
+                "// Calls with more than 16 query heads per KV head (several row groups per KV\n"
+                "// head, each reading the same pages); a head dim without rows here takes the\n"
+                "// table above.\n"
+                f"static const LutEntry {WIDE_NAME}[] = {{\n")
+        f.writelines(_table_rows(best_wide or {}))
+        f.write("    {0, 0, 0, 0, 0, 0, 0},\n};\n")
 
 if __name__ == "__main__":
     main()
