@@ -25,20 +25,21 @@ __global__ void __launch_bounds__(kThreads) cache_write_kernel(const uint4* __re
                                                               uint4* __restrict__ k_cache, uint4* __restrict__ v_cache,
                                                               int64_t num_slots, int row_chunks, int32_t* err) {
     const int64_t t = blockIdx.x;
+    // The slot and the token's rows are loaded together (the rows do not depend
+    // on the slot), so a CTA waits for one round trip before its stores, not two.
     const int64_t s = slot_mapping[t];
-    if (s < 0) return;
-    if (s >= num_slots) {
-        if (threadIdx.x == 0) flag_error(err, kDevBadBlock);
-        return;
-    }
+    const bool ok = s >= 0 && s < num_slots;  // s < 0: a token that is not cached
+    if (s >= num_slots && threadIdx.x == 0) flag_error(err, kDevBadBlock);
     // a token row is row_chunks 16-byte chunks ([Hkv, D] bf16), contiguous in
     // both the new-token tensors and the cache (slot s is row s of the cache)
     const int64_t src = t * row_chunks, dst = s * row_chunks;
     for (int c = threadIdx.x; c < row_chunks; c += kThreads) {
         const uint4 kv = __ldcs(k_new + src + c);  // streamed: read once
         const uint4 vv = __ldcs(v_new + src + c);
-        k_cache[dst + c] = kv;
-        v_cache[dst + c] = vv;
+        if (ok) {
+            k_cache[dst + c] = kv;
+            v_cache[dst + c] = vv;
+        }
     }
 }
 
