@@ -255,8 +255,9 @@ __global__ void __launch_bounds__(kWarps * 32, (kWarps == 4 && D <= 128) ? 3 : 1
     using Tile = DecodeTile<D, kWarps, kStages>;
     extern __shared__ __align__(128) uint8_t smem[];
     // Without early_metadata no memory is accessed before the previous kernel
-    // on the stream has completed; with it, only the metadata loads and the L2
-    // prefetches below come first (see pa_options.early_metadata).
+    // on the stream has completed; with it, the metadata loads, the setup that
+    // needs only them and the L2 prefetches come first (see
+    // pa_options.early_metadata).
     const bool early = a.early_metadata != 0;
     if (!early) grid_dependency_wait();
     const int warp = threadIdx.x >> 5;
@@ -296,42 +297,27 @@ __global__ void __launch_bounds__(kWarps * 32, (kWarps == 4 && D <= 128) ? 3 : 1
     const int q0 = ldg_s32(a.query_start_loc + b);
     const int q1 = ldg_s32(a.query_start_loc + b + 1);
     int L = ldg_s32(a.seq_lens + b);
-    const __nv_bfloat16* kc = reinterpret_cast<const __nv_bfloat16*>(a.k_cache);
-    const __nv_bfloat16* vc = reinterpret_cast<const __nv_bfloat16*>(a.v_cache);
-    if (early) {
-        // While the previous kernel finishes: warm L2 with the K and V rows of
-        // this warp's first a.prefetch_pages pages (reads only; every check
-        // that may write or leave comes after the wait).
-        const int n0 = q1 - q0, Lp = min(L, a.max_pages * kPage);
-        if (n0 >= 1 && n0 <= a.decode_max_q && Lp >= n0) {
-            int end0, np0;
-            split_pages(a, s, Lp, clustered, end0, np0);
-            const int mine = warp < np0 ? (np0 - warp + kWarps - 1) / kWarps : 0;
-            constexpr int kLines = D / 64;  // 128-byte lines per row of one KV head
-            for (int k = 0; k < a.prefetch_pages && k < mine; ++k) {  // (prefetch_pages <= 64)
-                const int page = __shfl_sync(0xffffffffu, k < 32 ? bt_cur : bt_nxt, k & 31);
-                const int valid = min(kPage, end0 - (p0 + pstep * (warp + kWarps * k)) * kPage);
-                if (static_cast<uint32_t>(page) < static_cast<uint64_t>(a.num_blocks)) {
-                    for (int i = lane; i < valid * kLines; i += 32) {
-                        const int64_t off =
-                            ((static_cast<int64_t>(page) * kPage + i / kLines) * a.num_kv_heads + h) * D + (i % kLines) * 64;
-                        prefetch_l2(kc + off);
-                        prefetch_l2(vc + off);
-                    }
-                }
-            }
-        }
-        grid_dependency_wait();
-    }
-    grid_launch_dependents();
+    // With early_metadata everything below that needs only the metadata runs
+    // before the wait for the previous kernel; whatever writes or reads q or KV
+    // waits for it first (wait_prev: a second wait returns at once), and so does
+    // every exit, so that the next kernel is only scheduled once this one has
+    // passed its wait.
+    auto wait_prev = [&]() {
+        if (early) grid_dependency_wait();
+    };
     const int n = q1 - q0;
-    if (n < 1 || n > a.decode_max_q) return;  // empty, or the prefill kernel's
+    if (n < 1 || n > a.decode_max_q) {  // empty, or the prefill kernel's
+        wait_prev();
+        return;
+    }
     if (q0 < 0 || static_cast<int64_t>(q0) + n > a.num_tokens) {
+        wait_prev();
         flag_error(a.err, kDevBadQueryStart);
         return;
     }
     const int cap = a.max_pages * kPage;
     if (L > cap) {
+        wait_prev();
         flag_error(a.err, kDevSeqTooLong);
         L = cap;
     }
@@ -348,6 +334,7 @@ __global__ void __launch_bounds__(kWarps * 32, (kWarps == 4 && D <= 128) ? 3 : 1
     __nv_bfloat16* out = reinterpret_cast<__nv_bfloat16*>(a.out);
     if (L < n) {
         // A query must see at least itself; the caller broke the contract.
+        wait_prev();
         if (s == 0) {
             flag_error(a.err, kDevQueryTooLong);
             for (int i = threadIdx.x; i < rows * D; i += blockDim.x)
@@ -360,7 +347,10 @@ __global__ void __launch_bounds__(kWarps * 32, (kWarps == 4 && D <= 128) ? 3 : 1
     // keys below `end`.
     int end, npages;
     split_pages(a, s, L, clustered, end, npages);
-    if (!clustered && npages == 0) return;  // past the end of the sequence
+    if (!clustered && npages == 0) {  // past the end of the sequence
+        wait_prev();
+        return;
+    }
     const int nsplits = clustered ? a.splits : (L + a.kv_chunk - 1) / a.kv_chunk;
     const int my_pages = warp < npages ? (npages - warp + kWarps - 1) / kWarps : 0;
     if (clustered) cluster_arrive_relaxed();  // waited for before the first push to a peer
@@ -373,6 +363,8 @@ __global__ void __launch_bounds__(kWarps * 32, (kWarps == 4 && D <= 128) ? 3 : 1
 
     // Each of this thread's two rows (g, g + 8) has its own causal limit.
     const __nv_bfloat16* q = reinterpret_cast<const __nv_bfloat16*>(a.q);
+    const __nv_bfloat16* kc = reinterpret_cast<const __nv_bfloat16*>(a.k_cache);
+    const __nv_bfloat16* vc = reinterpret_cast<const __nv_bfloat16*>(a.v_cache);
     const bool row_lo = g < rows, row_hi = g + 8 < rows;
     const __nv_bfloat16* qg =
         q + (static_cast<int64_t>(q0 + (row_lo ? tok_of(g) : 0)) * a.num_q_heads + (row_lo ? head_of(g) : 0)) * D;
@@ -423,6 +415,26 @@ __global__ void __launch_bounds__(kWarps * 32, (kWarps == 4 && D <= 128) ? 3 : 1
     float m_lo = -INFINITY, m_hi = -INFINITY;  // running max (log2 units) of rows g, g+8
     float l_lo = 0.f, l_hi = 0.f;              // this thread's share of the running sums
 
+    if (early) {
+        // While the previous kernel finishes: warm L2 with the K and V rows of
+        // this warp's first a.prefetch_pages pages (a prefetch reads nothing
+        // into the SM, so a page that kernel writes is still read after it).
+        constexpr int kLines = D / 64;  // 128-byte lines per row of one KV head
+        for (int k = 0; k < a.prefetch_pages && k < my_pages; ++k) {  // (prefetch_pages <= 64)
+            const int page = __shfl_sync(0xffffffffu, k < 32 ? bt_cur : bt_nxt, k & 31);
+            const int valid = min(kPage, end - (p0 + pstep * (warp + kWarps * k)) * kPage);
+            if (static_cast<uint32_t>(page) < static_cast<uint64_t>(a.num_blocks)) {
+                for (int i = lane; i < valid * kLines; i += 32) {
+                    const int64_t off =
+                        ((static_cast<int64_t>(page) * kPage + i / kLines) * a.num_kv_heads + h) * D + (i % kLines) * 64;
+                    prefetch_l2(kc + off);
+                    prefetch_l2(vc + off);
+                }
+            }
+        }
+        grid_dependency_wait();
+    }
+    grid_launch_dependents();
 #pragma unroll
     for (int i = 0; i < kStages - 1; ++i) issue(i);
     // Q fragments for all D/16 k-steps (rows >= `rows` zero), loaded after the
