@@ -223,6 +223,13 @@ __device__ __forceinline__ void st_peer(float* local, uint32_t peer, float v) {
     asm volatile("mapa.shared::cluster.u32 %0, %1, %2;\n" : "=r"(remote) : "r"(addr), "r"(peer));
     asm volatile("st.shared::cluster.f32 [%0], %1;\n" ::"r"(remote), "f"(v) : "memory");
 }
+__device__ __forceinline__ void st_peer4(float* local, uint32_t peer, float4 v) {
+    uint32_t addr = smem_u32(local), remote;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;\n" : "=r"(remote) : "r"(addr), "r"(peer));
+    asm volatile("st.shared::cluster.v4.f32 [%0], {%1, %2, %3, %4};\n" ::"r"(remote), "f"(v.x), "f"(v.y), "f"(v.z),
+                 "f"(v.w)
+                 : "memory");
+}
 __device__ __forceinline__ void st_peer2(float* local, uint32_t peer, float x, float y) {
     uint32_t addr = smem_u32(local), remote;
     asm volatile("mapa.shared::cluster.u32 %0, %1, %2;\n" : "=r"(remote) : "r"(addr), "r"(peer));
@@ -598,10 +605,15 @@ __global__ void __launch_bounds__(kWarps * 32, (kWarps == 4 && D <= 128) ? 3 : 1
         }
         const float av[4] = {acc.x, acc.y, acc.z, acc.w};
         if (clustered) {
+            if (ccols % 4 == 0) {  // the 4 columns have one owner: one 16-byte push
+                const int own = d / ccols;
+                st_peer4(recv_o + (s * kRows + r) * ccols + (d - own * ccols), own, acc);
+            } else {
 #pragma unroll
-            for (int j = 0; j < 4; ++j) {
-                const int own = (d + j) / ccols;
-                st_peer(recv_o + (s * kRows + r) * ccols + (d + j - own * ccols), own, av[j]);
+                for (int j = 0; j < 4; ++j) {
+                    const int own = (d + j) / ccols;
+                    st_peer(recv_o + (s * kRows + r) * ccols + (d + j - own * ccols), own, av[j]);
+                }
             }
             if (d == 0) {
                 const float M = row_max(r), l = row_sum(r);
@@ -612,10 +624,10 @@ __global__ void __launch_bounds__(kWarps * 32, (kWarps == 4 && D <= 128) ? 3 : 1
             uint2 packed;
             packed.x = pack_bf16(av[0] * inv, av[1] * inv);
             packed.y = pack_bf16(av[2] * inv, av[3] * inv);
-            *reinterpret_cast<uint2*>(out + (static_cast<int64_t>(q0 + tok_of(r)) * a.num_q_heads + head_of(r)) * D +
+            *reinterpret_cast<uint2*>(out + (static_cast<int64_t>(q0 + s_tok[r]) * a.num_q_heads + s_head[r]) * D +
                                       d) = packed;
         } else {
-            const int64_t slot = partial_row(a, b, s, tok_of(r), head_of(r));
+            const int64_t slot = partial_row(a, b, s, s_tok[r], s_head[r]);
             *reinterpret_cast<float4*>(a.ws_o + slot * D + d) = acc;
             if (d == 0) *reinterpret_cast<float2*>(a.ws_ml + slot * 2) = make_float2(row_max(r), row_sum(r));
         }
@@ -630,27 +642,60 @@ __global__ void __launch_bounds__(kWarps * 32, (kWarps == 4 && D <= 128) ? 3 : 1
         cluster_sync();
         __shared__ float s_w[kMaxCluster][kRows], s_inv[kRows];
         if (threadIdx.x < rows) {
+            // (unrolled over the largest cluster, so that every load is in flight at once)
             const int r = threadIdx.x;
+            float2 ml[kMaxCluster];
+#pragma unroll
+            for (int c = 0; c < kMaxCluster; ++c)
+                ml[c] = c < C ? *reinterpret_cast<const float2*>(recv_ml + (c * kRows + r) * 2)
+                              : make_float2(-INFINITY, 0.f);
             float M = -INFINITY;
-            for (int c = 0; c < C; ++c) M = fmaxf(M, recv_ml[(c * kRows + r) * 2]);
+#pragma unroll
+            for (int c = 0; c < kMaxCluster; ++c) M = fmaxf(M, ml[c].x);
             float l = 0.f;
-            for (int c = 0; c < C; ++c) {
-                const float mc = recv_ml[(c * kRows + r) * 2];
-                const float w = mc == -INFINITY ? 0.f : fast_exp2(mc - M);
-                s_w[c][r] = w;
-                l += w * recv_ml[(c * kRows + r) * 2 + 1];
+#pragma unroll
+            for (int c = 0; c < kMaxCluster; ++c) {
+                const float w = ml[c].x == -INFINITY ? 0.f : fast_exp2(ml[c].x - M);
+                if (c < C) {
+                    s_w[c][r] = w;
+                    l += w * ml[c].y;
+                }
             }
             s_inv[r] = 1.f / l;
         }
         __syncthreads();
         const int d0 = s * ccols;
         const int ncols = max(0, min(ccols, D - d0));
-        for (int i = threadIdx.x; i < rows * ncols; i += blockDim.x) {
-            const int r = i / ncols, j = i % ncols;
-            float acc = 0.f;
-            for (int c = 0; c < C; ++c) acc += s_w[c][r] * recv_o[(c * kRows + r) * ccols + j];
-            out[(static_cast<int64_t>(q0 + tok_of(r)) * a.num_q_heads + head_of(r)) * D + d0 + j] =
-                __float2bfloat16(acc * s_inv[r]);
+        if (ccols % 4 == 0) {  // (then ncols is a multiple of 4 too)
+            const int q4 = ncols / 4;
+            for (int i = threadIdx.x; i < rows * q4; i += blockDim.x) {
+                const int r = i / q4, j = (i - r * q4) * 4;
+                float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+                for (int c = 0; c < kMaxCluster; ++c)
+                    if (c < C) {
+                        const float w = s_w[c][r];
+                        const float4 v = *reinterpret_cast<const float4*>(recv_o + (c * kRows + r) * ccols + j);
+                        acc.x += w * v.x;
+                        acc.y += w * v.y;
+                        acc.z += w * v.z;
+                        acc.w += w * v.w;
+                    }
+                const float inv = s_inv[r];
+                uint2 packed;
+                packed.x = pack_bf16(acc.x * inv, acc.y * inv);
+                packed.y = pack_bf16(acc.z * inv, acc.w * inv);
+                *reinterpret_cast<uint2*>(out + (static_cast<int64_t>(q0 + s_tok[r]) * a.num_q_heads + s_head[r]) * D +
+                                          d0 + j) = packed;
+            }
+        } else {
+            for (int i = threadIdx.x; i < rows * ncols; i += blockDim.x) {
+                const int r = i / ncols, j = i % ncols;
+                float acc = 0.f;
+                for (int c = 0; c < C; ++c) acc += s_w[c][r] * recv_o[(c * kRows + r) * ccols + j];
+                out[(static_cast<int64_t>(q0 + s_tok[r]) * a.num_q_heads + s_head[r]) * D + d0 + j] =
+                    __float2bfloat16(acc * s_inv[r]);
+            }
         }
         return;
     }
