@@ -334,7 +334,7 @@ __global__ void __launch_bounds__(kWarps * 32, (kWarps == 4 && D <= 128) ? 3 : 1
     auto tok_of = [&](int r) { return packed ? r / a.group : 0; };
     auto head_of = [&](int r) { return packed ? h * a.group + r % a.group : h * a.group + rg * kRows + r; };
     __shared__ int s_tok[kRows], s_head[kRows];
-    if (threadIdx.x < kRows) {  // for the workspace merge; read after later barriers
+    if (threadIdx.x < kRows) {  // for the merges below; read after later barriers
         s_tok[threadIdx.x] = tok_of(threadIdx.x);
         s_head[threadIdx.x] = head_of(threadIdx.x);
     }
