@@ -65,3 +65,46 @@ def test_random_case(seed):
     what = f"q_lens {q_lens} seq_lens {seq_lens} heads {Hq}/{Hkv} D {D} {opts}"
     assert_close(got, oracle.batch_attention(b), what)
     torch.cuda.synchronize()
+
+
+@pytest.mark.parametrize("seed", range(64))
+def test_random_batch_early_metadata(seed):
+    """pa_options.early_metadata on random batches: the output equals the default
+    call's bit for bit, and two calls captured back to back in a CUDA graph (the
+    second reading the first's output as its queries, so it may be scheduled
+    while the first still runs) equal the same two calls with a device
+    synchronisation between them."""
+    import paged_kv_cache_forward_gb300 as pa
+    q_lens, seq_lens, Hq, Hkv, D, opts = draw_case(seed + 50000)
+    b = W.make_batch(q_lens, seq_lens, Hq, Hkv, D, seed=seed + 50000)
+    d = b.to("cuda")
+    outs = []
+    for early in (0, 1):
+        out = torch.full_like(d.q, float("nan"))
+        pa.forward(d.q, d.k_cache, d.v_cache, d.block_table, d.seq_lens, d.query_start_loc, out, scale=b.scale,
+                   early_metadata=early, **opts)
+        torch.cuda.synchronize()
+        assert pa.device_error() == 0
+        outs.append(out)
+    assert torch.equal(outs[0].view(torch.int16), outs[1].view(torch.int16))
+    ref = torch.empty_like(d.q)
+    pa.forward(outs[0], d.k_cache, d.v_cache, d.block_table, d.seq_lens, d.query_start_loc, ref, scale=b.scale, **opts)
+    torch.cuda.synchronize()
+    s = torch.cuda.Stream()
+    pa.prepare(d.q, d.k_cache, d.block_table, d.seq_lens, stream=s, **opts)
+    torch.cuda.synchronize()
+    mid, fin = torch.empty_like(d.q), torch.empty_like(d.q)
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s):
+        pa.forward(d.q, d.k_cache, d.v_cache, d.block_table, d.seq_lens, d.query_start_loc, mid, scale=b.scale,
+                   stream=s, early_metadata=1, **opts)
+        pa.forward(mid, d.k_cache, d.v_cache, d.block_table, d.seq_lens, d.query_start_loc, fin, scale=b.scale,
+                   stream=s, early_metadata=1, **opts)
+    mid.fill_(float("nan"))
+    fin.fill_(float("nan"))
+    torch.cuda.synchronize()
+    with torch.cuda.stream(s):
+        g.replay()
+    s.synchronize()
+    assert pa.device_error(s) == 0
+    assert torch.equal(fin.view(torch.int16), ref.view(torch.int16))
