@@ -193,3 +193,24 @@ def test_early_metadata_option(lib):
             assert st == B.PA_OK and info.as_dict() == base
         else:
             assert st == B.PA_ERR_INVALID_ARG and lib.pa_last_error().decode()
+
+
+def test_wide_groups_take_the_second_table(lib):
+    """More than 16 query heads per KV head (several row groups reading the same
+    pages): the plan takes the kSplitTableWide cell the call falls in; 16 or fewer
+    take the first table."""
+    from paged_kv_cache_forward_gb300 import sweep as S
+    table = os.path.join(os.path.dirname(B.__file__), "csrc", "lut_gb300.inc")
+    wide, first = S.read_table(table, S.WIDE_NAME), S.read_table(table)
+    assert wide, "no wide-group rows"
+    for (d, bound, units), (chunk, st, w, cl) in sorted(wide.items())[:12]:
+        seqs = units // 2  # Hq 32 / Hkv 1: two row groups per sequence
+        p = B.plan(llama_dims(num_q_heads=32, num_kv_heads=1, head_dim=d, num_seqs=seqs, num_tokens=seqs,
+                              max_pages=bound // 16, num_blocks=seqs * bound // 16 + 1))
+        assert (p["decode_warps"], p["decode_stages"], p["decode_cluster"]) == (w, st, max(cl, 1)), (bound, units)
+        if cl <= 1:
+            assert p["kv_chunk"] == min(chunk, bound), (bound, units)
+    # 4 query heads per KV head, same decode units: the first table
+    (d, bound, units), (chunk, st, w, cl) = sorted(first.items())[0]
+    p = B.plan(llama_dims(num_q_heads=4 * units, num_kv_heads=units, head_dim=d, max_pages=bound // 16))
+    assert (p["decode_warps"], p["decode_stages"], p["decode_cluster"]) == (w, st, max(cl, 1))
