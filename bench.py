@@ -31,6 +31,10 @@ Per workload:
     at least 0.2 s after one untimed replay.
 L2: each step reads one of R identical copies of the KV pool in rotation, with
 R * (KV bytes per step) > 3 * L2, so no step finds its pages in L2.
+Every call passes pa_options.early_metadata (the metadata is the same for every
+step, so no kernel before a call writes it): a decode grid launched early reads
+its metadata and prefetches its first pages while the previous call finishes;
+--no-early-metadata measures without it.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--config NAME] [--impl reference]
 """
