@@ -146,8 +146,11 @@ typedef struct {
     /* 1: the caller guarantees that block_table, seq_lens and query_start_loc
        are not written by the kernel immediately before this call on the stream
        (as in the attention layers of one decode step, which share the
-       metadata; work enqueued earlier than that kernel, host copies included,
-       is always finished by then).  A decode kernel launched with programmatic
+       metadata).  Work enqueued before that kernel, host copies included, is
+       finished by then if that kernel lets its successor be scheduled only
+       after its own wait for its predecessor, as this library's kernels do; a
+       kernel that does not use programmatic dependent launch lets it be
+       scheduled only when it completes.  A decode kernel launched with programmatic
        dependent launch (see "Streams and graphs") then loads its metadata and
        block-table entries, and prefetches the first KV pages of each warp into
        L2, while that kernel is still finishing; q, the KV values it computes
