@@ -40,7 +40,17 @@
  * Pointers.  Every data pointer is a DEVICE pointer on the current CUDA device
  * (the one the stream belongs to).  q, k_cache, v_cache and out must be 16-byte
  * aligned; the int32 arrays 4-byte aligned.  The caller owns all of them; the
- * library keeps none after a call returns.
+ * library keeps none after a call returns.  One exception: when the dims allow
+ * no prefill rows (pa_plan_info.prefill_ctas == 0), q, block_table, seq_lens,
+ * query_start_loc and out may be pinned host memory that the device can address
+ * (cudaHostAlloc / cudaHostRegister under unified addressing; a PyTorch
+ * pin_memory tensor), because the decode kernel reads them and writes out with
+ * plain loads and stores, which then cross the host link (NVLink-C2C on a
+ * Grace-Blackwell node): a decode step with host inputs and outputs needs no
+ * copies.  k_cache and v_cache are always device memory.  When the dims allow
+ * prefill rows, q must be device (or managed) memory, since the prefill kernel
+ * reads it with tensor copies; pa_forward and pa_forward_noalloc check this
+ * (one pointer query, made only then) and return PA_ERR_INVALID_ARG otherwise.
  *
  * Streams and graphs.  Every call is asynchronous on the given stream
  * (a cudaStream_t passed as void*; NULL is the legacy default stream).  No call

@@ -1,9 +1,11 @@
 """ctypes binding of libpagedattn (include/pagedattn.h): argument marshalling only.
 
 Every step of the attention runs in the library's CUDA kernels.  Tensors are
-PyTorch CUDA tensors (PyTorch provides the device memory and the stream); this
-module checks dtypes, shapes and contiguity, fills a ``pa_dims`` and passes raw
-pointers.  There is no fallback: if the library is missing, or a call fails,
+PyTorch CUDA tensors (PyTorch provides the device memory and the stream); q, the
+metadata and out may also be pinned host tensors, which the decode kernel reads
+and writes in place (the library rejects a host q when the shapes allow prefill
+rows).  This module checks dtypes, shapes and contiguity, fills a ``pa_dims``
+and passes raw pointers.  There is no fallback: if the library is missing, or a call fails,
 an exception is raised.
 """
 
@@ -162,6 +164,17 @@ def make_dims(q_shape, k_shape, bt_shape, num_seqs) -> Dims:
                 head_dim=D, page_size=P, max_pages=max_pages)
 
 
+# Arguments the decode kernel reads (or writes) with plain loads and stores, so
+# they may also be pinned host memory (pa_forward's pointer rules: decode-only
+# dims for q).
+_HOST_OK = ("q", "block_table", "seq_lens", "query_start_loc", "out")
+
+
+def _out_like(q):
+    # out where q is: on the device, or in pinned host memory
+    return torch.empty_like(q) if q.is_cuda else torch.empty(q.shape, dtype=q.dtype, pin_memory=True)
+
+
 def _check_tensors(q, k_cache, v_cache, block_table, seq_lens, query_start_loc, out):
     for name, t, dt, nd in (("q", q, torch.bfloat16, 3), ("k_cache", k_cache, torch.bfloat16, 4),
                             ("v_cache", v_cache, torch.bfloat16, 4), ("block_table", block_table, torch.int32, 2),
@@ -173,8 +186,9 @@ def _check_tensors(q, k_cache, v_cache, block_table, seq_lens, query_start_loc, 
             raise ValueError(f"{name} must have {nd} dims, got {tuple(t.shape)}")
         if not t.is_contiguous():
             raise ValueError(f"{name} must be contiguous")
-        if not t.is_cuda:
-            raise ValueError(f"{name} must be a CUDA tensor")
+        if not t.is_cuda and not (name in _HOST_OK and t.is_pinned()):
+            raise ValueError(f"{name} must be a CUDA tensor" +
+                             (" or a pinned host tensor" if name in _HOST_OK else ""))
     if k_cache.shape != v_cache.shape:
         raise ValueError("k_cache and v_cache shapes differ")
     if out.shape != q.shape:
@@ -219,7 +233,7 @@ def forward(q, k_cache, v_cache, block_table, seq_lens, query_start_loc, out=Non
     just before the call (pa_options).
     """
     if out is None:
-        out = torch.empty_like(q)
+        out = _out_like(q)
     _check_tensors(q, k_cache, v_cache, block_table, seq_lens, query_start_loc, out)
     if scale is None:
         scale = 1.0 / math.sqrt(q.shape[-1])
@@ -245,7 +259,7 @@ def forward_noalloc(q, k_cache, v_cache, block_table, seq_lens, query_start_loc,
     ``device_error`` (optional) is a CUDA int32 tensor of one element that
     receives the first device-side error code; the caller zeroes it."""
     if out is None:
-        out = torch.empty_like(q)
+        out = _out_like(q)
     _check_tensors(q, k_cache, v_cache, block_table, seq_lens, query_start_loc, out)
     if device_error is not None and (device_error.dtype != torch.int32 or not device_error.is_cuda):
         raise TypeError("device_error must be a CUDA int32 tensor")

@@ -324,6 +324,24 @@ pa_status record(void* ev, cudaStream_t s, bool capturing) {
 namespace pa {
 // Lets other translation units of the library report through pa_last_error().
 void set_last_error(const char* msg) { snprintf(g_last_error, sizeof g_last_error, "%s", msg); }
+
+// True if p is device (or managed) memory of the CUDA driver, false for host
+// memory, mapped or not.  The prefill kernel reads q with tensor copies and needs
+// the former; the decode kernel reads q and the metadata and writes out with
+// plain loads and stores, which reach pinned host memory as well.
+bool device_resident(const void* p) {
+    // (a query, not stream work: allowed inside a capture in any capture mode)
+    cudaStreamCaptureMode mode = cudaStreamCaptureModeRelaxed;
+    cudaThreadExchangeStreamCaptureMode(&mode);
+    cudaPointerAttributes at{};
+    const cudaError_t e = cudaPointerGetAttributes(&at, p);
+    cudaThreadExchangeStreamCaptureMode(&mode);
+    if (e != cudaSuccess) {
+        cudaGetLastError();  // (the query's error is not sticky; clear it)
+        return false;
+    }
+    return at.type == cudaMemoryTypeDevice || at.type == cudaMemoryTypeManaged;
+}
 }  // namespace pa
 
 extern "C" {
@@ -373,6 +391,8 @@ pa_status pa_forward_ex(const void* q, const void* k_cache, const void* v_cache,
     st = check_pointers(q, k_cache, v_cache, block_table, seq_lens, query_start_loc, out);
     if (st != PA_OK) return st;
     if (!(scale == scale)) return fail(PA_ERR_INVALID_ARG, "scale is NaN");
+    if (p.prefill_ctas > 0 && !pa::device_resident(q))
+        return fail(PA_ERR_INVALID_ARG, "q must be device memory when the dims allow prefill rows");
 
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;

@@ -35,6 +35,11 @@
 #include "pa_internal.h"
 #include "pagedattn.h"
 
+namespace pa {
+// (api.cpp) True if p is device or managed memory, false for host memory.
+bool device_resident(const void* p);
+}  // namespace pa
+
 namespace {
 
 constexpr int64_t kNoAllocScratchBytes = 32ll << 20;
@@ -99,6 +104,8 @@ extern "C" pa_status pa_forward_noalloc(const void* q, const void* k_cache, cons
         !aligned(device_error, 4))
         return report(PA_ERR_INVALID_ARG, "int32 arguments must be 4-byte aligned");
     if (!(scale == scale)) return report(PA_ERR_INVALID_ARG, "scale is NaN");
+    if (info.prefill_ctas > 0 && !pa::device_resident(q))
+        return report(PA_ERR_INVALID_ARG, "q must be device memory when the dims allow prefill rows");
 
     void* scratch = nullptr;
     if ((st = scratch_address(&scratch)) != PA_OK) return st;

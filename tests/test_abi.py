@@ -214,3 +214,23 @@ def test_wide_groups_take_the_second_table(lib):
     (d, bound, units), (chunk, st, w, cl) = sorted(first.items())[0]
     p = B.plan(llama_dims(num_q_heads=4 * units, num_kv_heads=units, head_dim=d, max_pages=bound // 16))
     assert (p["decode_warps"], p["decode_stages"], p["decode_cluster"]) == (w, st, max(cl, 1))
+
+
+def test_binding_host_tensor_rules(monkeypatch):
+    """Host tensors: q, the metadata and out may be pinned host memory (the
+    library checks q against the shapes); the caches must be on the device; a
+    pageable host tensor is refused before the library is called."""
+    import torch
+
+    q = torch.zeros(2, 4, 64, dtype=torch.bfloat16)
+    kv = torch.zeros(3, 16, 1, 64, dtype=torch.bfloat16)
+    bt = torch.zeros(2, 1, dtype=torch.int32)
+    sl = torch.ones(2, dtype=torch.int32)
+    qsl = torch.arange(3, dtype=torch.int32)
+    assert set(B._HOST_OK) == {"q", "block_table", "seq_lens", "query_start_loc", "out"}
+    with pytest.raises(ValueError, match="q must be a CUDA tensor or a pinned host tensor"):
+        B._check_tensors(q, kv, kv, bt, sl, qsl, q)
+    # every host tensor taken as pinned: the first refusal is the KV cache's
+    monkeypatch.setattr(torch.Tensor, "is_pinned", lambda self: True)
+    with pytest.raises(ValueError, match="k_cache must be a CUDA tensor$"):
+        B._check_tensors(q, kv, kv, bt, sl, qsl, q)
