@@ -5,8 +5,8 @@ PyTorch CUDA tensors (PyTorch provides the device memory and the stream); q, the
 metadata and out may also be pinned host tensors, which the decode kernel reads
 and writes in place (the library rejects a host q when the shapes allow prefill
 rows).  This module checks dtypes, shapes and contiguity, fills a ``pa_dims``
-and passes raw pointers.  There is no fallback: if the library is missing, or a call fails,
-an exception is raised.
+and passes raw pointers.  There is no fallback: if the library is missing, or a
+call fails, an exception is raised.
 """
 
 from __future__ import annotations
